@@ -1,0 +1,160 @@
+"""CPU oracle for block-quantized mul_mat -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package. It never touches a GPU, shares no code with the CUDA library and
+imports nothing from it. The arithmetic lives in ``gq_oracle.c`` (plain C, fp64
+accumulation, single thread); this module only marshals numpy arrays into it.
+
+Every function follows the pages as cited in ``gq_oracle.c``:
+  - quantize: "A Complete Guide to llama.cpp and Customization with C++", section 2.2
+    (Delta = max |w| / 7, codes in [-8, 7]) and the Q4_0 layout of "Development Guide for
+    Small AI Models (TinyLLaMA, etc.) Using C++", section 6.1 (fp16 scale + 16 code bytes).
+  - dequantize / mul_mat: "Development Guide ...", section 6.2 (load, unpack, dequantize,
+    FMA) and "No Python! Building an AI Inference Engine Exclusively in C++", sections 6
+    and 7.2 (C = A B; Y = X W^T in the cuBLAS call's layout).
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` (IEEE fp16
+conversion against numpy, closed-form blocks, exact-rational brute force, one-hot rows).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+TYPE_Q4_0 = 2
+TYPE_Q8_0 = 8
+_TYPES = {"q4_0": TYPE_Q4_0, "q8_0": TYPE_Q8_0, TYPE_Q4_0: TYPE_Q4_0, TYPE_Q8_0: TYPE_Q8_0}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gq_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+# IEEE arithmetic only: no fast-math, no contraction of a*b+c into fma.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile gq_oracle.c into liboracle.so next to it (gcc, a second or two)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        # GQ_ORACLE_SO names another build of gq_oracle.c; the mutation test uses it to
+        # run the pins against copies with a mistake planted in them.
+        lib = ctypes.CDLL(os.environ.get("GQ_ORACLE_SO") or build())
+        c_int64, c_int, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.oracle_fp16_from_f32.argtypes = [ctypes.c_float]
+        lib.oracle_fp16_from_f32.restype = ctypes.c_uint16
+        lib.oracle_f32_from_fp16.argtypes = [ctypes.c_uint16]
+        lib.oracle_f32_from_fp16.restype = ctypes.c_float
+        lib.oracle_fp16_from_f32_array.argtypes = [vp, c_int64, vp]
+        lib.oracle_fp16_from_f32_array.restype = None
+        lib.oracle_f32_from_fp16_array.argtypes = [vp, c_int64, vp]
+        lib.oracle_f32_from_fp16_array.restype = None
+        lib.oracle_block_bytes.argtypes = [c_int]
+        lib.oracle_block_bytes.restype = c_int64
+        lib.oracle_quantize.argtypes = [c_int, vp, c_int64, c_int64, vp]
+        lib.oracle_quantize.restype = c_int
+        lib.oracle_dequantize.argtypes = [c_int, vp, c_int64, c_int64, vp]
+        lib.oracle_dequantize.restype = c_int
+        lib.oracle_mul_mat.argtypes = [c_int, vp, c_int64, c_int64, vp, c_int64, vp, vp]
+        lib.oracle_mul_mat.restype = c_int
+        _lib = lib
+    return _lib
+
+
+def _type(t) -> int:
+    try:
+        return _TYPES[t]
+    except KeyError:
+        raise ValueError(f"unknown block type {t!r}") from None
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def block_bytes(t) -> int:
+    """Bytes per 32-weight block: 18 for Q4_0, 34 for Q8_0."""
+    return int(_load().oracle_block_bytes(_type(t)))
+
+
+def row_bytes(t, K: int) -> int:
+    return (K // 32) * block_bytes(t)
+
+
+def fp16_from_f32(x) -> np.ndarray:
+    """IEEE binary32 -> binary16 bit patterns (uint16), round to nearest even."""
+    x = _f32(x)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_fp16_from_f32_array(x.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+def f32_from_fp16(h) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    _load().oracle_f32_from_fp16_array(h.ctypes.data, h.size, out.ctypes.data)
+    return out
+
+
+def quantize(t, W) -> np.ndarray:
+    """W (M x K fp32) -> uint8 array of shape (M, K/32 * block_bytes)."""
+    W = _f32(W)
+    M, K = W.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    out = np.empty((M, row_bytes(t, K)), dtype=np.uint8)
+    rc = _load().oracle_quantize(_type(t), W.ctypes.data, M, K, out.ctypes.data)
+    if rc:
+        raise ValueError("oracle_quantize rejected its arguments")
+    return out
+
+
+def dequantize(t, blocks, M: int, K: int) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    if blocks.size != M * row_bytes(t, K):
+        raise ValueError("block buffer size does not match M, K")
+    out = np.empty((M, K), dtype=np.float32)
+    rc = _load().oracle_dequantize(_type(t), blocks.ctypes.data, M, K, out.ctypes.data)
+    if rc:
+        raise ValueError("oracle_dequantize rejected its arguments")
+    return out
+
+
+def mul_mat(t, blocks, M: int, K: int, X) -> np.ndarray:
+    """Y (N x M fp32) = X (N x K fp32) . What^T, accumulated in fp64 on one CPU thread."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    X = _f32(X)
+    if X.ndim == 1:
+        X = X.reshape(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K or blocks.size != M * row_bytes(t, K):
+        raise ValueError("shape mismatch")
+    Y = np.empty((N, M), dtype=np.float32)
+    wrow = np.empty(max(K, 1), dtype=np.float32)
+    rc = _load().oracle_mul_mat(_type(t), blocks.ctypes.data, M, K, X.ctypes.data, N,
+                                Y.ctypes.data, wrow.ctypes.data)
+    if rc:
+        raise ValueError("oracle_mul_mat rejected its arguments")
+    return Y
+
+
+def mul_mat_rows(t, blocks, M: int, K: int, X, rows) -> np.ndarray:
+    """Y[:, rows] only: the oracle run on the selected rows' blocks (row-major, so each
+    row is one contiguous byte range). Used to check sampled outputs of large problems."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(M, row_bytes(t, K))
+    rows = np.asarray(rows, dtype=np.int64)
+    sub = np.ascontiguousarray(blocks[rows])
+    return mul_mat(t, sub, len(rows), K, X)

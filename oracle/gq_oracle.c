@@ -1,0 +1,261 @@
+/*
+ * gq_oracle.c -- plain, slow, single-threaded CPU oracle for block-quantized mul_mat.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may include, link or call this
+ * file; only the tests, the package smoke check and the benchmark's CPU-baseline leg do.
+ * It shares no code, header, table or constant with the CUDA library: the two meet only
+ * in the seeded input generators.
+ *
+ * What it computes, and where the pages say so:
+ *   - Q4_0 block layout: one fp16 scale (2 bytes) followed by 32 4-bit codes (16 bytes),
+ *     i.e. 18 bytes per 32 weights ("Development Guide for Small AI Models (TinyLLaMA,
+ *     etc.) Using C++", section 6.1).
+ *   - Block quantization w_i ~= Delta * q_i with Delta = max_i |w_i| / 7 and 4-bit codes
+ *     q_i in [-8, 7] ("A Complete Guide to llama.cpp and Customization with C++",
+ *     section 2.2, the two displayed formulas for w_i and Delta). Stored codes carry an
+ *     offset of +8 so that they fit an unsigned nibble.
+ *   - Q8_0: the pages name 8-bit quantization ("No Python! Building an AI Inference
+ *     Engine Exclusively in C++", section 9; "A Complete Guide ...", section 1.1) but lay
+ *     out no 8-bit block. This oracle takes the 4-bit rule with signed 8-bit codes:
+ *     Delta = max |w| / 127, code = round(w / Delta) in [-127, 127], same fp16 scale.
+ *   - Dequantize right after the load, then multiply-accumulate with fp32 activations
+ *     ("Development Guide ...", section 6.2, the load / unpack / dequantize / FMA flow;
+ *     "No Python! ...", section 9).
+ *   - The product itself: C_ij = sum_k A_ik B_kj ("No Python! ...", section 6), realised
+ *     as Y[n][m] = sum_k What[m][k] * X[n][k] -- the layout of the cuBLAS call in
+ *     section 7.2 of the same article (W is M x K row-major, X is N x K row-major,
+ *     Y is N x M row-major).
+ *
+ * Readings where the pages are silent (each is also listed in the design notes):
+ *   - round() is C roundf: halves go away from zero.
+ *   - the code is computed from the fp32 quotient w / d, with d = amax / 7 in fp32; the
+ *     fp16 copy of d is what is stored and what dequantization uses.
+ *   - an all-zero block stores d = +0 and the zero-point code (8 for Q4_0, 0 for Q8_0).
+ *   - nibble order: byte j holds element j in its low nibble and element j + 16 in its
+ *     high nibble.
+ *   - fp32 -> fp16 is IEEE 754 round-to-nearest-even with subnormals kept and overflow to
+ *     infinity, written here from the IEEE 754 binary16 definition.
+ *   - accumulation is in fp64 in increasing k, rounded once to fp32 at the end.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (never -ffast-math: the
+ * quantizer must be bit-exact IEEE division and rounding).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_TYPE_Q4_0 2
+#define ORACLE_TYPE_Q8_0 8
+
+/* ---------------------------------------------------------------------------------- */
+/* IEEE 754 binary32 -> binary16, round to nearest, ties to even.                      */
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. Normal numbers   */
+/* cover 2^-14 .. 65504, subnormals are m * 2^-24 for m in 1..1023.                    */
+/* ---------------------------------------------------------------------------------- */
+uint16_t oracle_fp16_from_f32(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    const uint32_t biased = (x >> 23) & 0xFFu;
+    const uint32_t frac = x & 0x7FFFFFu;
+
+    if (biased == 0xFFu) {                       /* infinity or NaN */
+        if (frac == 0) return (uint16_t)(sign | 0x7C00u);
+        return (uint16_t)(sign | 0x7E00u | (frac >> 13));   /* quiet NaN */
+    }
+    if (biased == 0) return sign;                /* |f| < 2^-126: far below 2^-25 */
+
+    const int e = (int)biased - 127;             /* f = sig * 2^(e - 23) */
+    const uint32_t sig = frac | 0x800000u;       /* 24-bit significand */
+
+    if (e > 15) return (uint16_t)(sign | 0x7C00u);           /* >= 2^16: overflow */
+
+    if (e >= -14) {                              /* binary16 normal range */
+        uint32_t h = sig >> 13;                  /* keep 11 bits */
+        const uint32_t rest = sig & 0x1FFFu;     /* 13 dropped bits */
+        if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;
+        uint32_t hexp = (uint32_t)(e + 15);
+        if (h == 0x800u) { h = 0x400u; hexp += 1u; }         /* carry into exponent */
+        if (hexp >= 31u) return (uint16_t)(sign | 0x7C00u);
+        return (uint16_t)(sign | (hexp << 10) | (h & 0x3FFu));
+    }
+
+    /* binary16 subnormal: value = m * 2^-24 with m = sig * 2^(e + 1) */
+    const int drop = -(e + 1);                   /* >= 14 */
+    if (drop > 24) return sign;                  /* below 2^-25: rounds to zero */
+    uint32_t m = sig >> drop;
+    const uint32_t rest = sig & ((1u << drop) - 1u);
+    const uint32_t half = 1u << (drop - 1);
+    if (rest > half || (rest == half && (m & 1u))) m += 1u;
+    return (uint16_t)(sign | m);                 /* m == 1024 is the smallest normal */
+}
+
+float oracle_f32_from_fp16(uint16_t h)
+{
+    const int negative = (h & 0x8000u) != 0;
+    const int biased = (h >> 10) & 0x1F;
+    const int frac = h & 0x3FF;
+    double v;
+    if (biased == 0) {
+        v = ldexp((double)frac, -24);
+    } else if (biased == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), biased - 25);
+    }
+    return (float)(negative ? -v : v);
+}
+
+/* Element-wise loops over the two conversions, so that tests can sweep every pattern. */
+void oracle_fp16_from_f32_array(const float* x, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp16_from_f32(x[i]);
+}
+
+void oracle_f32_from_fp16_array(const uint16_t* h, int64_t n, float* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_from_fp16(h[i]);
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* Quantization, one 32-element block at a time, blocks in row-major order.           */
+/* ---------------------------------------------------------------------------------- */
+static float block_absmax(const float* w)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+        const float a = fabsf(w[i]);
+        if (a > amax) amax = a;
+    }
+    return amax;
+}
+
+static void put_u16_le(uint8_t* p, uint16_t v)
+{
+    p[0] = (uint8_t)(v & 0xFFu);
+    p[1] = (uint8_t)(v >> 8);
+}
+
+static uint16_t get_u16_le(const uint8_t* p)
+{
+    return (uint16_t)(p[0] | (p[1] << 8));
+}
+
+/* Q4_0 block: Delta = amax / 7, code = clamp(round(w / Delta) + 8, 0, 15). */
+static void quantize_block_q4_0(const float* w, uint8_t* out)
+{
+    const float amax = block_absmax(w);
+    const float d = amax / 7.0f;
+    int code[32];
+    for (int i = 0; i < 32; ++i) {
+        if (d == 0.0f) {
+            code[i] = 8;
+        } else {
+            int c = (int)roundf(w[i] / d) + 8;
+            if (c < 0) c = 0;
+            if (c > 15) c = 15;
+            code[i] = c;
+        }
+    }
+    put_u16_le(out, oracle_fp16_from_f32(d));
+    for (int j = 0; j < 16; ++j)
+        out[2 + j] = (uint8_t)(code[j] | (code[j + 16] << 4));
+}
+
+/* Q8_0 block: Delta = amax / 127, code = clamp(round(w / Delta), -127, 127). */
+static void quantize_block_q8_0(const float* w, uint8_t* out)
+{
+    const float amax = block_absmax(w);
+    const float d = amax / 127.0f;
+    put_u16_le(out, oracle_fp16_from_f32(d));
+    for (int i = 0; i < 32; ++i) {
+        int c = 0;
+        if (d != 0.0f) {
+            c = (int)roundf(w[i] / d);
+            if (c < -127) c = -127;
+            if (c > 127) c = 127;
+        }
+        out[2 + i] = (uint8_t)(int8_t)c;
+    }
+}
+
+int64_t oracle_block_bytes(int type)
+{
+    if (type == ORACLE_TYPE_Q4_0) return 2 + 16;
+    if (type == ORACLE_TYPE_Q8_0) return 2 + 32;
+    return -1;
+}
+
+/* W: M x K fp32 row-major, K a multiple of 32. out: M * K/32 blocks, row-major. */
+int oracle_quantize(int type, const float* W, int64_t M, int64_t K, uint8_t* out)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0) return -1;
+    const int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* w = W + m * K + b * 32;
+            uint8_t* o = out + (m * nb + b) * bb;
+            if (type == ORACLE_TYPE_Q4_0) quantize_block_q4_0(w, o);
+            else quantize_block_q8_0(w, o);
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* Dequantization: What = (code - 8) * Delta (Q4_0) or code * Delta (Q8_0).            */
+/* Both products are exact in fp32 (at most 8 + 11 significant bits).                 */
+/* ---------------------------------------------------------------------------------- */
+static void dequantize_block(int type, const uint8_t* blk, float* w)
+{
+    const float d = oracle_f32_from_fp16(get_u16_le(blk));
+    if (type == ORACLE_TYPE_Q4_0) {
+        for (int j = 0; j < 16; ++j) {
+            const int lo = blk[2 + j] & 0x0F;
+            const int hi = blk[2 + j] >> 4;
+            w[j] = (float)(lo - 8) * d;
+            w[j + 16] = (float)(hi - 8) * d;
+        }
+    } else {
+        for (int i = 0; i < 32; ++i)
+            w[i] = (float)(int8_t)blk[2 + i] * d;
+    }
+}
+
+int oracle_dequantize(int type, const uint8_t* blocks, int64_t M, int64_t K, float* out)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0) return -1;
+    const int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < nb; ++b)
+            dequantize_block(type, blocks + (m * nb + b) * bb, out + m * K + b * 32);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* mul_mat: Y[n][m] = (float) sum_k (double) What[m][k] * (double) X[n][k].           */
+/* Each product is exact in fp64; the sum runs over k in increasing order and is      */
+/* rounded to fp32 once. `wrow` is caller-provided space for one dequantized row (K). */
+/* ---------------------------------------------------------------------------------- */
+int oracle_mul_mat(int type, const uint8_t* blocks, int64_t M, int64_t K,
+                   const float* X, int64_t N, float* Y, float* wrow)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0 || N < 0) return -1;
+    const int64_t nb = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < nb; ++b)
+            dequantize_block(type, blocks + (m * nb + b) * bb, wrow + b * 32);
+        for (int64_t n = 0; n < N; ++n) {
+            const float* x = X + n * K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)wrow[k] * (double)x[k];
+            Y[n * M + m] = (float)acc;
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,54 @@
+"""The pins must be strong enough to catch a plausible mistake anywhere in the oracle.
+
+Each case copies gq_oracle.c, plants one mistake (a wrong constant, sign, index, rounding
+rule or a dropped term), compiles the copy on the CPU and runs the pin suite against it
+in a child process: the suite has to fail. The oracle itself is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "gq_oracle.c")
+
+MUTANTS = {
+    "scale_divisor": ("const float d = amax / 7.0f;", "const float d = amax / 8.0f;"),
+    "code_offset": ("int c = (int)roundf(w[i] / d) + 8;", "int c = (int)roundf(w[i] / d) + 7;"),
+    "nibble_order": ("(uint8_t)(code[j] | (code[j + 16] << 4))",
+                     "(uint8_t)(code[j + 16] | (code[j] << 4))"),
+    "ties_to_even": ("int c = (int)roundf(w[i] / d) + 8;", "int c = (int)rintf(w[i] / d) + 8;"),
+    "q8_ties_to_even": ("c = (int)roundf(w[i] / d);", "c = (int)rintf(w[i] / d);"),
+    "dequant_sign": ("w[j] = (float)(lo - 8) * d;", "w[j] = (float)(8 - lo) * d;"),
+    "dequant_high_nibble": ("w[j + 16] = (float)(hi - 8) * d;", "w[j + 16] = (float)(hi - 7) * d;"),
+    "dropped_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k + 1 < K; ++k)"),
+    "transposed_x": ("acc += (double)wrow[k] * (double)x[k];",
+                     "acc += (double)wrow[k] * (double)X[k * N + n];"),
+    "transposed_y": ("Y[n * M + m] = (float)acc;", "Y[m * N + n] = (float)acc;"),
+    "fp32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
+    "fp16_ties_away": ("if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;",
+                       "if (rest >= 0x1000u) h += 1u;"),
+    "fp16_flush_subnormal": ("if (drop > 24) return sign;", "if (drop > 13) return sign;"),
+    "fp16_truncate": ("if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;", ""),
+    "q8_scale_divisor": ("const float d = amax / 127.0f;", "const float d = amax / 128.0f;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(before, after, 1)
+    c_path = tmp_path / "mutant.c"
+    so_path = tmp_path / "mutant.so"
+    c_path.write_text(mutated)
+    import oracle
+    subprocess.check_call(["gcc", *oracle.CFLAGS, str(c_path), "-o", str(so_path), "-lm"])
+    env = dict(os.environ, GQ_ORACLE_SO=str(so_path))
+    r = subprocess.run(
+        [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
