@@ -1,0 +1,164 @@
+"""Python face of libgq (include/gq.h): argument marshalling only.
+
+Every call passes device pointers and sizes straight to the C ABI on torch's current
+CUDA stream; all arithmetic runs in the library's sm_103a kernels. There is no CPU path:
+importing this module fails loudly if libgq.so has not been built, and the calls refuse
+CPU tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libgq.so not found at {LIB_PATH}: build it first "
+        "(python -m block_quantized_matmul_gq_gb300.build); there is no fallback path")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+Q4_0 = 2
+Q8_0 = 8
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, Q4_0: Q4_0, Q8_0: Q8_0}
+MAX_BATCH = 256
+
+STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
+          -4: "GQ_ERR_ALIGN", -5: "GQ_ERR_CUDA", -6: "GQ_ERR_TIMEOUT"}
+
+# Every symbol declared in include/gq.h.
+EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
+           "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_batched",
+           "gq_get_last_error", "gq_status_string")
+
+
+class Problem(ctypes.Structure):
+    """gq_mul_mat_problem."""
+    _fields_ = [("W_blocks", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_i64, _i32, _vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+lib.gq_abi_version.argtypes, lib.gq_abi_version.restype = [], _i32
+lib.gq_block_bytes.argtypes, lib.gq_block_bytes.restype = [ctypes.c_int], ctypes.c_size_t
+lib.gq_row_bytes.argtypes, lib.gq_row_bytes.restype = [ctypes.c_int, _i64], ctypes.c_size_t
+for _q in (lib.gq_quantize_q4_0, lib.gq_quantize_q8_0):
+    _q.argtypes, _q.restype = [_vp, _i64, _i64, _vp, _vp], ctypes.c_int
+lib.gq_dequantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _vp]
+lib.gq_dequantize.restype = ctypes.c_int
+lib.gq_mul_mat.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _i64, _vp, _vp]
+lib.gq_mul_mat.restype = ctypes.c_int
+lib.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), _i32, ctypes.c_int, _i64, _vp]
+lib.gq_mul_mat_batched.restype = ctypes.c_int
+lib.gq_get_last_error.argtypes, lib.gq_get_last_error.restype = [_vp], ctypes.c_int
+lib.gq_status_string.argtypes, lib.gq_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+
+
+class GQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = lib.gq_status_string(status).decode()
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({msg})")
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise GQError(status, what)
+
+
+def _type(t) -> int:
+    try:
+        return TYPES[t]
+    except KeyError:
+        raise ValueError(f"unknown block type {t!r}") from None
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libgq has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def block_bytes(t) -> int:
+    return int(lib.gq_block_bytes(_type(t)))
+
+
+def row_bytes(t, K: int) -> int:
+    return int(lib.gq_row_bytes(_type(t), K))
+
+
+def quantize(W: torch.Tensor, t, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 (M, K) CUDA tensor -> uint8 (M, row_bytes) blocks."""
+    M, K = W.shape
+    if out is None:
+        out = torch.empty((M, row_bytes(t, K) if K % 32 == 0 else 0), dtype=torch.uint8,
+                          device=W.device)
+    fn = lib.gq_quantize_q4_0 if _type(t) == Q4_0 else lib.gq_quantize_q8_0
+    _check(fn(_dev(W, torch.float32, "W"), M, K, _dev(out, torch.uint8, "W_blocks"),
+              _stream(stream)), "gq_quantize")
+    return out
+
+
+def dequantize(blocks: torch.Tensor, t, M: int, K: int, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.float32, device=blocks.device)
+    _check(lib.gq_dequantize(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
+                             _dev(out, torch.float32, "W_out"), _stream(stream)),
+           "gq_dequantize")
+    return out
+
+
+def mul_mat(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y (N, M) = X (N, K) . What^T."""
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K:
+        raise ValueError("X must be (N, K)")
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    _check(lib.gq_mul_mat(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
+                          _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
+                          _stream(stream)), "gq_mul_mat")
+    return out
+
+
+def make_problems(items) -> ctypes.Array:
+    """items: iterable of (blocks, M, K, X, Y) CUDA tensors -> a gq_mul_mat_problem array
+    that can be handed to mul_mat_batched repeatedly (e.g. while capturing a graph)."""
+    items = list(items)
+    arr = (Problem * max(1, len(items)))()
+    for i, (blocks, M, K, X, Y) in enumerate(items):
+        arr[i] = Problem(_dev(blocks, torch.uint8, "W_blocks"), _dev(X, torch.float32, "X"),
+                         _dev(Y, torch.float32, "Y"), M, K)
+    arr._count = len(items)
+    return arr
+
+
+def mul_mat_batched(problems, t, N: int, stream=None) -> None:
+    """Independent problems sharing type and N, in one launch. `problems` is the result
+    of make_problems() or an iterable of (blocks, M, K, X, Y)."""
+    if not isinstance(problems, ctypes.Array):
+        problems = make_problems(problems)
+    _check(lib.gq_mul_mat_batched(problems, problems._count, _type(t), N, _stream(stream)),
+           "gq_mul_mat_batched")
+
+
+def get_last_error(stream=None) -> int:
+    """Synchronizes the stream; returns the device-side status (0, or -6 for a timeout)."""
+    return int(lib.gq_get_last_error(_stream(stream)))

@@ -1,0 +1,194 @@
+// gq_capi.cu -- the extern "C" entry points of include/gq.h: host-side argument checks,
+// dispatch to the kernels, and the per-device status word that kernels set when a
+// bounded wait runs out.
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+#include "gq_device.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+
+// Set by kernels (atomicOr) when a device-side wait gives up; read and cleared by
+// gq_get_last_error. Host code reaches it only through cudaGetSymbolAddress.
+__device__ unsigned g_status_word;
+
+cudaError_t current_device_info(DeviceInfo** out) {
+    static std::mutex mu;
+    static DeviceInfo infos[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = infos[dev];
+    if (d.device < 0) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&d.max_smem_optin,
+                                       cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        void* p = nullptr;
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return e;
+        d.status = static_cast<unsigned*>(p);
+        d.device = dev;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+}  // namespace gq
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+bool known_type(gq_type t) { return t == GQ_TYPE_Q4_0 || t == GQ_TYPE_Q8_0; }
+
+gq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GQ_OK : GQ_ERR_CUDA; }
+
+// Shapes: non-negative, K a multiple of 32, every dimension and product in range.
+gq_status check_shape(int64_t M, int64_t K, int64_t N) {
+    if (M < 0 || K < 0 || N < 0 || K % 32 != 0) return GQ_ERR_SHAPE;
+    if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return GQ_ERR_SHAPE;
+    if (M * K > kMaxElems || N * K > kMaxElems || N * M > kMaxElems) return GQ_ERR_SHAPE;
+    return GQ_OK;
+}
+
+gq_status quantize_impl(gq_type t, const float* W, int64_t M, int64_t K, void* out,
+                        void* stream) {
+    gq_status st = check_shape(M, K, 0);
+    if (st != GQ_OK) return st;
+    if (M == 0 || K == 0) return GQ_OK;
+    if (!W || !out) return GQ_ERR_NULL;
+    if (!aligned(W, 4) || !aligned(out, 16)) return GQ_ERR_ALIGN;
+    return from_cuda(gq::launch_quantize(t, W, M * (K / 32), static_cast<uint8_t*>(out),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+// Validates one problem; sets *empty when there is nothing to launch for it.
+gq_status check_problem(const void* W, gq_type t, int64_t M, int64_t K, const float* X,
+                        int64_t N, const float* Y, bool* empty) {
+    if (!known_type(t)) return GQ_ERR_TYPE;
+    gq_status st = check_shape(M, K, N);
+    if (st != GQ_OK) return st;
+    *empty = (M == 0 || N == 0);
+    if (*empty) return GQ_OK;
+    if (!Y) return GQ_ERR_NULL;
+    if (K > 0 && (!W || !X)) return GQ_ERR_NULL;
+    if (!aligned(Y, 4)) return GQ_ERR_ALIGN;
+    if (K > 0 && (!aligned(W, 16) || !aligned(X, 4))) return GQ_ERR_ALIGN;
+    return GQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t gq_abi_version(void) { return GQ_ABI_VERSION; }
+
+size_t gq_block_bytes(gq_type t) { return static_cast<size_t>(gq::block_bytes_of(t)); }
+
+size_t gq_row_bytes(gq_type t, int64_t K) {
+    const int bb = gq::block_bytes_of(t);
+    if (bb == 0 || K < 0 || K % 32 != 0) return 0;
+    return static_cast<size_t>(K / 32) * static_cast<size_t>(bb);
+}
+
+gq_status gq_quantize_q4_0(const float* W, int64_t M, int64_t K, void* W_blocks,
+                           void* stream) {
+    return quantize_impl(GQ_TYPE_Q4_0, W, M, K, W_blocks, stream);
+}
+
+gq_status gq_quantize_q8_0(const float* W, int64_t M, int64_t K, void* W_blocks,
+                           void* stream) {
+    return quantize_impl(GQ_TYPE_Q8_0, W, M, K, W_blocks, stream);
+}
+
+gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K, float* W_out,
+                        void* stream) {
+    if (!known_type(t)) return GQ_ERR_TYPE;
+    gq_status st = check_shape(M, K, 0);
+    if (st != GQ_OK) return st;
+    if (M == 0 || K == 0) return GQ_OK;
+    if (!W_blocks || !W_out) return GQ_ERR_NULL;
+    if (!aligned(W_blocks, 16) || !aligned(W_out, 4)) return GQ_ERR_ALIGN;
+    return from_cuda(gq::launch_dequantize(t, static_cast<const uint8_t*>(W_blocks), M * K,
+                                           W_out, static_cast<cudaStream_t>(stream)));
+}
+
+gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K, const float* X,
+                     int64_t N, float* Y, void* stream) {
+    bool empty = false;
+    gq_status st = check_problem(W_blocks, t, M, K, X, N, Y, &empty);
+    if (st != GQ_OK || empty) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s));
+    gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
+    return from_cuda(gq::launch_mul_mat(t, &p, 1, N, s));
+}
+
+gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
+                             int64_t N, void* stream) {
+    if (count < 0 || count > GQ_MAX_BATCH) return GQ_ERR_SHAPE;
+    if (!known_type(t)) return GQ_ERR_TYPE;
+    if (count == 0) return GQ_OK;
+    if (!problems) return GQ_ERR_NULL;
+    gq::MatProblem run[GQ_MAX_BATCH];
+    int n_run = 0;
+    for (int i = 0; i < count; ++i) {
+        const gq_mul_mat_problem& p = problems[i];
+        bool empty = false;
+        gq_status st = check_problem(p.W_blocks, t, p.M, p.K, p.X, N, p.Y, &empty);
+        if (st != GQ_OK) return st;
+        if (!empty) run[n_run++] = {static_cast<const uint8_t*>(p.W_blocks), p.X, p.Y, p.M, p.K};
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int n_launch = 0;
+    for (int i = 0; i < n_run; ++i) {
+        if (run[i].K == 0) {
+            cudaError_t e = cudaMemsetAsync(run[i].Y, 0, sizeof(float) * N * run[i].M, s);
+            if (e != cudaSuccess) return GQ_ERR_CUDA;
+        } else {
+            run[n_launch++] = run[i];
+        }
+    }
+    if (n_launch == 0) return GQ_OK;
+    return from_cuda(gq::launch_mul_mat(t, run, n_launch, N, s));
+}
+
+gq_status gq_get_last_error(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GQ_ERR_CUDA;
+    gq::DeviceInfo* info = nullptr;
+    if (gq::current_device_info(&info) != cudaSuccess) return GQ_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, info->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GQ_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(info->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GQ_ERR_CUDA;
+        return GQ_ERR_TIMEOUT;
+    }
+    return GQ_OK;
+}
+
+const char* gq_status_string(gq_status s) {
+    switch (s) {
+        case GQ_OK: return "ok";
+        case GQ_ERR_NULL: return "a required pointer is NULL";
+        case GQ_ERR_SHAPE: return "invalid shape (negative, K not a multiple of 32, too large)";
+        case GQ_ERR_TYPE: return "unknown block type";
+        case GQ_ERR_ALIGN: return "misaligned pointer (blocks need 16 bytes, fp32 arrays 4)";
+        case GQ_ERR_CUDA: return "CUDA runtime error";
+        case GQ_ERR_TIMEOUT: return "a device-side wait ran out of time";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

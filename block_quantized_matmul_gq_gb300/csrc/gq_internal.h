@@ -1,0 +1,46 @@
+// gq_internal.h -- host-side interface between the C ABI (gq_capi.cu) and the kernel
+// translation units. Not installed; callers use include/gq.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gq.h"
+
+namespace gq {
+
+constexpr int kQ4Bytes = 18;   // fp16 scale + 16 bytes of nibble codes
+constexpr int kQ8Bytes = 34;   // fp16 scale + 32 int8 codes
+
+inline int block_bytes_of(gq_type t) {
+    return t == GQ_TYPE_Q4_0 ? kQ4Bytes : (t == GQ_TYPE_Q8_0 ? kQ8Bytes : 0);
+}
+
+// One validated, non-empty mul_mat problem (K > 0, M > 0) as the launchers see it.
+struct MatProblem {
+    const uint8_t* W;
+    const float* X;
+    float* Y;
+    int64_t M;
+    int64_t K;
+};
+
+// Per-device facts, looked up once per device.
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    unsigned* status = nullptr;   // device address of this device's status word
+};
+cudaError_t current_device_info(DeviceInfo** out);
+
+cudaError_t launch_quantize(gq_type t, const float* W, int64_t n_blocks, uint8_t* out,
+                            cudaStream_t s);
+cudaError_t launch_dequantize(gq_type t, const uint8_t* blocks, int64_t n_elems, float* out,
+                              cudaStream_t s);
+
+// Y = X . What^T for every problem; all share type t and N tokens.
+cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_t N,
+                           cudaStream_t s);
+
+}  // namespace gq

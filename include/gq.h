@@ -1,0 +1,152 @@
+/*
+ * gq.h -- C ABI of libgq: block-quantized (Q4_0 / Q8_0) weights times fp32 activations on
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation is the `mul_mat` that "No Python! Building an AI Inference Engine
+ * Exclusively in C++" (section 6) says takes over 90% of inference compute, with the
+ * weight held in 32-element blocks as "Development Guide for Small AI Models (TinyLLaMA,
+ * etc.) Using C++" (section 6.1) lays them out and dequantized right after the load
+ * ("No Python! ...", section 9; "Development Guide ...", section 6.2).
+ *
+ * Conventions shared by every call below.
+ *   - Shapes. W is M x K (row m holds output feature m, K contiguous); X is N x K
+ *     (token n is row n, K contiguous); Y is N x M (token n is row n, M contiguous):
+ *         Y[n][m] = sum_k What[m][k] * X[n][k],   i.e.  Y = X . What^T.
+ *     This is the layout of the cuBLAS call in "No Python! ...", section 7.2
+ *     (cublasSgemm(T, N, m, n, k, W, k, X, k, Y, m)): column-major m x n is row-major N x M.
+ *   - Block layout (public, fixed). Blocks follow each other row by row, K/32 per row,
+ *     with no padding between rows.
+ *       Q4_0, 18 bytes: fp16 scale d (little-endian), then 16 bytes of codes; byte j holds
+ *             element j in its low nibble and element j+16 in its high nibble; a code c
+ *             means What = (c - 8) * d.
+ *       Q8_0, 34 bytes: fp16 scale d, then 32 signed bytes c; What = c * d.
+ *   - Pointers. Every array pointer is a DEVICE pointer owned by the caller; the library
+ *     keeps none of them after the call returns and allocates no device memory on these
+ *     paths. W_blocks must be 16-byte aligned, fp32 arrays 4-byte aligned (16-byte
+ *     alignment of X is used when present). A pointer may be NULL only when its array is
+ *     empty.
+ *   - Streams. `stream` is a cudaStream_t (NULL = the legacy default stream) passed as
+ *     void* so that this header needs no CUDA include. Calls only enqueue work: they do
+ *     not synchronize, and results are ready when the stream reaches them.
+ *   - Errors. Argument checks run on the host before anything is launched and return a
+ *     negative gq_status; nothing is enqueued then. A failed CUDA launch returns
+ *     GQ_ERR_CUDA. Kernels never trap: a device-side wait that runs past its limit sets a
+ *     per-device status word that gq_get_last_error() returns.
+ *   - Empty inputs. M == 0 or N == 0 is a valid no-op; K == 0 writes Y = 0 (empty sum).
+ *   - Range. Values are finite; |w| / 7 and |w| / 127 must fit fp16 (|d| <= 65504).
+ *     Non-finite inputs give unspecified results.
+ */
+#ifndef GQ_H_
+#define GQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQ_ABI_VERSION 1
+/* Largest number of problems one gq_mul_mat_batched call takes. */
+#define GQ_MAX_BATCH 256
+
+typedef enum gq_type {
+    GQ_TYPE_Q4_0 = 2,   /* 18-byte blocks: fp16 scale + 32 4-bit codes */
+    GQ_TYPE_Q8_0 = 8    /* 34-byte blocks: fp16 scale + 32 int8 codes */
+} gq_type;
+
+typedef enum gq_status {
+    GQ_OK = 0,
+    GQ_ERR_NULL = -1,     /* a required pointer is NULL */
+    GQ_ERR_SHAPE = -2,    /* negative size, K not a multiple of 32, size overflow, count */
+    GQ_ERR_TYPE = -3,     /* unknown gq_type */
+    GQ_ERR_ALIGN = -4,    /* W_blocks not 16-byte aligned, or an fp32 array not 4-byte */
+    GQ_ERR_CUDA = -5,     /* a CUDA runtime call failed (launch, attribute, no device) */
+    GQ_ERR_TIMEOUT = -6   /* a device-side wait ran out (reported by gq_get_last_error) */
+} gq_status;
+
+/* Version of this ABI (GQ_ABI_VERSION of the header the library was built with). */
+int32_t gq_abi_version(void);
+
+/* Bytes of one 32-weight block: 18 (Q4_0) or 34 (Q8_0); 0 for an unknown type. */
+size_t gq_block_bytes(gq_type t);
+
+/* Bytes of one quantized row of K weights: (K / 32) * gq_block_bytes(t); 0 if K is
+ * negative or not a multiple of 32, or the type is unknown. */
+size_t gq_row_bytes(gq_type t, int64_t K);
+
+/*
+ * Quantize W (M x K fp32) into Q4_0 blocks, per 32-element block
+ * ("A Complete Guide to llama.cpp and Customization with C++", section 2.2: w_i ~= Delta*q_i
+ * with Delta = max|w_i| / 7 and q_i in [-8, 7]):
+ *     amax = max_i |w_i|;  d = amax / 7 (fp32, IEEE division);  stored scale = fp16(d),
+ *     round to nearest even;  code_i = clamp(roundf(w_i / d) + 8, 0, 15) with roundf
+ *     rounding halves away from zero; an all-zero block stores d = 0 and codes 8.
+ * Bit-for-bit reproducible. W_blocks receives M * gq_row_bytes(GQ_TYPE_Q4_0, K) bytes.
+ */
+gq_status gq_quantize_q4_0(const float* W, int64_t M, int64_t K, void* W_blocks,
+                           void* stream);
+
+/*
+ * Quantize W into Q8_0 blocks: d = amax / 127, stored as fp16(d);
+ * code_i = clamp(roundf(w_i / d), -127, 127); all-zero block -> d = 0, codes 0.
+ * The pages name 8-bit quantization ("No Python! ...", section 9) without a layout; this
+ * is the 4-bit rule above carried to signed 8-bit codes.
+ */
+gq_status gq_quantize_q8_0(const float* W, int64_t M, int64_t K, void* W_blocks,
+                           void* stream);
+
+/*
+ * Expand blocks back to fp32: W_out[m][k] = (c - 8) * d (Q4_0) or c * d (Q8_0), exact in
+ * fp32 ("Development Guide ...", section 6.2, the unpack and dequantize steps).
+ * W_out receives M x K floats.
+ */
+gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                        float* W_out, void* stream);
+
+/*
+ * Y (N x M fp32) = X (N x K fp32) . What^T, What the dequantized W_blocks (M rows).
+ * ("No Python! ...", sections 6 and 7.2; "A Complete Guide ...", section 2.1: N = 1 at
+ * decode makes this a matrix-vector product.) The weights are dequantized inside the
+ * kernel right after they are loaded and never written back.
+ * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element. Results are
+ * deterministic: the same inputs give the same bits on every call.
+ * Y must not overlap W_blocks or X.
+ */
+gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                     const float* X, int64_t N, float* Y, void* stream);
+
+/* One independent problem of gq_mul_mat_batched. */
+typedef struct gq_mul_mat_problem {
+    const void* W_blocks;   /* M rows of K/32 blocks, 16-byte aligned */
+    const float* X;         /* N x K */
+    float* Y;               /* N x M */
+    int64_t M;
+    int64_t K;
+} gq_mul_mat_problem;
+
+/*
+ * `count` independent gq_mul_mat problems that share the block type and N, computed by
+ * one launch that streams all their weights as one sequence. This is how one decode step
+ * runs its many matrix-vector products without a launch per matrix. Each problem follows
+ * gq_mul_mat's contract; Y buffers must not overlap each other or any input.
+ * count <= GQ_MAX_BATCH. The problem array is read on the host during the call.
+ */
+gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count,
+                             gq_type t, int64_t N, void* stream);
+
+/*
+ * Device-side status of the current device: synchronizes `stream`, then returns and
+ * clears the status word (GQ_OK, or GQ_ERR_TIMEOUT if a kernel gave up waiting), or
+ * GQ_ERR_CUDA if the stream itself reports an error.
+ */
+gq_status gq_get_last_error(void* stream);
+
+/* Static English text for a status code. */
+const char* gq_status_string(gq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H_ */

@@ -18,3 +18,20 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def gq_lib():
+    """libgq built in-tree (nvcc cross-compiles without a GPU) and its binding loaded."""
+    from block_quantized_matmul_gq_gb300 import build
+    build.build()
+    from block_quantized_matmul_gq_gb300 import binding
+    return binding
+
+
+@pytest.fixture(scope="session")
+def cuda_dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")

@@ -1,0 +1,64 @@
+"""Host-side pieces of bench.py, on CPU: byte accounting, the max-over-ranks / sum-of-
+units aggregation with two gloo ranks, and the profile-summary parser."""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from block_quantized_matmul_gq_gb300 import workloads  # noqa: E402
+
+
+def test_step_bytes_tinyllama():
+    nb = bench.step_bytes(workloads.tinyllama_decode_set(), 1, 18)
+    assert nb["weights"] == 581_861_376
+    assert nb["x"] == 4 * (22 * (6 * 2048 + 5632) + 2048)
+    assert nb["y"] == 4 * (22 * (2 * 2048 + 2 * 256 + 2 * 5632 + 2048) + 32000)
+    assert nb["total"] == nb["weights"] + nb["x"] + nb["y"]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t, u = bench.aggregate(1.0 + rank, 100.0 * (rank + 1), world)
+    out[rank] = (t, u)
+    dist.destroy_process_group()
+
+
+def test_aggregate_two_gloo_ranks():
+    port = _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1] == (2.0, 300.0)
+
+
+def test_aggregate_single_rank():
+    assert bench.aggregate(0.5, 7.0, 1) == (0.5, 7.0)
+
+
+def test_profile_summary_requires_current_kernel(tmp_path, monkeypatch):
+    p = tmp_path / "summary.md"
+    p.write_text(f"traffic_bytes_per_launch: 123\nkernel_source_sha256_16: {bench.kernel_source_hash()}\n")
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(p))
+    assert bench.profiled_traffic() == 123
+    p.write_text("traffic_bytes_per_launch: 123\nkernel_source_sha256_16: 0000\n")
+    assert bench.profiled_traffic() is None
+
+
+def test_reference_arm_sample_sizes():
+    shapes = workloads.tinyllama_decode_set()[:3]
+    sample = bench.oracle_sample(shapes, 2, 2)
+    assert [r for _, r, _, _ in sample] == [2, 2, 2]
+    assert bench.sample_bytes(sample) == sum(2 * 18 * s.K // 32 + 4 * s.K + 8 for s in shapes)

@@ -1,0 +1,105 @@
+"""C ABI checks that need no GPU: the library loads, exports every function that
+include/gq.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gq.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("gq_quantize_q4_0", "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat",
+                 "gq_mul_mat_batched", "gq_get_last_error", "gq_block_bytes", "gq_row_bytes",
+                 "gq_status_string", "gq_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(gq_lib):
+    lib = ctypes.CDLL(gq_lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gq.h but not exported"
+    assert set(declared_functions()) == set(gq_lib.EXPORTS)
+
+
+def test_sizes(gq_lib):
+    lib = gq_lib.lib
+    assert lib.gq_abi_version() == 1
+    assert lib.gq_block_bytes(2) == 18 and lib.gq_block_bytes(8) == 34
+    assert lib.gq_block_bytes(5) == 0
+    assert lib.gq_row_bytes(2, 2048) == 1152 and lib.gq_row_bytes(8, 5632) == 5984
+    assert lib.gq_row_bytes(2, 33) == 0 and lib.gq_row_bytes(2, -32) == 0
+    assert lib.gq_row_bytes(2, 0) == 0
+
+
+def test_status_strings(gq_lib):
+    for code in range(-6, 1):
+        assert gq_lib.lib.gq_status_string(code)
+    assert b"unknown" in gq_lib.lib.gq_status_string(-99)
+
+
+# Fake device addresses: the library must reject these before dereferencing anything.
+A16 = 0x7000_0000_0000
+A4 = A16 + 4
+A2 = A16 + 2
+
+
+def test_mul_mat_argument_checks(gq_lib):
+    mm = gq_lib.lib.gq_mul_mat
+    assert mm(A16, 7, 4, 64, A16, 1, A16, None) == -3              # unknown type
+    assert mm(A16, 2, 4, 48, A16, 1, A16, None) == -2              # K % 32
+    assert mm(A16, 2, -1, 64, A16, 1, A16, None) == -2             # negative M
+    assert mm(A16, 2, 4, 64, A16, -1, A16, None) == -2             # negative N
+    assert mm(A16, 2, 1 << 31, 64, A16, 1, A16, None) == -2        # dimension too large
+    assert mm(None, 2, 4, 64, A16, 1, A16, None) == -1             # NULL weights
+    assert mm(A16, 2, 4, 64, None, 1, A16, None) == -1             # NULL X
+    assert mm(A16, 2, 4, 64, A16, 1, None, None) == -1             # NULL Y
+    assert mm(A4, 2, 4, 64, A16, 1, A16, None) == -4               # blocks not 16B aligned
+    assert mm(A16, 2, 4, 64, A2, 1, A16, None) == -4               # X not 4B aligned
+    assert mm(A16, 2, 4, 64, A16, 1, A2, None) == -4               # Y not 4B aligned
+    assert mm(None, 2, 0, 64, None, 1, None, None) == 0            # M = 0: no-op
+    assert mm(None, 2, 4, 64, None, 0, None, None) == 0            # N = 0: no-op
+
+
+def test_batched_argument_checks(gq_lib):
+    P = gq_lib.Problem
+    arr = (P * 2)(P(A16, A16, A16, 4, 64), P(A16, A16, A16, 4, 48))
+    bm = gq_lib.lib.gq_mul_mat_batched
+    assert bm(arr, 2, 2, 1, None) == -2                            # second problem: K % 32
+    assert bm(arr, 257, 2, 1, None) == -2                          # count > GQ_MAX_BATCH
+    assert bm(arr, -1, 2, 1, None) == -2
+    assert bm(arr, 1, 9, 1, None) == -3
+    assert bm(None, 1, 2, 1, None) == -1
+    assert bm(arr, 0, 2, 1, None) == 0
+    arr2 = (P * 1)(P(A16, A16, A16, 0, 64))
+    assert bm(arr2, 1, 2, 1, None) == 0                            # only empty problems
+
+
+def test_quantize_dequantize_argument_checks(gq_lib):
+    lib = gq_lib.lib
+    for q in (lib.gq_quantize_q4_0, lib.gq_quantize_q8_0):
+        assert q(A16, 4, 40, A16, None) == -2
+        assert q(None, 4, 64, A16, None) == -1
+        assert q(A2, 4, 64, A16, None) == -4
+        assert q(A16, 4, 64, A4, None) == -4
+        assert q(None, 0, 64, None, None) == 0
+    dq = lib.gq_dequantize
+    assert dq(A16, 3, 4, 64, A16, None) == -3
+    assert dq(A4, 2, 4, 64, A16, None) == -4
+    assert dq(A16, 2, 4, 64, None, None) == -1
+    assert dq(None, 8, 0, 64, None, None) == 0
+
+
+def test_binding_refuses_cpu_tensors(gq_lib):
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="CUDA"):
+        gq_lib.quantize(torch.zeros(4, 64), "q4_0", out=torch.zeros(4, 36, dtype=torch.uint8))

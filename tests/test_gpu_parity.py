@@ -1,0 +1,256 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element.
+
+Quantize and dequantize must be bit-exact. mul_mat must satisfy, per element,
+    |Y - Y_oracle| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2
+where What is the oracle's own dequantization of the oracle's own blocks. Inputs are
+seeded synthetic tensors drawn on the CPU; no oracle input comes from the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_quantized_matmul_gq_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+def _np_weights(M, K, seed, scale=None):
+    W = workloads.weights(M, K, seed).numpy()
+    return W if scale is None else (W * scale).astype(np.float32)
+
+
+def check_tolerance(Y, Y_ref, What, X, where=""):
+    Y = np.asarray(Y, np.float64)
+    xn = np.linalg.norm(np.asarray(X, np.float64), axis=1)
+    wn = np.linalg.norm(np.asarray(What, np.float64), axis=1)
+    tol = TOL * xn[:, None] * wn[None, :]
+    err = np.abs(Y - np.asarray(Y_ref, np.float64))
+    bad = err > tol
+    if bad.any():
+        n, m = np.argwhere(bad)[0]
+        raise AssertionError(f"{where}: {bad.sum()} elements out of tolerance, first (n={n}, "
+                             f"m={m}) err={err[n, m]:.3e} tol={tol[n, m]:.3e}")
+    return float((err / np.where(tol > 0, tol, 1)).max()) if err.size else 0.0
+
+
+def gpu_quantize(gq_lib, W, t, dev):
+    return gq_lib.quantize(torch.from_numpy(W).to(dev), t).cpu().numpy()
+
+
+# ------------------------------------------------------------------------------------
+# quantize / dequantize: bit-exact
+# ------------------------------------------------------------------------------------
+QUANT_SHAPES = [(1, 32), (3, 96), (37, 288), (64, 2048), (129, 5632), (5, 11008)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K", QUANT_SHAPES)
+def test_quantize_bit_exact(gq_lib, oracle_mod, cuda_dev, t, M, K):
+    W = _np_weights(M, K, seed=M * 7 + K)
+    assert np.array_equal(gpu_quantize(gq_lib, W, t, cuda_dev), oracle_mod.quantize(t, W))
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_quantize_special_blocks(gq_lib, oracle_mod, cuda_dev, t):
+    """Zero blocks, exact ties of w/d, powers of two, subnormal and huge magnitudes."""
+    rng = np.random.default_rng(99)
+    rows = []
+    rows.append(np.zeros(64, np.float32))
+    s = 0.25
+    tie = np.zeros(32, np.float32)
+    tie[:8] = np.array([7, 2.5, -2.5, 0.5, -0.5, 6.5, -6.5, 1.5]) * s
+    rows.append(np.concatenate([tie, tie * 4]))
+    rows.append((rng.integers(-8, 8, 64) * 2.0 ** -10).astype(np.float32))
+    rows.append((rng.standard_normal(64) * 1e-7).astype(np.float32))     # fp16 subnormal d
+    rows.append((rng.standard_normal(64) * 1e-41).astype(np.float32))    # fp32 subnormal w
+    rows.append((rng.standard_normal(64) * 1e4).astype(np.float32))
+    rows.append(np.full(64, -3.0, np.float32))
+    W = np.stack(rows)
+    assert np.array_equal(gpu_quantize(gq_lib, W, t, cuda_dev), oracle_mod.quantize(t, W))
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_dequantize_bit_exact(gq_lib, oracle_mod, cuda_dev, t):
+    """Arbitrary block bytes (random codes, any finite fp16 scale, code 0 included)."""
+    rng = np.random.default_rng(5)
+    M, K = 41, 288
+    bb = oracle_mod.block_bytes(t)
+    blocks = rng.integers(0, 256, size=(M, K // 32, bb), dtype=np.uint8)
+    scales = rng.standard_normal((M, K // 32)).astype(np.float16)
+    scales[0, 0] = np.float16(6e-8)          # subnormal scale
+    blocks[..., :2] = scales.view(np.uint8).reshape(M, K // 32, 2)
+    blocks = blocks.reshape(M, -1)
+    got = gq_lib.dequantize(torch.from_numpy(blocks).to(cuda_dev), t, M, K).cpu().numpy()
+    ref = oracle_mod.dequantize(t, blocks, M, K)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------------------------
+# mul_mat
+# ------------------------------------------------------------------------------------
+def run_mul_mat(gq_lib, oracle_mod, dev, t, M, K, N, seed=0, X=None):
+    W = _np_weights(M, K, seed=seed + 11)
+    q = oracle_mod.quantize(t, W)
+    if X is None:
+        X = workloads.activations(N, K, seed=seed + 12).numpy()
+    Y = gq_lib.mul_mat(torch.from_numpy(q).to(dev), t, M, K, torch.from_numpy(X).to(dev))
+    Y = Y.cpu().numpy()
+    Y_ref = oracle_mod.mul_mat(t, q, M, K, X)
+    What = oracle_mod.dequantize(t, q, M, K)
+    return Y, Y_ref, What, X
+
+
+# Fast streaming kernel: K % 256 == 0. Rows of K = 11008 (Q4_0: 43 chunks) straddle the
+# 256-chunk stages, M values leave ragged tails, N covers 1..4 and token groups 4+4+1.
+FAST = [(1, 256, 1), (7, 2048, 1), (300, 2048, 1), (1000, 2048, 2), (129, 5632, 3),
+        (64, 11008, 4), (33, 4096, 5), (257, 1024, 9), (2048, 2048, 1)]
+# Generic kernel: K % 256 != 0.
+GENERIC = [(1, 32, 1), (5, 96, 2), (37, 288, 3), (64, 800, 4), (9, 160, 7)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", FAST + GENERIC)
+def test_mul_mat_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    Y, Y_ref, What, X = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, N, seed=M + K + N)
+    assert Y.shape == (N, M)
+    check_tolerance(Y, Y_ref, What, X, f"{t} M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("K", [2048, 96])
+def test_mul_mat_one_hot_is_exact(gq_lib, oracle_mod, cuda_dev, t, K):
+    """X = e_k returns column k of What bit for bit, on both kernels."""
+    M = 77
+    ks = [0, 1, 15, 16, 31, 32, K - 1] + ([255, 256, 1000] if K > 1000 else [])
+    X = np.zeros((len(ks), K), np.float32)
+    for n, k in enumerate(ks):
+        X[n, k] = 1.0
+    Y, Y_ref, What, _ = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, len(ks), X=X)
+    for n, k in enumerate(ks):
+        assert np.array_equal(Y[n], What[:, k]), k
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_mul_mat_scaled_inputs(gq_lib, oracle_mod, cuda_dev, t):
+    """Activations far from N(0,1): huge, tiny and mixed magnitudes per block."""
+    M, K = 50, 2048
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((4, K)).astype(np.float32)
+    X[0] *= 3e4
+    X[1] *= 1e-30
+    X[2, ::64] *= 1e3
+    X[3, :256] = 0.0
+    Y, Y_ref, What, _ = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, 4, X=X)
+    check_tolerance(Y, Y_ref, What, X, t)
+
+
+def test_mul_mat_deterministic(gq_lib, cuda_dev):
+    M, K, N = 3000, 5632, 2
+    W = workloads.weights(M, K, 1, device=cuda_dev)
+    q = gq_lib.quantize(W, "q4_0")
+    X = workloads.activations(N, K, 2, device=cuda_dev)
+    y1 = gq_lib.mul_mat(q, "q4_0", M, K, X)
+    y2 = gq_lib.mul_mat(q, "q4_0", M, K, X)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_mul_mat_misaligned_x(gq_lib, oracle_mod, cuda_dev):
+    """X 4-byte but not 16-byte aligned: correct through the generic kernel."""
+    M, K = 40, 2048
+    W = _np_weights(M, K, seed=8)
+    q = oracle_mod.quantize("q4_0", W)
+    X = workloads.activations(1, K, seed=9).numpy()
+    buf = torch.zeros(K + 1, dtype=torch.float32, device=cuda_dev)
+    buf[1:] = torch.from_numpy(X[0]).to(cuda_dev)
+    xv = buf[1:].view(1, K)
+    assert xv.data_ptr() % 16 == 4
+    Y = gq_lib.mul_mat(torch.from_numpy(q).to(cuda_dev), "q4_0", M, K, xv).cpu().numpy()
+    check_tolerance(Y, oracle_mod.mul_mat("q4_0", q, M, K, X),
+                    oracle_mod.dequantize("q4_0", q, M, K), X)
+
+
+def test_empty_and_zero_k(gq_lib, cuda_dev):
+    q = torch.zeros(16, dtype=torch.uint8, device=cuda_dev)
+    X = torch.zeros((3, 0), device=cuda_dev)
+    Y = torch.full((3, 5), 7.0, device=cuda_dev)
+    gq_lib.mul_mat(q, "q4_0", 5, 0, X, out=Y)          # empty sum
+    assert torch.count_nonzero(Y) == 0
+    Y2 = torch.full((0, 5), 7.0, device=cuda_dev)
+    gq_lib.mul_mat(q, "q4_0", 5, 64, torch.zeros((0, 64), device=cuda_dev), out=Y2)
+    Y3 = torch.full((2, 0), 7.0, device=cuda_dev)
+    gq_lib.mul_mat(q, "q8_0", 0, 64, torch.zeros((2, 64), device=cuda_dev), out=Y3)
+    assert gq_lib.get_last_error() == 0
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_batched_mixed_shapes(gq_lib, oracle_mod, cuda_dev, t):
+    """Problems of different M and K (fast and generic mixed) in one batched call."""
+    shapes = [(256, 2048), (2048, 2048), (7, 96), (300, 5632), (1, 256), (64, 11008),
+              (0, 512), (5, 0)]
+    N = 3
+    items, refs = [], []
+    for i, (M, K) in enumerate(shapes):
+        W = _np_weights(M, K, seed=50 + i) if M * K else np.zeros((M, K), np.float32)
+        q = oracle_mod.quantize(t, W) if M * K else np.zeros((M, 0), np.uint8)
+        X = workloads.activations(N, K, seed=60 + i).numpy()
+        Yd = torch.full((N, M), 9.0, device=cuda_dev)
+        items.append((torch.from_numpy(q).contiguous().to(cuda_dev), M, K,
+                      torch.from_numpy(X).to(cuda_dev), Yd))
+        refs.append((q, X))
+    gq_lib.mul_mat_batched(items, t, N)
+    for (M, K), (q, X), it in zip(shapes, refs, items):
+        Y = it[4].cpu().numpy()
+        if M == 0:
+            continue
+        if K == 0:
+            assert not Y.any()
+            continue
+        check_tolerance(Y, oracle_mod.mul_mat(t, q, M, K, X),
+                        oracle_mod.dequantize(t, q, M, K), X, f"M={M} K={K}")
+    assert gq_lib.get_last_error() == 0
+
+
+# ------------------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times, on sampled rows
+# ------------------------------------------------------------------------------------
+def _sampled_step_check(gq_lib, oracle_mod, dev, workload, t, N, shapes, rows_per_mat=6):
+    from block_quantized_matmul_gq_gb300.weightset import QuantizedWeightSet
+    rng = np.random.default_rng(workload * 10 + N)
+    keep = {j: np.unique(np.concatenate([[0, s.M - 1], rng.integers(0, s.M, rows_per_mat)]))
+            for j, s in enumerate(shapes)}
+    ws = QuantizedWeightSet.synthetic(workload, shapes, t, dev, keep_rows=keep)
+    xs, ys = ws.make_io(N, workload, dev)
+    ws.run(ws.problem_arrays(xs, ys), N)
+    assert gq_lib.get_last_error() == 0
+    worst = 0.0
+    for j, s in enumerate(shapes):
+        rows = keep[j]
+        W_rows = ws.kept[j].numpy()
+        q_rows = oracle_mod.quantize(t, W_rows)
+        got_blocks = ws.mats[j].blocks[torch.as_tensor(rows, device=dev)].cpu().numpy()
+        assert np.array_equal(got_blocks, q_rows), (j, s)
+        X = xs[j].cpu().numpy()
+        Y_ref = oracle_mod.mul_mat(t, q_rows, len(rows), s.K, X)
+        Y = ys[j].cpu().numpy()[:, rows]
+        worst = max(worst, check_tolerance(Y, Y_ref, oracle_mod.dequantize(t, q_rows, len(rows), s.K),
+                                           X, f"{s.name}[{j}]"))
+    return worst
+
+
+def test_tinyllama_decode_step_q4_0_full_size(gq_lib, oracle_mod, cuda_dev):
+    """All 155 matmuls of the TinyLLaMA decode step, Q4_0, N = 1, batched as timed."""
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 2, "q4_0", 1,
+                        workloads.tinyllama_decode_set())
+
+
+@pytest.mark.parametrize("N", [1, 16])
+def test_tinyllama_decode_step_q8_0_full_size(gq_lib, oracle_mod, cuda_dev, N):
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 3, "q8_0", N,
+                        workloads.tinyllama_decode_set(), rows_per_mat=3)
+
+
+@pytest.mark.parametrize("N", [1, 16])
+def test_llama7b_shapes_full_size(gq_lib, oracle_mod, cuda_dev, N):
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 5, "q4_0", N, workloads.llama7b_set())
