@@ -32,7 +32,9 @@
 // Shapes the fast kernel does not take (K % 256 != 0, unaligned X, very large K) run on
 // gemv_generic_kernel: one warp per row, plain loads, fp32 FMA.
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "gq_device.cuh"
 #include "gq_internal.h"
@@ -479,16 +481,18 @@ int64_t stream_smem_bytes(int n_tok_template, int max_c) {
 }
 
 // cudaFuncSetAttribute once per (kernel, device) for the largest size asked so far.
+// Keyed by the kernel's address: instantiations share a function type.
 template <typename KernelT>
 cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
     static std::mutex mu;
-    static int set_bytes[64] = {0};
+    static std::map<std::pair<const void*, int>, int64_t> set_bytes;
     std::lock_guard<std::mutex> lock(mu);
-    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    if (set_bytes[device] >= bytes) return cudaSuccess;
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), device);
+    auto it = set_bytes.find(key);
+    if (it != set_bytes.end() && it->second >= bytes) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
-    if (e == cudaSuccess) set_bytes[device] = static_cast<int>(bytes);
+    if (e == cudaSuccess) set_bytes[key] = bytes;
     return e;
 }
 
