@@ -20,7 +20,7 @@ if not os.path.exists(LIB_PATH):
         f"libgq.so not found at {LIB_PATH}: build it first "
         "(python -m block_quantized_matmul_gq_gb300.build); there is no fallback path")
 
-lib = ctypes.CDLL(LIB_PATH)
+lib = None
 
 Q4_0 = 2
 Q8_0 = 8
@@ -42,20 +42,30 @@ class Problem(ctypes.Structure):
                 ("M", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
-_i64, _i32, _vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
-lib.gq_abi_version.argtypes, lib.gq_abi_version.restype = [], _i32
-lib.gq_block_bytes.argtypes, lib.gq_block_bytes.restype = [ctypes.c_int], ctypes.c_size_t
-lib.gq_row_bytes.argtypes, lib.gq_row_bytes.restype = [ctypes.c_int, _i64], ctypes.c_size_t
-for _q in (lib.gq_quantize_q4_0, lib.gq_quantize_q8_0):
-    _q.argtypes, _q.restype = [_vp, _i64, _i64, _vp, _vp], ctypes.c_int
-lib.gq_dequantize.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _vp]
-lib.gq_dequantize.restype = ctypes.c_int
-lib.gq_mul_mat.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _i64, _vp, _vp]
-lib.gq_mul_mat.restype = ctypes.c_int
-lib.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), _i32, ctypes.c_int, _i64, _vp]
-lib.gq_mul_mat_batched.restype = ctypes.c_int
-lib.gq_get_last_error.argtypes, lib.gq_get_last_error.restype = [_vp], ctypes.c_int
-lib.gq_status_string.argtypes, lib.gq_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+def load(path: str = LIB_PATH):
+    """(Re)binds this module to the libgq shared library at `path` (default: the in-tree
+    build) and declares the C signatures of include/gq.h."""
+    global lib
+    L = ctypes.CDLL(path)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    L.gq_abi_version.argtypes, L.gq_abi_version.restype = [], i32
+    L.gq_block_bytes.argtypes, L.gq_block_bytes.restype = [ctypes.c_int], ctypes.c_size_t
+    L.gq_row_bytes.argtypes, L.gq_row_bytes.restype = [ctypes.c_int, i64], ctypes.c_size_t
+    for q in (L.gq_quantize_q4_0, L.gq_quantize_q8_0):
+        q.argtypes, q.restype = [vp, i64, i64, vp, vp], ctypes.c_int
+    L.gq_dequantize.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp]
+    L.gq_dequantize.restype = ctypes.c_int
+    L.gq_mul_mat.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp]
+    L.gq_mul_mat.restype = ctypes.c_int
+    L.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
+    L.gq_mul_mat_batched.restype = ctypes.c_int
+    L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
+    L.gq_status_string.argtypes, L.gq_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+    lib = L
+    return L
+
+
+load()
 
 
 class GQError(RuntimeError):

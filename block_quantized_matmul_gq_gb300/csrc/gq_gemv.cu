@@ -11,26 +11,33 @@
 //  * One persistent CTA per SM. All problems of a launch form one sequence of rows; each
 //    CTA takes a contiguous, row-aligned share of equal bytes, so small matrices (GQA
 //    k/v projections) ride along with large ones and no CTA idles on a tail.
-//  * Thread 0 streams that share through a 3-stage ring of 1-D bulk copies (TMA,
-//    cp.async.bulk) with an L2 evict-first hint; 256 threads consume it. A stage holds
-//    256 "chunks": 8 Q4_0 blocks (144 B, 256 weights) or 4 Q8_0 blocks (136 B, 128
-//    weights), one chunk per thread. Rows are whole chunks (K % 256 == 0), so every
-//    copy is 16-byte aligned.
-//  * Activations: each CTA converts the problem's X into 16-bit block fixed point in
-//    shared memory (one power-of-two scale 2^e per chunk of 256 / 128 elements), so that
-//    the inner product of a 32-weight block is EXACT integer arithmetic:
+//  * Inside a CTA, each warp owns tiles of 4 rows; eight lanes share a row and walk its K
+//    columns eight "chunks" at a time (a chunk is 8 Q4_0 blocks = 144 B = 256 weights, or
+//    4 Q8_0 blocks = 136 B = 128 weights), one chunk per lane. Every warp streams its own
+//    tiles through a private ring of shared-memory stages filled by 1-D bulk copies (TMA
+//    cp.async.bulk, L2 evict-first) issued by one lane -- a single copy when the stage
+//    holds whole rows (K <= 2048 for Q4_0), else one per row -- completing on a per-warp
+//    mbarrier; warps never wait for each other inside a problem. Rows are whole chunks
+//    (K % 256 == 0), so copies are 16-byte aligned.
+//  * Activations: at each problem boundary the CTA converts X into 16-bit block fixed
+//    point in shared memory (one power-of-two scale 2^e per chunk), so the inner product
+//    of a 32-weight block is EXACT integer arithmetic with dp2a (two 16x8-bit products
+//    per instruction):
 //        S = sum_i (16 (c_i - 8)) * x16_i       (Q4_0; codes become signed bytes 16(c-8))
 //        S = sum_i c_i * x16_i                  (Q8_0)
-//    with dp2a (two 16x8-bit products per instruction). Then acc += d * float(S) and, per
-//    chunk, partial = acc * 2^e. The only approximation is x16 = rint(x / 2^e) with
-//    |x16| <= 32767, i.e. |error| <= sqrt(256) / 65534 * ||x|| ||What|| = 2.4e-4 of the
-//    bound 1e-3 ||x|| ||What|| (Cauchy-Schwarz per chunk), whatever the inputs.
-//  * Row sums: per-chunk partials go to shared memory and one thread per row adds them in
-//    k order (a carry links rows that straddle stages), so results are deterministic.
-//  * Waits are bounded: a stage that never arrives sets the device status word and the
-//    CTA leaves after draining its own copies.
-// Shapes the fast kernel does not take (K % 256 != 0, unaligned X, very large K) run on
-// gemv_generic_kernel: one warp per row, plain loads, fp32 FMA.
+//    then acc += d * float(S) and, per chunk, partial = acc * 2^e. The only approximation
+//    is x16 = rint(x / 2^e) with |x16| <= 32767, i.e. |error| <= sqrt(256) / 65534 *
+//    ||x|| ||What|| = 0.24 of the bound 1e-3 ||x|| ||What|| (Cauchy-Schwarz per chunk),
+//    whatever the inputs. All lanes of a warp read the same x16 columns (broadcast).
+//  * A lane keeps its row's running sum in registers across all columns; the eight lanes
+//    of a row add their sums with three shuffles at the end. When a CTA's part of a problem
+//    has fewer 4-row tiles than warps, each tile's columns are split between warps and
+//    the per-warp sums are added in a fixed order in shared memory: deterministic, no
+//    atomics.
+//  * Waits are bounded: a stage that never arrives sets the device status word; the CTA
+//    leaves at the next problem boundary after draining its own copies.
+// Shapes the streaming kernel does not take (K % 256 != 0, unaligned X, very large K)
+// run on gemv_generic_kernel: one warp per row, plain loads, fp32 FMA.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -42,9 +49,26 @@
 namespace gq {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kStages = 3;
-constexpr int kMaxTok = 4;   // tokens per pass of the weight stream
+// Build-time tuning: warps per CTA and ring depth per warp (for <= 3 tokens / 4 tokens).
+#ifndef GQ_GEMV_WARPS
+#define GQ_GEMV_WARPS 16
+#endif
+#ifndef GQ_GEMV_STAGES
+#define GQ_GEMV_STAGES 2
+#endif
+#ifndef GQ_GEMV_STAGES_N4
+#define GQ_GEMV_STAGES_N4 2
+#endif
+constexpr int kWarps = GQ_GEMV_WARPS;
+constexpr int kThreads = kWarps * 32;
+constexpr int kLanesPerRow = 8;               // one chunk per lane, 8 chunks per row per stage
+constexpr int kTileRows = 32 / kLanesPerRow;   // 4 rows per warp tile
+constexpr int kMaxTok = 4;                     // tokens per pass of the weight stream
+// Ring depth per warp: deeper while the x16 buffer is small (<= 3 tokens).
+template <int kNT>
+__host__ __device__ constexpr int ring_stages() {
+    return kNT <= 3 ? GQ_GEMV_STAGES : GQ_GEMV_STAGES_N4;
+}
 
 template <int kType>
 struct Fmt;
@@ -52,7 +76,7 @@ template <>
 struct Fmt<GQ_TYPE_Q4_0> {
     static constexpr int kBB = kQ4Bytes;
     static constexpr int kBlocksPerChunk = 8;
-    static constexpr int kCodeShift = 4;   // codes enter dp2a as 16 * (c - 8)
+    static constexpr int kCodeShift = 4;   // dp2a sums come out as 16 * sum (c - 8) x16
 };
 template <>
 struct Fmt<GQ_TYPE_Q8_0> {
@@ -68,10 +92,17 @@ struct Geo {
     static constexpr int kChunkBytes = kBB * kBPC;                 // 144 or 136
     static constexpr int kChunkWords = kChunkBytes / 4;            // 36 or 34
     static constexpr int kWPC = 32 * kBPC;                         // weights per chunk
-    static constexpr int kStageBytes = kThreads * kChunkBytes;
-    // x16 record of one chunk for one token: kWPC int16, then the int exponent, padded
-    // to a 16-byte multiple whose word count is 4 mod 32 (bank-conflict-free reads).
-    static constexpr int kXRec = kWPC * 2 + 16;                    // 528 or 272
+    static constexpr int kRowStride = kLanesPerRow * kChunkBytes;  // 1152 or 1088 in a stage
+    // One stage of one warp: 4 rows x 8 chunks, padded to 128-byte multiples.
+    static constexpr int kStageBytes = (kTileRows * kRowStride + 127) / 128 * 128;
+    // x16 record of one chunk for one token: kWPC int16; for Q4_0 one int bias per block
+    // (-128 * sum of the block's x16, the code offset 8 folded in); then two float
+    // factors whose product is the chunk's power-of-two scale. Record strides are
+    // 140 / 68 words (12 / 4 mod 32), so the 8 columns a warp reads sit in 8 different
+    // groups of 4 banks: one wavefront per 16-byte load.
+    static constexpr int kBiasOff = kWPC * 2;
+    static constexpr int kScaleOff = kBiasOff + (kType == GQ_TYPE_Q4_0 ? 4 * kBPC : 0);
+    static constexpr int kXRec = kScaleOff + 16;                   // 560 or 272
 };
 
 struct GemvProb {
@@ -89,7 +120,7 @@ template <int kMaxProbs>
 struct GemvParams {
     int32_t count;
     int32_t n_tok;        // valid tokens of this pass, 1..kMaxTok
-    int32_t max_c;        // largest C: x buffer holds n_tok * max_c records
+    int32_t max_c;        // largest C: the x buffer holds kNT * max_c records
     int32_t pad_;
     int64_t total_bytes;
     unsigned* status;
@@ -109,36 +140,91 @@ __device__ void row_at_byte(const GemvParams<kMaxProbs>& P, int64_t byte, int& p
     }
 }
 
-// Walks this CTA's share as a sequence of stages: (problem, segment rows, chunk offset).
-struct Cursor {
+// A CTA's share is a list of segments: one problem each, a row range [rb, re).
+struct Segment {
     int p;
-    int64_t r_begin, r_end;   // rows of the current segment (one problem)
-    int64_t chunk, n_chunks;  // chunk offset of the current stage within the segment
+    int64_t rb, re;
     bool valid;
 };
 
 template <int kMaxProbs>
-__device__ void open_segment(const GemvParams<kMaxProbs>& P, Cursor& c, int p, int64_t rb,
-                             int p_end, int64_t r_end) {
+__device__ Segment find_segment(const GemvParams<kMaxProbs>& P, int p, int64_t rb, int p_end,
+                                int64_t r_end) {
     for (; p < P.count && p <= p_end; ++p, rb = 0) {
         const int64_t re = (p == p_end) ? r_end : P.p[p].M;
-        if (re > rb) {
-            c.p = p;
-            c.r_begin = rb;
-            c.r_end = re;
-            c.chunk = 0;
-            c.n_chunks = (re - rb) * P.p[p].C;
+        if (re > rb) return Segment{p, rb, re, true};
+    }
+    return Segment{0, 0, 0, false};
+}
+
+// How a segment is cut into work items: 4-row tiles whose K runs in column groups of 8
+// chunks (one stage each); when there are fewer tiles than warps, each tile's column
+// groups split into `ksplit` ranges so every warp works.
+struct SegPlan {
+    int ntiles, ncs, ksplit, items;
+};
+
+__device__ __forceinline__ SegPlan plan_segment(int64_t rows, int C) {
+    SegPlan s;
+    s.ntiles = static_cast<int>((rows + kTileRows - 1) / kTileRows);
+    s.ncs = (C + kLanesPerRow - 1) / kLanesPerRow;
+    s.ksplit = s.ntiles >= kWarps ? 1 : max(1, min(s.ncs, kWarps / s.ntiles));
+    s.items = s.ntiles * s.ksplit;
+    return s;
+}
+
+// Column-group range [cs_begin, cs_end) of k-group kg.
+__device__ __forceinline__ void kgroup_range(const SegPlan& sp, int kg, int& cb, int& ce) {
+    cb = kg * sp.ncs / sp.ksplit;
+    ce = (kg + 1) * sp.ncs / sp.ksplit;
+}
+
+// One warp's walk through its stages: segment -> its items (item = warp, warp + kWarps,
+// ...) -> column pairs of the item. Uniform across the lanes of the warp.
+struct WarpCursor {
+    Segment seg;
+    SegPlan plan;
+    int item;
+    int cs, ce;           // current column group and end of the item's range
+    bool valid;
+};
+
+template <int kMaxProbs>
+__device__ void cursor_item(const GemvParams<kMaxProbs>& P, WarpCursor& c) {
+    int cb, ce;
+    kgroup_range(c.plan, c.item % c.plan.ksplit, cb, ce);
+    c.cs = cb;
+    c.ce = ce;
+}
+
+template <int kMaxProbs>
+__device__ void cursor_enter(const GemvParams<kMaxProbs>& P, WarpCursor& c, Segment seg,
+                             int warp, int p_end, int64_t r_end) {
+    while (seg.valid) {
+        const SegPlan sp = plan_segment(seg.re - seg.rb, P.p[seg.p].C);
+        if (warp < sp.items) {
+            c.seg = seg;
+            c.plan = sp;
+            c.item = warp;
             c.valid = true;
+            cursor_item(P, c);
             return;
         }
+        seg = find_segment(P, seg.p + 1, 0, p_end, r_end);
     }
     c.valid = false;
 }
 
 template <int kMaxProbs>
-__device__ void advance(const GemvParams<kMaxProbs>& P, Cursor& c, int p_end, int64_t r_end) {
-    c.chunk += kThreads;
-    if (c.chunk >= c.n_chunks) open_segment(P, c, c.p + 1, 0, p_end, r_end);
+__device__ void cursor_advance(const GemvParams<kMaxProbs>& P, WarpCursor& c, int warp,
+                               int p_end, int64_t r_end) {
+    if (++c.cs < c.ce) return;
+    c.item += kWarps;
+    if (c.item < c.plan.items) {
+        cursor_item(P, c);
+        return;
+    }
+    cursor_enter(P, c, find_segment(P, c.seg.p + 1, 0, p_end, r_end), warp, p_end, r_end);
 }
 
 __device__ __forceinline__ uint32_t word_at(const uint32_t* r, int byte_off) {
@@ -165,15 +251,14 @@ __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbu
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int C = pr.C;
-    for (int idx = warp; idx < kNT * C; idx += kThreads / 32) {
+    for (int idx = warp; idx < kNT * C; idx += kWarps) {
         const int t = idx / C;
         const int col = idx - t * C;
-        uint8_t* rec = xbuf + (static_cast<int64_t>(t) * max_c + col) * G::kXRec;
+        uint8_t* rec = xbuf + (t * max_c + col) * G::kXRec;
         float v[kPerLane];
         if (t < n_tok) {
             const float4* src = reinterpret_cast<const float4*>(
-                pr.X + static_cast<int64_t>(t) * pr.K + static_cast<int64_t>(col) * G::kWPC +
-                lane * kPerLane);
+                pr.X + static_cast<int64_t>(t) * pr.K + col * G::kWPC + lane * kPerLane);
 #pragma unroll
             for (int i = 0; i < kPerLane / 4; ++i) {
                 const float4 f = __ldg(src + i);
@@ -192,25 +277,55 @@ __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbu
         amax = warp_max(amax);
         int e = 0;
         frexpf(amax, &e);   // amax = f * 2^e, f in [0.5, 1); e = 0 for amax = 0
+        // x16 = rint(x * 2^(15 - e)): an exact power-of-two scaling, then one rounding.
+        // 2^(15-e) as two normal floats (e spans -148..128 for finite inputs).
+        const int sh = 15 - e, sh_a = sh / 2;
+        const float f_a = __int_as_float((sh_a + 127) << 23);
+        const float f_b = __int_as_float((sh - sh_a + 127) << 23);
         uint32_t packed[kPerLane / 2];
+        int lane_sum = 0;
 #pragma unroll
         for (int i = 0; i < kPerLane / 2; ++i) {
-            const int a = max(-32767, min(32767, __float2int_rn(ldexpf(v[2 * i], 15 - e))));
-            const int b = max(-32767, min(32767, __float2int_rn(ldexpf(v[2 * i + 1], 15 - e))));
+            const int a = max(-32767, min(32767, __float2int_rn((v[2 * i] * f_a) * f_b)));
+            const int b = max(-32767, min(32767, __float2int_rn((v[2 * i + 1] * f_a) * f_b)));
+            lane_sum += a + b;
             packed[i] = (static_cast<uint32_t>(a) & 0xFFFFu) | (static_cast<uint32_t>(b) << 16);
         }
         if constexpr (kPerLane == 8) {
             *reinterpret_cast<uint4*>(rec + lane * 16) =
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            // Q4_0 block j covers lanes 4j..4j+3 (32 elements): bias = -128 * their sum.
+            lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 1);
+            lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 2);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<int*>(rec + G::kBiasOff + lane) = -128 * lane_sum;
         } else {
             *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
         }
-        if (lane == 0)
-            *reinterpret_cast<int*>(rec + G::kWPC * 2) = e - 15 - Fmt<kType>::kCodeShift;
+        if (lane == 0) {
+            // Partial sums come out scaled by 2^(15 - e + kCodeShift); undo with two
+            // power-of-two factors, each a normal float.
+            const int u = e - 15 - Fmt<kType>::kCodeShift, u_a = u / 2;
+            float* sc = reinterpret_cast<float*>(rec + G::kScaleOff);
+            sc[0] = __int_as_float((u_a + 127) << 23);
+            sc[1] = __int_as_float((u - u_a + 127) << 23);
+        }
     }
 }
 
-// One chunk for every token: returns per-token partial sums (already scaled by 2^e).
+__device__ __forceinline__ int dp2a_lo_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// One chunk against every token's x16 record: out[t] += chunk partial (scaled by 2^e).
 template <int kType, int kNT>
 __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xrec0,
                                           int rec_stride, float (&out)[kNT]) {
@@ -242,35 +357,39 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xre
         const int base = j * G::kBB;
         const float d = half_bits_to_float(u16_at(r, base));
         if constexpr (kType == GQ_TYPE_Q4_0) {
+            // Unsigned codes: lo bytes c (elements 4i..4i+3), hi bytes 16c (16+4i..).
+            // 16 * sum (c - 8) x = 16 * sum_lo c x + sum_hi (16c) x - 128 * sum x.
             uint32_t lo[4], hi[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t q = word_at(r, base + 2 + 4 * i);
-                lo[i] = ((q << 4) & 0xF0F0F0F0u) ^ 0x80808080u;   // bytes 16*(c-8), elems 4i..
-                hi[i] = (q & 0xF0F0F0F0u) ^ 0x80808080u;          // elems 16+4i..
+                lo[i] = q & 0x0F0F0F0Fu;
+                hi[i] = q & 0xF0F0F0F0u;
             }
 #pragma unroll
             for (int t = 0; t < kNT; ++t) {
-                const uint4* xw = reinterpret_cast<const uint4*>(xrec0 + t * rec_stride + 64 * j);
+                const uint8_t* rec = xrec0 + t * rec_stride;
+                const uint4* xw = reinterpret_cast<const uint4*>(rec + 64 * j);
                 const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
-                int s0 = 0, s1 = 0;
-                s0 = __dp2a_lo(static_cast<int>(x0.x), static_cast<int>(lo[0]), s0);
-                s0 = __dp2a_hi(static_cast<int>(x0.y), static_cast<int>(lo[0]), s0);
-                s1 = __dp2a_lo(static_cast<int>(x0.z), static_cast<int>(lo[1]), s1);
-                s1 = __dp2a_hi(static_cast<int>(x0.w), static_cast<int>(lo[1]), s1);
-                s0 = __dp2a_lo(static_cast<int>(x1.x), static_cast<int>(lo[2]), s0);
-                s0 = __dp2a_hi(static_cast<int>(x1.y), static_cast<int>(lo[2]), s0);
-                s1 = __dp2a_lo(static_cast<int>(x1.z), static_cast<int>(lo[3]), s1);
-                s1 = __dp2a_hi(static_cast<int>(x1.w), static_cast<int>(lo[3]), s1);
-                s0 = __dp2a_lo(static_cast<int>(x2.x), static_cast<int>(hi[0]), s0);
-                s0 = __dp2a_hi(static_cast<int>(x2.y), static_cast<int>(hi[0]), s0);
-                s1 = __dp2a_lo(static_cast<int>(x2.z), static_cast<int>(hi[1]), s1);
-                s1 = __dp2a_hi(static_cast<int>(x2.w), static_cast<int>(hi[1]), s1);
-                s0 = __dp2a_lo(static_cast<int>(x3.x), static_cast<int>(hi[2]), s0);
-                s0 = __dp2a_hi(static_cast<int>(x3.y), static_cast<int>(hi[2]), s0);
-                s1 = __dp2a_lo(static_cast<int>(x3.z), static_cast<int>(hi[3]), s1);
-                s1 = __dp2a_hi(static_cast<int>(x3.w), static_cast<int>(hi[3]), s1);
-                acc[t] = fmaf(d, static_cast<float>(s0 + s1), acc[t]);
+                int sl = 0;
+                int sh = *reinterpret_cast<const int*>(rec + G::kBiasOff + 4 * j);
+                sl = dp2a_lo_su(static_cast<int>(x0.x), lo[0], sl);
+                sl = dp2a_hi_su(static_cast<int>(x0.y), lo[0], sl);
+                sl = dp2a_lo_su(static_cast<int>(x0.z), lo[1], sl);
+                sl = dp2a_hi_su(static_cast<int>(x0.w), lo[1], sl);
+                sh = dp2a_lo_su(static_cast<int>(x2.x), hi[0], sh);
+                sh = dp2a_hi_su(static_cast<int>(x2.y), hi[0], sh);
+                sh = dp2a_lo_su(static_cast<int>(x2.z), hi[1], sh);
+                sh = dp2a_hi_su(static_cast<int>(x2.w), hi[1], sh);
+                sl = dp2a_lo_su(static_cast<int>(x1.x), lo[2], sl);
+                sl = dp2a_hi_su(static_cast<int>(x1.y), lo[2], sl);
+                sl = dp2a_lo_su(static_cast<int>(x1.z), lo[3], sl);
+                sl = dp2a_hi_su(static_cast<int>(x1.w), lo[3], sl);
+                sh = dp2a_lo_su(static_cast<int>(x3.x), hi[2], sh);
+                sh = dp2a_hi_su(static_cast<int>(x3.y), hi[2], sh);
+                sh = dp2a_lo_su(static_cast<int>(x3.z), hi[3], sh);
+                sh = dp2a_hi_su(static_cast<int>(x3.w), hi[3], sh);
+                acc[t] = fmaf(d, static_cast<float>(16 * sl + sh), acc[t]);
             }
         } else {
             uint32_t q[8];
@@ -294,8 +413,8 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xre
     }
 #pragma unroll
     for (int t = 0; t < kNT; ++t) {
-        const int e = *reinterpret_cast<const int*>(xrec0 + t * rec_stride + G::kWPC * 2);
-        out[t] = ldexpf(acc[t], e);
+        const float2 sc = *reinterpret_cast<const float2*>(xrec0 + t * rec_stride + G::kScaleOff);
+        out[t] = fmaf(acc[t] * sc.x, sc.y, out[t]);
     }
 }
 
@@ -304,19 +423,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     using G = Geo<kType>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* raw = smem;
-    uint8_t* xbuf = raw + kStages * G::kStageBytes;
-    const int64_t xbytes = static_cast<int64_t>(kNT) * P.max_c * G::kXRec;
-    float* partial = reinterpret_cast<float*>(xbuf + xbytes);     // [2][kThreads][kNT]
-    float* carry = partial + 2 * kThreads * kNT;                  // [2][kNT]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(carry + 2 * kNT + 2);   // 8-byte aligned
+    constexpr int S = ring_stages<kNT>();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* ring = smem + warp * S * G::kStageBytes;                    // this warp's stages
+    uint8_t* xbuf = smem + kWarps * S * G::kStageBytes;
+    const int rec_stride = P.max_c * G::kXRec;
+    // Partial row sums of k-split items: [item < kWarps][row][token].
+    float* red = reinterpret_cast<float*>(xbuf + kNT * rec_stride);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(red + kWarps * kTileRows * kNT) + warp * S;
 
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_addr(&bars[s]), 1);
         fence_mbar_init();
     }
-    __syncthreads();
+    __syncwarp();
 
     // This CTA's rows: from the first row starting at or after byte c*T/G to the first
     // row starting at or after byte (c+1)*T/G.
@@ -324,97 +445,117 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     int64_t r0, r1;
     row_at_byte(P, P.total_bytes * blockIdx.x / gridDim.x, p0, r0);
     row_at_byte(P, P.total_bytes * (blockIdx.x + 1) / gridDim.x, p1, r1);
+    const Segment first = find_segment(P, p0, r0, p1, r1);
 
-    Cursor prod, cons;
-    open_segment(P, prod, p0, r0, p1, r1);
-    cons = prod;
-
+    // Producer side of this warp's ring: the cursor's tile rows, one column group (up to 8
+    // chunks) each. When a column group is a whole row, the tile's rows are contiguous in
+    // memory and one copy fills the stage; otherwise one copy per row.
+    WarpCursor prod;
+    cursor_enter(P, prod, first, warp, p1, r1);
     int issued = 0;
     auto issue = [&](int s) {
-        const GemvProb& pr = P.p[prod.p];
-        const int cnt = static_cast<int>(min(static_cast<int64_t>(kThreads), prod.n_chunks - prod.chunk));
-        const uint32_t bytes = static_cast<uint32_t>(cnt) * G::kChunkBytes;
-        const uint8_t* src =
-            pr.W + prod.r_begin * pr.row_bytes + prod.chunk * G::kChunkBytes;
+        const GemvProb& pr = P.p[prod.seg.p];
+        const int tile = prod.item / prod.plan.ksplit;
+        const int64_t row0 = prod.seg.rb + static_cast<int64_t>(tile) * kTileRows;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(kTileRows), prod.seg.re - row0));
+        const int c0 = kLanesPerRow * prod.cs;
+        const int nc = min(kLanesPerRow, pr.C - c0);
+        const uint32_t row_copy = static_cast<uint32_t>(nc * G::kChunkBytes);
         const uint32_t bar = smem_addr(&bars[s]);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s_evict_first(smem_addr(raw + s * G::kStageBytes), src, bytes, bar);
-        advance(P, prod, p1, r1);
+        const uint32_t dst = smem_addr(ring + s * G::kStageBytes);
+        const uint8_t* src = pr.W + row0 * pr.row_bytes + static_cast<int64_t>(c0) * G::kChunkBytes;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, row_copy * rows);
+            if (pr.C <= kLanesPerRow) {
+                bulk_g2s_evict_first(dst, src, row_copy * rows, bar);
+            } else {
+                for (int r = 0; r < rows; ++r)
+                    bulk_g2s_evict_first(dst + r * G::kRowStride, src + r * pr.row_bytes,
+                                         row_copy, bar);
+            }
+        }
+        cursor_advance(P, prod, warp, p1, r1);
         ++issued;
     };
-    if (tid == 0)
-        for (int s = 0; s < kStages && prod.valid; ++s) issue(s);
+    for (int s = 0; s < S && prod.valid; ++s) issue(s);
 
-    int stage = 0;
-    int cur_prob = -1;
-    bool failed = false;
-    const int rec_stride = P.max_c * G::kXRec;
-    while (cons.valid) {
-        const GemvProb& pr = P.p[cons.p];
-        if (cons.p != cur_prob) {
-            prepare_x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
-            __syncthreads();
-            cur_prob = cons.p;
-        }
-        const int s = stage % kStages;
-        const int cnt = static_cast<int>(min(static_cast<int64_t>(kThreads), cons.n_chunks - cons.chunk));
-        const bool ok = mbar_wait(smem_addr(&bars[s]), (stage / kStages) & 1);
-        float part[kNT];
+    // Consumer side: all warps walk the CTA's segments together (x16 is per problem);
+    // inside a segment each warp works through its own tiles.
+    const int lc = lane % kLanesPerRow;   // which chunk of the column group this lane takes
+    const int rrow = lane / kLanesPerRow; // which row of the tile
+    int consumed = 0;
+    bool timed_out = false;
+    for (Segment seg = first; seg.valid; seg = find_segment(P, seg.p + 1, 0, p1, r1)) {
+        if (__syncthreads_or(timed_out)) break;   // previous segment done everywhere
+        const GemvProb& pr = P.p[seg.p];
+        prepare_x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
+        __syncthreads();
+        const SegPlan sp = plan_segment(seg.re - seg.rb, pr.C);
+        for (int item = warp; item < sp.items && !timed_out; item += kWarps) {
+            const int tile = item / sp.ksplit;
+            int cb, ce;
+            kgroup_range(sp, item % sp.ksplit, cb, ce);
+            const int64_t row0 = seg.rb + static_cast<int64_t>(tile) * kTileRows;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(kTileRows), seg.re - row0));
+            float acc[kNT];
 #pragma unroll
-        for (int t = 0; t < kNT; ++t) part[t] = 0.0f;
-        if (ok && tid < cnt) {
-            const int64_t g = cons.chunk + tid;            // chunk index within segment
-            const int col = static_cast<int>(g % pr.C);
-            chunk_dot<kType, kNT>(raw + s * G::kStageBytes + tid * G::kChunkBytes,
-                                  xbuf + col * G::kXRec, rec_stride, part);
-        }
-        float* pbuf = partial + (stage & 1) * kThreads * kNT;
-#pragma unroll
-        for (int t = 0; t < kNT; ++t) pbuf[tid * kNT + t] = part[t];
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        // Row sums in k order; a row cut by the stage end carries into the next stage.
-        {
-            const int64_t s0 = cons.chunk;
-            const int64_t C = pr.C;
-            const int64_t r_first = s0 / C;
-            const int nrows = static_cast<int>((s0 + cnt - 1) / C - r_first + 1);
-            const float* cin = carry + ((stage + 1) & 1) * kNT;
-            float* cout = carry + (stage & 1) * kNT;
-            for (int rr = tid; rr < nrows; rr += kThreads) {
-                const int64_t r = r_first + rr;
-                const int64_t cb = max(s0, r * C);
-                const int64_t ce = min(s0 + cnt, (r + 1) * C);
-                float acc[kNT];
-#pragma unroll
-                for (int t = 0; t < kNT; ++t) acc[t] = cb > r * C ? cin[t] : 0.0f;
-                for (int64_t c = cb; c < ce; ++c) {
-#pragma unroll
-                    for (int t = 0; t < kNT; ++t) acc[t] += pbuf[(c - s0) * kNT + t];
+            for (int t = 0; t < kNT; ++t) acc[t] = 0.0f;
+            for (int cs = cb; cs < ce; ++cs) {
+                const int s = consumed % S;
+                if (!mbar_wait(smem_addr(&bars[s]), (consumed / S) & 1)) {
+                    timed_out = true;
+                    break;
                 }
-                if (ce == (r + 1) * C) {
-                    const int64_t row = cons.r_begin + r;
+                const int col = kLanesPerRow * cs + lc;
+                // Whole-row stages hold rows at their global stride; others at kRowStride.
+                const int rs = pr.C <= kLanesPerRow ? static_cast<int>(pr.row_bytes) : G::kRowStride;
+                if (rrow < rows && col < pr.C)
+                    chunk_dot<kType, kNT>(ring + s * G::kStageBytes + rrow * rs +
+                                              lc * G::kChunkBytes,
+                                          xbuf + col * G::kXRec, rec_stride, acc);
+                __syncwarp();
+                ++consumed;
+                if (prod.valid) issue(s);   // refill the stage just read
+            }
+            if (timed_out) break;
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+#pragma unroll
+                for (int o = 1; o < kLanesPerRow; o <<= 1)
+                    acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+            }
+            if (lc == 0 && rrow < rows) {
+                if (sp.ksplit == 1) {
 #pragma unroll
                     for (int t = 0; t < kNT; ++t)
-                        if (t < P.n_tok) pr.Y[t * pr.M + row] = acc[t];
+                        if (t < P.n_tok) pr.Y[t * pr.M + row0 + rrow] = acc[t];
                 } else {
 #pragma unroll
-                    for (int t = 0; t < kNT; ++t) cout[t] = acc[t];
+                    for (int t = 0; t < kNT; ++t) red[(item * kTileRows + rrow) * kNT + t] = acc[t];
                 }
             }
         }
-        if (tid == 0 && prod.valid) issue(s);
-        advance(P, cons, p1, r1);
-        ++stage;
+        if (sp.ksplit > 1) {
+            // Sum the k-groups of each row in group order (deterministic).
+            if (__syncthreads_or(timed_out)) break;
+            const int n_out = sp.ntiles * kTileRows * kNT;
+            for (int idx = threadIdx.x; idx < n_out; idx += kThreads) {
+                const int t = idx % kNT;
+                const int rr = (idx / kNT) % kTileRows;
+                const int tile = idx / (kNT * kTileRows);
+                const int64_t row = seg.rb + static_cast<int64_t>(tile) * kTileRows + rr;
+                if (row >= seg.re || t >= P.n_tok) continue;
+                float v = 0.0f;
+                for (int kg = 0; kg < sp.ksplit; ++kg)
+                    v += red[((tile * sp.ksplit + kg) * kTileRows + rr) * kNT + t];
+                pr.Y[t * pr.M + row] = v;
+            }
+        }
     }
-    if (failed && tid == 0) {
-        report_status(P.status, kStatusTimeout);
-        // Let copies already in flight land before this CTA's shared memory is released.
-        for (int st = stage; st < issued; ++st)
-            mbar_wait(smem_addr(&bars[st % kStages]), (st / kStages) & 1, 100000000ull);
-    }
+    if (timed_out && lane == 0) report_status(P.status, kStatusTimeout);
+    // Copies still in flight (only after a timeout) must land before the CTA exits.
+    for (int i = consumed; i < issued; ++i)
+        mbar_wait(smem_addr(&bars[i % S]), (i / S) & 1, 100000000ull);
 }
 
 // Any K % 32 == 0: one warp per row, lanes over blocks, fp32 FMA, xor-shuffle reduction
@@ -475,9 +616,11 @@ gemv_generic_kernel(const uint8_t* __restrict__ W, int64_t M, int64_t K,
 template <int kType>
 int64_t stream_smem_bytes(int n_tok_template, int max_c) {
     using G = Geo<kType>;
-    return static_cast<int64_t>(kStages) * G::kStageBytes +
+    const int stages = n_tok_template <= 3 ? GQ_GEMV_STAGES : GQ_GEMV_STAGES_N4;
+    return static_cast<int64_t>(kWarps) * stages * G::kStageBytes +
            static_cast<int64_t>(n_tok_template) * max_c * G::kXRec +
-           (2 * kThreads * n_tok_template + 2 * n_tok_template + 2) * 4 + kStages * 8 + 8;
+           static_cast<int64_t>(kWarps) * kTileRows * n_tok_template * 4 +
+           static_cast<int64_t>(kWarps) * stages * 8;
 }
 
 // cudaFuncSetAttribute once per (kernel, device) for the largest size asked so far.
@@ -497,10 +640,10 @@ cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
 }
 
 template <int kType, int kNT, int kMaxProbs>
-cudaError_t launch_stream_t(const GemvParams<kMaxProbs>& P, const DeviceInfo* info,
-                            cudaStream_t s) {
+cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
     auto kernel = gemv_stream_kernel<kType, kNT, kMaxProbs>;
     const int64_t smem = stream_smem_bytes<kType>(kNT, P.max_c);
+    if (smem > info->max_smem_optin) return cudaErrorInvalidValue;   // see stream_eligible
     cudaError_t e = ensure_smem(kernel, info->device, smem);
     if (e != cudaSuccess) return e;
     // Enough CTAs that each streams at least ~32 KB, at most one per SM.
@@ -511,8 +654,7 @@ cudaError_t launch_stream_t(const GemvParams<kMaxProbs>& P, const DeviceInfo* in
 }
 
 template <int kType, int kMaxProbs>
-cudaError_t launch_stream_nt(const GemvParams<kMaxProbs>& P, const DeviceInfo* info,
-                             cudaStream_t s) {
+cudaError_t launch_stream_nt(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
     switch (P.n_tok) {
         case 1: return launch_stream_t<kType, 1, kMaxProbs>(P, info, s);
         case 2: return launch_stream_t<kType, 2, kMaxProbs>(P, info, s);
@@ -566,10 +708,10 @@ cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_t
 }
 
 bool stream_eligible(gq_type t, const MatProblem& p, const DeviceInfo* info) {
-    if (p.K % 256 != 0 || p.K > (int64_t(1) << 30)) return false;
+    if (p.K % 256 != 0 || p.K > (int64_t(1) << 24)) return false;
     if (reinterpret_cast<uintptr_t>(p.X) % 16 != 0) return false;
     if (reinterpret_cast<uintptr_t>(p.W) % 16 != 0) return false;
-    const int64_t c = p.K / (t == GQ_TYPE_Q4_0 ? 256 : 128);
+    const int c = static_cast<int>(p.K / (t == GQ_TYPE_Q4_0 ? 256 : 128));
     const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0>(kMaxTok, c)
                                            : stream_smem_bytes<GQ_TYPE_Q8_0>(kMaxTok, c);
     return smem <= info->max_smem_optin;
@@ -583,10 +725,9 @@ cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_
     cudaError_t e = current_device_info(&info);
     if (e != cudaSuccess) return e;
     MatProblem fast[GQ_MAX_BATCH];
-    int n_fast = 0;
     for (int64_t tok0 = 0; tok0 < N; tok0 += kMaxTok) {
         const int n_tok = static_cast<int>(std::min<int64_t>(kMaxTok, N - tok0));
-        n_fast = 0;
+        int n_fast = 0;
         for (int i = 0; i < count; ++i) {
             if (stream_eligible(t, probs[i], info)) {
                 fast[n_fast++] = probs[i];
