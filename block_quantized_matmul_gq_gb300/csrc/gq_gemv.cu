@@ -184,17 +184,28 @@ __device__ __forceinline__ void kgroup_range(const SegPlan& sp, int kg, int& cb,
 struct WarpCursor {
     Segment seg;
     SegPlan plan;
-    int item;
+    int item, tile;
     int cs, ce;           // current column group and end of the item's range
     bool valid;
 };
 
+// Tile and column-group range of the cursor's item. No division when ksplit == 1, the
+// common case (every stage of a K <= 2048 Q4_0 problem is its own item).
+__device__ __forceinline__ void item_bounds(const SegPlan& sp, int item, int& tile, int& cb,
+                                            int& ce) {
+    if (sp.ksplit == 1) {
+        tile = item;
+        cb = 0;
+        ce = sp.ncs;
+    } else {
+        tile = item / sp.ksplit;
+        kgroup_range(sp, item - tile * sp.ksplit, cb, ce);
+    }
+}
+
 template <int kMaxProbs>
 __device__ void cursor_item(const GemvParams<kMaxProbs>& P, WarpCursor& c) {
-    int cb, ce;
-    kgroup_range(c.plan, c.item % c.plan.ksplit, cb, ce);
-    c.cs = cb;
-    c.ce = ce;
+    item_bounds(c.plan, c.item, c.tile, c.cs, c.ce);
 }
 
 template <int kMaxProbs>
@@ -455,8 +466,7 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     int issued = 0;
     auto issue = [&](int s) {
         const GemvProb& pr = P.p[prod.seg.p];
-        const int tile = prod.item / prod.plan.ksplit;
-        const int64_t row0 = prod.seg.rb + static_cast<int64_t>(tile) * kTileRows;
+        const int64_t row0 = prod.seg.rb + static_cast<int64_t>(prod.tile) * kTileRows;
         const int rows = static_cast<int>(min(static_cast<int64_t>(kTileRows), prod.seg.re - row0));
         const int c0 = kLanesPerRow * prod.cs;
         const int nc = min(kLanesPerRow, pr.C - c0);
@@ -492,9 +502,8 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
         __syncthreads();
         const SegPlan sp = plan_segment(seg.re - seg.rb, pr.C);
         for (int item = warp; item < sp.items && !timed_out; item += kWarps) {
-            const int tile = item / sp.ksplit;
-            int cb, ce;
-            kgroup_range(sp, item % sp.ksplit, cb, ce);
+            int tile, cb, ce;
+            item_bounds(sp, item, tile, cb, ce);
             const int64_t row0 = seg.rb + static_cast<int64_t>(tile) * kTileRows;
             const int rows = static_cast<int>(min(static_cast<int64_t>(kTileRows), seg.re - row0));
             float acc[kNT];
@@ -707,13 +716,18 @@ cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_t
     return cudaGetLastError();
 }
 
-bool stream_eligible(gq_type t, const MatProblem& p, const DeviceInfo* info) {
+// Shapes and pointers the streaming kernel takes at all (any token count).
+bool stream_shape_ok(const MatProblem& p) {
     if (p.K % 256 != 0 || p.K > (int64_t(1) << 24)) return false;
     if (reinterpret_cast<uintptr_t>(p.X) % 16 != 0) return false;
-    if (reinterpret_cast<uintptr_t>(p.W) % 16 != 0) return false;
+    return reinterpret_cast<uintptr_t>(p.W) % 16 == 0;
+}
+
+// Whether the shared-memory plan for `n_tok` tokens of this problem fits the device.
+bool stream_fits(gq_type t, const MatProblem& p, int n_tok, const DeviceInfo* info) {
     const int c = static_cast<int>(p.K / (t == GQ_TYPE_Q4_0 ? 256 : 128));
-    const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0>(kMaxTok, c)
-                                           : stream_smem_bytes<GQ_TYPE_Q8_0>(kMaxTok, c);
+    const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0>(n_tok, c)
+                                           : stream_smem_bytes<GQ_TYPE_Q8_0>(n_tok, c);
     return smem <= info->max_smem_optin;
 }
 
@@ -725,11 +739,23 @@ cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_
     cudaError_t e = current_device_info(&info);
     if (e != cudaSuccess) return e;
     MatProblem fast[GQ_MAX_BATCH];
-    for (int64_t tok0 = 0; tok0 < N; tok0 += kMaxTok) {
-        const int n_tok = static_cast<int>(std::min<int64_t>(kMaxTok, N - tok0));
+    int64_t step = 0;
+    for (int64_t tok0 = 0; tok0 < N; tok0 += step) {
+        // Tokens in this pass: as many as the x16 buffers of the streamable problems allow
+        // (up to kMaxTok); a problem that does not fit even one token goes to the generic
+        // kernel.
+        int n_tok = static_cast<int>(std::min<int64_t>(kMaxTok, N - tok0));
+        for (; n_tok > 1; --n_tok) {
+            bool all_fit = true;
+            for (int i = 0; i < count && all_fit; ++i)
+                if (stream_shape_ok(probs[i]) && stream_fits(t, probs[i], 1, info))
+                    all_fit = stream_fits(t, probs[i], n_tok, info);
+            if (all_fit) break;
+        }
+        step = n_tok;
         int n_fast = 0;
         for (int i = 0; i < count; ++i) {
-            if (stream_eligible(t, probs[i], info)) {
+            if (stream_shape_ok(probs[i]) && stream_fits(t, probs[i], n_tok, info)) {
                 fast[n_fast++] = probs[i];
             } else {
                 e = launch_generic(t, probs[i], tok0, n_tok, info, s);
