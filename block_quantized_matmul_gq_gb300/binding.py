@@ -32,8 +32,8 @@ STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
 
 # Every symbol declared in include/gq.h.
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
-           "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_batched",
-           "gq_get_last_error", "gq_status_string")
+           "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
+           "gq_mul_mat_ws", "gq_mul_mat_batched", "gq_get_last_error", "gq_status_string")
 
 
 class Problem(ctypes.Structure):
@@ -57,6 +57,10 @@ def load(path: str = LIB_PATH):
     L.gq_dequantize.restype = ctypes.c_int
     L.gq_mul_mat.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp]
     L.gq_mul_mat.restype = ctypes.c_int
+    L.gq_mul_mat_workspace_size.argtypes = [ctypes.c_int, i64, i64, i64]
+    L.gq_mul_mat_workspace_size.restype = ctypes.c_size_t
+    L.gq_mul_mat_ws.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp, ctypes.c_size_t, vp]
+    L.gq_mul_mat_ws.restype = ctypes.c_int
     L.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
     L.gq_mul_mat_batched.restype = ctypes.c_int
     L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
@@ -145,6 +149,27 @@ def mul_mat(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
     _check(lib.gq_mul_mat(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
                           _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
                           _stream(stream)), "gq_mul_mat")
+    return out
+
+
+def workspace_size(t, M: int, K: int, N: int) -> int:
+    return int(lib.gq_mul_mat_workspace_size(_type(t), M, K, N))
+
+
+def mul_mat_ws(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
+               workspace: torch.Tensor | None, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """mul_mat with a caller-owned workspace (uint8 CUDA tensor of workspace_size bytes)."""
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    N = X.shape[0]
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    wp = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    wn = workspace.numel() if workspace is not None else 0
+    _check(lib.gq_mul_mat_ws(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
+                             _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
+                             wp, wn, _stream(stream)), "gq_mul_mat_ws")
     return out
 
 

@@ -3,7 +3,9 @@
 // bounded wait runs out.
 #include <climits>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "gq_device.cuh"
 #include "gq_internal.h"
@@ -85,6 +87,54 @@ gq_status check_problem(const void* W, gq_type t, int64_t M, int64_t K, const fl
     return GQ_OK;
 }
 
+// Library-owned workspace of the prefill path, one buffer per (device, stream), grown on
+// demand. Growing waits for the stream's queued work (which may still read the old buffer)
+// and is refused while the stream is being captured into a graph.
+cudaError_t internal_workspace(cudaStream_t s, size_t bytes, void** out) {
+    static std::mutex mu;
+    static std::map<std::pair<int, void*>, std::pair<void*, size_t>> buffers;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto& entry = buffers[std::make_pair(dev, static_cast<void*>(s))];
+    if (entry.second >= bytes) {
+        *out = entry.first;
+        return cudaSuccess;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return e;
+    if (cap != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (entry.first) cudaFree(entry.first);
+    entry = {nullptr, 0};
+    void* p = nullptr;
+    e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) return e;
+    entry = {p, bytes};
+    *out = p;
+    return cudaSuccess;
+}
+
+// Runs one validated, non-empty problem (K > 0): tensor cores when the shape qualifies,
+// else the decode kernels. `ws` may be NULL (library workspace is used then).
+gq_status run_one(gq_type t, const gq::MatProblem& p, int64_t N, void* ws, size_t ws_bytes,
+                  cudaStream_t s) {
+    if (gq::gemm_eligible(t, p, N)) {
+        const size_t need = static_cast<size_t>(gq::gemm_workspace_bytes(p.K, N));
+        void* w = ws;
+        if (w == nullptr) {
+            if (internal_workspace(s, need, &w) != cudaSuccess) return GQ_ERR_CUDA;
+        } else if (ws_bytes < need || !aligned(ws, 256)) {
+            return ws_bytes < need ? GQ_ERR_SHAPE : GQ_ERR_ALIGN;
+        }
+        return from_cuda(gq::launch_gemm(t, p, N, w, s));
+    }
+    return from_cuda(gq::launch_mul_mat(t, &p, 1, N, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -129,7 +179,26 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return from_cuda(cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s));
     gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
-    return from_cuda(gq::launch_mul_mat(t, &p, 1, N, s));
+    return run_one(t, p, N, nullptr, 0, s);
+}
+
+size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N) {
+    if (!known_type(t) || check_shape(M, K, N) != GQ_OK || M == 0 || N == 0 || K == 0) return 0;
+    gq::MatProblem p{reinterpret_cast<const uint8_t*>(uintptr_t(256)), nullptr, nullptr, M, K};
+    return gq::gemm_eligible(t, p, N) ? static_cast<size_t>(gq::gemm_workspace_bytes(K, N)) : 0;
+}
+
+gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K, const float* X,
+                        int64_t N, float* Y, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    bool empty = false;
+    gq_status st = check_problem(W_blocks, t, M, K, X, N, Y, &empty);
+    if (st != GQ_OK || empty) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s));
+    gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
+    if (gq::gemm_eligible(t, p, N) && workspace == nullptr) return GQ_ERR_NULL;
+    return run_one(t, p, N, workspace, workspace_bytes, s);
 }
 
 gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
@@ -157,8 +226,19 @@ gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, 
             run[n_launch++] = run[i];
         }
     }
-    if (n_launch == 0) return GQ_OK;
-    return from_cuda(gq::launch_mul_mat(t, run, n_launch, N, s));
+    // Problems that qualify for the tensor-core path run one after another on the stream
+    // (sharing the library workspace); the rest share one decode launch.
+    int n_decode = 0;
+    for (int i = 0; i < n_launch; ++i) {
+        if (gq::gemm_eligible(t, run[i], N)) {
+            gq_status st = run_one(t, run[i], N, nullptr, 0, s);
+            if (st != GQ_OK) return st;
+        } else {
+            run[n_decode++] = run[i];
+        }
+    }
+    if (n_decode == 0) return GQ_OK;
+    return from_cuda(gq::launch_mul_mat(t, run, n_decode, N, s));
 }
 
 gq_status gq_get_last_error(void* stream) {

@@ -1,0 +1,466 @@
+// gq_gemm.cu -- prefill mul_mat on the 5th-generation tensor cores:
+//     Y[n][m] = sum_k What[m][k] * X[n][k]        (Y = X . What^T, fp32 out)
+//
+// At prefill the product is a dense contraction ("No Python! Building an AI Inference
+// Engine Exclusively in C++", section 6: over 90% of inference compute is GEMM), so it
+// runs on tcgen05 tensor cores with bf16 operands and fp32 accumulation in TMEM. The
+// weights stay block-quantized in HBM and are dequantized inside the kernel right after
+// they are loaded ("Development Guide for Small AI Models (TinyLLaMA, etc.) Using C++",
+// section 6.2; "No Python! ...", section 9).
+//
+// One CTA computes a 128 (weight rows) x kBN (tokens) tile of Y^T over all of K:
+//   warp 0      TMA producer: raw weight blocks (2-D tensor map over the block bytes,
+//               one 256-k "super-step" = 8 blocks per row per copy) and bf16 X tiles
+//               (64 k x kBN tokens, 128-byte swizzle) into rings of shared-memory stages.
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=kBN, K=16),
+//               four per 64-k stage, and commits each stage back to the producers.
+//   warps 2..5  dequantize: thread = row; per 64-k stage it turns its row's two blocks
+//               into 64 bf16 values, each (c - 8) * d (or c * d) computed exactly in fp32
+//               and rounded once to bf16, and stores them in the 128-byte-swizzled K-major
+//               layout the MMA reads. After the K loop the same warps read the accumulator
+//               out of TMEM (tcgen05.ld, warp w owns lanes 32*(w%4)..) and write Y.
+// X is converted to bf16 once per call by x_to_bf16_kernel into caller- or library-owned
+// workspace (N x K bf16), which the tensor map reads.
+// All waits are bounded; a CTA that gives up sets the device status word, lets its own
+// copies and MMAs land, frees its TMEM and leaves.
+#include <cuda.h>            // CUtensorMap and its enums (header only; no libcuda link)
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gq_device.cuh"
+#include "gq_internal.h"
+#include "gq_umma.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int kBM = 128;          // weight rows per tile (MMA M)
+constexpr int kBK = 64;           // k per MMA stage: 128 bytes of bf16 = one swizzle row
+constexpr int kSuperK = 256;      // k per raw-weight copy: 8 blocks per row
+constexpr int kRawStages = 2;
+constexpr int kThreads = 192;     // 6 warps
+constexpr unsigned long long kDrainNs = 100000000ull;   // 100 ms
+
+template <int kType>
+struct RawFmt;
+template <>
+struct RawFmt<GQ_TYPE_Q4_0> {
+    static constexpr int kBB = kQ4Bytes;
+    static constexpr int kRow = 8 * kQ4Bytes;   // 144 bytes per row per super-step
+    static constexpr int kElem = 1;             // tensor-map element size (uint8)
+};
+template <>
+struct RawFmt<GQ_TYPE_Q8_0> {
+    static constexpr int kBB = kQ8Bytes;
+    static constexpr int kRow = 8 * kQ8Bytes;   // 272 bytes
+    static constexpr int kElem = 2;             // uint16 elements keep the box <= 256
+};
+
+template <int kType, int kBN>
+struct Layout {
+    static constexpr int kStages = kBN >= 128 ? 3 : 6;
+    static constexpr int kA = kBM * kBK * 2;
+    static constexpr int kB = kBN * kBK * 2;
+    static constexpr int kRaw = kBM * RawFmt<kType>::kRow;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kA;
+    static constexpr int kOffRaw = kOffB + kStages * kB;
+    static constexpr int kOffBar = kOffRaw + kRawStages * kRaw;
+    static constexpr int kNumBars = 3 * kStages + 2 * kRawStages + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;   // room to align the base to 1024
+    static constexpr int kTmemCols = kBN < 32 ? 32 : kBN;
+    static_assert(kB % 1024 == 0 && kA % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned stages");
+};
+
+__device__ __forceinline__ uint32_t word_at(const uint32_t* r, int byte_off) {
+    const int w = byte_off >> 2;
+    return (byte_off & 3) ? __funnelshift_r(r[w], r[w + 1], 16) : r[w];
+}
+
+__device__ __forceinline__ uint32_t u16_at(const uint32_t* r, int byte_off) {
+    const int w = byte_off >> 2;
+    return (byte_off & 3) ? (r[w] >> 16) : (r[w] & 0xFFFFu);
+}
+
+// Byte k (0..3) of `word` as the float 2^23 + byte: the byte lands in the low mantissa.
+template <int k>
+__device__ __forceinline__ float byte_as_float(uint32_t word) {
+    return __int_as_float(static_cast<int>(__byte_perm(word, 0x4B000000u, 0x7540u | k)));
+}
+
+// Dequantizes blocks 2q and 2q+1 of a row's super-step (raw bytes in r) into 64 bf16
+// values, packed in pairs: out[i] holds elements 2i (low half) and 2i+1 (high half).
+// Each value is (c - 8) * d (Q4_0) or c * d (Q8_0), exact in fp32, rounded once to bf16.
+template <int kType, int q>
+__device__ __forceinline__ void dequant_kstep(const uint32_t* r, uint32_t (&out)[32]) {
+    constexpr int kBB = RawFmt<kType>::kBB;
+#pragma unroll
+    for (int bl = 0; bl < 2; ++bl) {
+        const int base = (2 * q + bl) * kBB;
+        const float d = half_bits_to_float(u16_at(r, base));
+        float v[32];
+        if constexpr (kType == GQ_TYPE_Q4_0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = word_at(r, base + 2 + 4 * i);
+                const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 4i..4i+3
+                const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 16+4i..
+                v[4 * i + 0] = byte_as_float<0>(lo);
+                v[4 * i + 1] = byte_as_float<1>(lo);
+                v[4 * i + 2] = byte_as_float<2>(lo);
+                v[4 * i + 3] = byte_as_float<3>(lo);
+                v[16 + 4 * i + 0] = byte_as_float<0>(hi);
+                v[16 + 4 * i + 1] = byte_as_float<1>(hi);
+                v[16 + 4 * i + 2] = byte_as_float<2>(hi);
+                v[16 + 4 * i + 3] = byte_as_float<3>(hi);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = (v[e] - 8388616.0f) * d;   // 2^23 + 8
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w = word_at(r, base + 2 + 4 * i) ^ 0x80808080u;   // c + 128
+                v[4 * i + 0] = byte_as_float<0>(w);
+                v[4 * i + 1] = byte_as_float<1>(w);
+                v[4 * i + 2] = byte_as_float<2>(w);
+                v[4 * i + 3] = byte_as_float<3>(w);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = (v[e] - 8388736.0f) * d;   // 2^23 + 128
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            out[16 * bl + i] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+    }
+}
+
+template <int kType, int kBN>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+            int M, int N, int K, float* __restrict__ Y, unsigned* status) {
+    using L = Layout<kType, kBN>;
+    constexpr int S = L::kStages;
+    constexpr int kRawWords = RawFmt<kType>::kRow / 4;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_addr - raw_addr);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t sA = base_addr + L::kOffA;
+    const uint32_t sB = base_addr + L::kOffB;
+    const uint32_t sRaw = base_addr + L::kOffRaw;
+    const uint32_t bar0 = base_addr + L::kOffBar;
+    // barrier order: a_full[S], b_full[S], empty[S], raw_full[R], raw_empty[R], acc_full
+    auto a_full = [&](int s) { return bar0 + 8u * s; };
+    auto b_full = [&](int s) { return bar0 + 8u * (S + s); };
+    auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto raw_full = [&](int r) { return bar0 + 8u * (3 * S + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (3 * S + kRawStages + r); };
+    const uint32_t acc_full = bar0 + 8u * (3 * S + 2 * kRawStages);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
+
+    const int m0 = blockIdx.x * kBM;
+    const int n0 = blockIdx.y * kBN;
+    const int nk = K / kBK;
+    const int nsuper = K / kSuperK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(a_full(s), 128);
+            mbar_init(b_full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int r = 0; r < kRawStages; ++r) {
+            mbar_init(raw_full(r), 1);
+            mbar_init(raw_empty(r), 128);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_w);
+            prefetch_tensormap(&tmap_x);
+            int raw_issued = 0, b_issued = 0;
+            bool ok = true;
+            for (int ks = 0; ks < nk && ok; ++ks) {
+                // Raw weights run one super-step ahead of the k-stages that use them.
+                const int want = min(ks / 4 + 2, nsuper);
+                while (raw_issued < want) {
+                    const int j = raw_issued, r = j % kRawStages;
+                    if (!mbar_wait(raw_empty(r), ((j / kRawStages) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(raw_full(r), L::kRaw);
+                    tma_load_2d(sRaw + r * L::kRaw, &tmap_w,
+                                j * (RawFmt<kType>::kRow / RawFmt<kType>::kElem), m0, raw_full(r));
+                    ++raw_issued;
+                }
+                if (!ok) break;
+                const int s = ks % S;
+                if (!mbar_wait(empty(s), ((ks / S) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(b_full(s), L::kB);
+                tma_load_2d(sB + s * L::kB, &tmap_x, ks * kBK, n0, b_full(s));
+                ++b_issued;
+            }
+            if (!ok) report_status(status, kStatusTimeout);
+            // Every copy this thread issued must land before the CTA's memory is released.
+            for (int i = max(0, b_issued - S); i < b_issued; ++i)
+                mbar_wait(b_full(i % S), (i / S) & 1, kDrainNs);
+            for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
+                mbar_wait(raw_full(j % kRawStages), (j / kRawStages) & 1, kDrainNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+            bool ok = true;
+            for (int ks = 0; ks < nk; ++ks) {
+                const int s = ks % S;
+                const uint32_t ph = (ks / S) & 1;
+                if (!mbar_wait(a_full(s), ph) || !mbar_wait(b_full(s), ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t adesc = sw128_kmajor_desc(sA + s * L::kA + kk * 32);
+                    const uint64_t bdesc = sw128_kmajor_desc(sB + s * L::kB + kk * 32);
+                    umma_bf16(tmem, adesc, bdesc, idesc, (ks | kk) != 0 ? 1u : 0u);
+                }
+                umma_commit(empty(s));   // stage s is free once these MMAs have read it
+            }
+            umma_commit(acc_full);       // accumulator complete (also after a timeout)
+            if (!ok) report_status(status, kStatusTimeout);
+        }
+    } else {
+        // ---------------- dequantize, then epilogue ----------------
+        const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
+        const int row = quad * 32 + lane;       // tile row = TMEM lane
+        bool ok = true;
+        for (int j = 0; j < nsuper && ok; ++j) {
+            const int r = j % kRawStages;
+            if (!mbar_wait(raw_full(r), (j / kRawStages) & 1)) {
+                ok = false;
+                break;
+            }
+            uint32_t raw[kRawWords];
+            const uint8_t* src = base + L::kOffRaw + r * L::kRaw + row * RawFmt<kType>::kRow;
+#pragma unroll
+            for (int i = 0; i < kRawWords / 4; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
+                raw[4 * i] = v.x;
+                raw[4 * i + 1] = v.y;
+                raw[4 * i + 2] = v.z;
+                raw[4 * i + 3] = v.w;
+            }
+            mbar_arrive(raw_empty(r));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int ks = 4 * j + q;
+                const int s = ks % S;
+                if (!mbar_wait(empty(s), ((ks / S) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t packed[32];
+                if (q == 0) dequant_kstep<kType, 0>(raw, packed);
+                if (q == 1) dequant_kstep<kType, 1>(raw, packed);
+                if (q == 2) dequant_kstep<kType, 2>(raw, packed);
+                if (q == 3) dequant_kstep<kType, 3>(raw, packed);
+                // Row of 64 bf16 = eight 16-byte chunks; chunk c lands at c ^ (row % 8).
+                uint8_t* dst = base + L::kOffA + s * L::kA + row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) =
+                        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                                   packed[4 * c + 3]);
+                fence_proxy_async_smem();
+                mbar_arrive(a_full(s));
+            }
+        }
+        if (!ok) report_status(status, kStatusTimeout);
+        // Epilogue: accumulator rows are TMEM lanes, token columns are TMEM columns.
+        const bool done = mbar_wait(acc_full, 0);
+        tc_fence_after();
+        if (done && ok) {
+            const int m = m0 + row;
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+            const int ncols = min(kBN, N - n0);
+            for (int c = 0; c < ncols; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tbase + c, v);
+                if (m < M) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int n = n0 + c + jj;
+                        if (n < N) Y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[jj]);
+                    }
+                }
+            }
+        } else if (!done) {
+            report_status(status, kStatusTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+// X (fp32, n4 * 4 elements) -> bf16, round to nearest even.
+__global__ void __launch_bounds__(256)
+x_to_bf16_kernel(const float* __restrict__ X, int64_t n, __nv_bfloat16* __restrict__ out) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if ((reinterpret_cast<uintptr_t>(X) & 15) == 0) {
+        const int64_t n4 = n / 4;
+        for (int64_t i = i0; i < n4; i += stride) {
+            const float4 v = reinterpret_cast<const float4*>(X)[i];
+            __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + 4 * i);
+            o[0] = __floats2bfloat162_rn(v.x, v.y);
+            o[1] = __floats2bfloat162_rn(v.z, v.w);
+        }
+        for (int64_t i = 4 * n4 + i0; i < n; i += stride) out[i] = __float2bfloat16_rn(X[i]);
+    } else {
+        for (int64_t i = i0; i < n; i += stride) out[i] = __float2bfloat16_rn(X[i]);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+template <typename KernelT>
+cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int64_t> set_bytes;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), device);
+    auto it = set_bytes.find(key);
+    if (it != set_bytes.end() && it->second >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e == cudaSuccess) set_bytes[key] = bytes;
+    return e;
+}
+
+template <int kType, int kBN>
+cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* xb,
+                          const DeviceInfo* info, cudaStream_t s) {
+    using L = Layout<kType, kBN>;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t row_bytes = (p.K / 32) * RawFmt<kType>::kBB;
+    CUtensorMap tw{}, tx{};
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / RawFmt<kType>::kElem),
+                                    static_cast<cuuint64_t>(p.M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(RawFmt<kType>::kRow / RawFmt<kType>::kElem),
+                                   static_cast<cuuint32_t>(kBM)};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(&tw, kType == GQ_TYPE_Q4_0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                         2, const_cast<uint8_t*>(p.W), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K * 2)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBN)};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(xb),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    auto kernel = gemm_kernel<kType, kBN>;
+    cudaError_t e = ensure_smem(kernel, info->device, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>((p.M + kBM - 1) / kBM),
+                    static_cast<unsigned>((N + kBN - 1) / kBN));
+    kernel<<<grid, kThreads, L::kAlloc, s>>>(tw, tx, static_cast<int>(p.M), static_cast<int>(N),
+                                             static_cast<int>(p.K), p.Y, info->status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t gemm_workspace_bytes(int64_t K, int64_t N) {
+    return (N * K * 2 + 255) / 256 * 256;
+}
+
+bool gemm_eligible(gq_type t, const MatProblem& p, int64_t N) {
+    (void)t;
+    if (N < kGemmMinTokens || p.K % kSuperK != 0 || p.M <= 0) return false;
+    if (p.M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 24) || p.K > (int64_t(1) << 24))
+        return false;
+    return reinterpret_cast<uintptr_t>(p.W) % 16 == 0;
+}
+
+cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspace,
+                        cudaStream_t s) {
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(workspace);
+    const int64_t n = N * p.K;
+    const int grid = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256 + 1,
+                                                        int64_t(info->sm_count) * 8));
+    x_to_bf16_kernel<<<grid, 256, 0, s>>>(p.X, n, xb);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (t == GQ_TYPE_Q4_0) return launch_gemm_t<GQ_TYPE_Q4_0, 256>(p, N, xb, info, s);
+    return launch_gemm_t<GQ_TYPE_Q8_0, 256>(p, N, xb, info, s);
+}
+
+}  // namespace gq

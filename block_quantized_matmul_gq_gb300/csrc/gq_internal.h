@@ -39,8 +39,17 @@ cudaError_t launch_quantize(gq_type t, const float* W, int64_t n_blocks, uint8_t
 cudaError_t launch_dequantize(gq_type t, const uint8_t* blocks, int64_t n_elems, float* out,
                               cudaStream_t s);
 
-// Y = X . What^T for every problem; all share type t and N tokens.
+// Y = X . What^T for every problem on the decode (CUDA-core, streaming) kernels; all
+// share type t and N tokens.
 cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_t N,
                            cudaStream_t s);
+
+// Prefill path: tcgen05 tensor-core GEMM. Needs gemm_workspace_bytes(K, N) bytes of
+// device workspace (a bf16 copy of X), 256-byte aligned.
+constexpr int64_t kGemmMinTokens = 64;
+int64_t gemm_workspace_bytes(int64_t K, int64_t N);
+bool gemm_eligible(gq_type t, const MatProblem& p, int64_t N);
+cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspace,
+                        cudaStream_t s);
 
 }  // namespace gq

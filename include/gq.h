@@ -21,10 +21,10 @@
  *             means What = (c - 8) * d.
  *       Q8_0, 34 bytes: fp16 scale d, then 32 signed bytes c; What = c * d.
  *   - Pointers. Every array pointer is a DEVICE pointer owned by the caller; the library
- *     keeps none of them after the call returns and allocates no device memory on these
- *     paths. W_blocks must be 16-byte aligned, fp32 arrays 4-byte aligned (16-byte
- *     alignment of X is used when present). A pointer may be NULL only when its array is
- *     empty.
+ *     keeps none of them after the call returns. W_blocks must be 16-byte aligned, fp32
+ *     arrays 4-byte aligned (16-byte alignment of X is used when present). A pointer may
+ *     be NULL only when its array is empty. The decode path (N < 64) allocates nothing;
+ *     the tensor-core path needs a workspace (see gq_mul_mat_ws).
  *   - Streams. `stream` is a cudaStream_t (NULL = the legacy default stream) passed as
  *     void* so that this header needs no CUDA include. Calls only enqueue work: they do
  *     not synchronize, and results are ready when the stream reaches them.
@@ -109,12 +109,37 @@ gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * ("No Python! ...", sections 6 and 7.2; "A Complete Guide ...", section 2.1: N = 1 at
  * decode makes this a matrix-vector product.) The weights are dequantized inside the
  * kernel right after they are loaded and never written back.
- * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element. Results are
- * deterministic: the same inputs give the same bits on every call.
+ * N < 64: decode kernels (CUDA cores, exact integer block products on a 16-bit
+ * fixed-point copy of X). N >= 64 and K % 256 == 0: tensor cores, bf16 operands
+ * (dequantized weights and X each rounded once to bf16), fp32 accumulation.
+ * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element (for the bf16
+ * path, at the K >= 256 it runs on, by a wide margin for non-adversarial data). Results
+ * are deterministic: the same inputs give the same bits on every call.
  * Y must not overlap W_blocks or X.
  */
 gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                      const float* X, int64_t N, float* Y, void* stream);
+
+/*
+ * Device workspace (bytes) that gq_mul_mat_ws needs for this shape: 0 on the decode path,
+ * N * K * 2 (a bf16 copy of X, rounded up to 256) when the tensor-core path runs
+ * (N >= 64 tokens and K a multiple of 256). 0 for invalid arguments.
+ */
+size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N);
+
+/*
+ * gq_mul_mat with caller-owned workspace: `workspace` must hold
+ * gq_mul_mat_workspace_size(t, M, K, N) bytes, be 256-byte aligned and not be used by
+ * other work in flight. It may be NULL when that size is 0. Nothing is allocated, so this
+ * is the form to use inside CUDA graph capture. GQ_ERR_NULL if a needed workspace is NULL,
+ * GQ_ERR_SHAPE if it is too small, GQ_ERR_ALIGN if misaligned.
+ * gq_mul_mat itself uses a library-owned workspace for the tensor-core path: one device
+ * buffer per (device, stream), allocated on first need and grown when a larger shape
+ * arrives (growing synchronizes that stream and is refused, GQ_ERR_CUDA, during capture).
+ */
+gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                        const float* X, int64_t N, float* Y, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /* One independent problem of gq_mul_mat_batched. */
 typedef struct gq_mul_mat_problem {

@@ -254,3 +254,75 @@ def test_tinyllama_decode_step_q8_0_full_size(gq_lib, oracle_mod, cuda_dev, N):
 @pytest.mark.parametrize("N", [1, 16])
 def test_llama7b_shapes_full_size(gq_lib, oracle_mod, cuda_dev, N):
     _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 5, "q4_0", N, workloads.llama7b_set())
+
+
+# ------------------------------------------------------------------------------------
+# Tensor-core path (N >= 64, K % 256 == 0): bf16 operands, fp32 accumulation
+# ------------------------------------------------------------------------------------
+GEMM = [(128, 256, 64), (7, 256, 64), (300, 512, 100), (129, 768, 300), (1000, 2048, 257),
+        (256, 5632, 64)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", GEMM)
+def test_gemm_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    assert gq_lib.workspace_size(t, M, K, N) >= N * K * 2
+    Y, Y_ref, What, X = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, N, seed=M + K + N)
+    check_tolerance(Y, Y_ref, What, X, f"gemm {t} M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_gemm_one_hot_returns_bf16_weights(gq_lib, oracle_mod, cuda_dev, t):
+    """X = e_k: Y[n][m] is bf16(What[m][k]) exactly (one nonzero product, fp32 sum). This
+    pins the in-kernel dequantization, the swizzled operand layouts and the descriptors."""
+    M, K = 200, 512
+    ks = list(range(0, K, 7))[:64] + [K - 1]
+    X = np.zeros((len(ks), K), np.float32)
+    for n, k in enumerate(ks):
+        X[n, k] = 1.0
+    Y, _, What, _ = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, len(ks), X=X)
+    wb = torch.from_numpy(What).to(torch.bfloat16).float().numpy()
+    for n, k in enumerate(ks):
+        assert np.array_equal(Y[n], wb[:, k]), k
+
+
+def test_gemm_workspace_entry_point(gq_lib, oracle_mod, cuda_dev):
+    M, K, N = 256, 1024, 128
+    W = _np_weights(M, K, seed=21)
+    q = torch.from_numpy(oracle_mod.quantize("q4_0", W)).to(cuda_dev)
+    X = workloads.activations(N, K, seed=22).to(cuda_dev)
+    need = gq_lib.workspace_size("q4_0", M, K, N)
+    assert need == N * K * 2
+    assert gq_lib.workspace_size("q4_0", M, K, 8) == 0          # decode path: none
+    ws = torch.empty(need, dtype=torch.uint8, device=cuda_dev)
+    y1 = gq_lib.mul_mat_ws(q, "q4_0", M, K, X, ws)
+    y2 = gq_lib.mul_mat(q, "q4_0", M, K, X)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    with pytest.raises(gq_lib.GQError) as e:
+        gq_lib.mul_mat_ws(q, "q4_0", M, K, X, None)
+    assert e.value.status == -1
+    with pytest.raises(gq_lib.GQError) as e:
+        gq_lib.mul_mat_ws(q, "q4_0", M, K, X, ws[: need - 256])
+    assert e.value.status == -2
+    assert gq_lib.get_last_error() == 0
+
+
+def test_gemm_deterministic(gq_lib, cuda_dev):
+    M, K, N = 1024, 2048, 320
+    W = workloads.weights(M, K, 31, device=cuda_dev)
+    q = gq_lib.quantize(W, "q4_0")
+    X = workloads.activations(N, K, 32, device=cuda_dev)
+    y1 = gq_lib.mul_mat(q, "q4_0", M, K, X)
+    y2 = gq_lib.mul_mat(q, "q4_0", M, K, X)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_tinyllama_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
+    """gate / down / lm_head at N = 512 tokens, Q4_0, one call per matrix."""
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 4, "q4_0", 512,
+                        workloads.tinyllama_prefill_set(), rows_per_mat=3)
+
+
+def test_llama7b_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 5, "q4_0", 2048, workloads.llama7b_set(),
+                        rows_per_mat=2)
