@@ -236,6 +236,70 @@ def run_reference(args, shapes):
 
 
 # --------------------------------------------------------------------------------------
+# Prefill (tensor-core GEMM): TinyLLaMA gate / down / lm_head at N = 512 and the LLaMA-7B
+# shapes at N = 2048, one gq_mul_mat_ws call per matrix, as TFLOP/s (2 M N K / time).
+# --------------------------------------------------------------------------------------
+PREFILL_SETS = [("tinyllama_prefill_n512", 4, 512), ("llama7b_prefill_n2048", 5, 2048)]
+
+
+def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None):
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    peak_tf = measured_bf16_peak()
+    out = {}
+    for set_name, wl, N in PREFILL_SETS:
+        shapes = workloads.tinyllama_prefill_set() if wl == 4 else workloads.llama7b_set()
+        rows, tot_flop, tot_s = [], 0.0, 0.0
+        for j, sh in enumerate(shapes):
+            if only is not None and (set_name, sh.name) != only:
+                continue
+            W = workloads.weights(sh.M, sh.K, workloads.weight_seed(wl, j), device=dev)
+            q = binding.quantize(W, "q4_0")
+            del W
+            X = workloads.activations(N, sh.K, workloads.act_seed(wl, N, j), device=dev)
+            Y = torch.empty((N, sh.M), device=dev)
+            ws = torch.empty(max(256, binding.workspace_size("q4_0", sh.M, sh.K, N)),
+                             dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                binding.mul_mat_ws(q, "q4_0", sh.M, sh.K, X, ws, out=Y)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(reps):
+                    binding.mul_mat_ws(q, "q4_0", sh.M, sh.K, X, ws, out=Y)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(iters):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+            flop = 2.0 * sh.M * N * sh.K
+            tf = flop / sec / 1e12
+            rows.append({"matrix": sh.name, "M": sh.M, "K": sh.K, "N": N,
+                         "us": round(sec * 1e6, 2), "tflops": round(tf, 1),
+                         "frac": round(tf / peak_tf, 4)})
+            tot_flop += flop
+            tot_s += sec
+            del q, X, Y, ws, g
+        if rows:
+            tf = tot_flop / tot_s / 1e12
+            out[set_name] = {"tflops": round(tf, 1), "frac": round(tf / peak_tf, 4),
+                             "matrices": rows}
+    return out
+
+
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
+# --------------------------------------------------------------------------------------
 # GB300 arm
 # --------------------------------------------------------------------------------------
 def run_gb300(args, shapes):
@@ -380,6 +444,12 @@ def run_gb300(args, shapes):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if rank == 0:
+        pf = prefill_measure(dev)
+        line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16 operands, fp32 accumulate",
+                           "peak": measured_bf16_peak(),
+                           "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json), burst",
+                           **pf}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shapes)
     if rank == 0:
@@ -400,8 +470,15 @@ def main(argv=None):
     ap.add_argument("--profile", action="store_true",
                     help="for ncu: warm-up and the timed steps only (no load phase, no e2e, "
                          "no clock sampling, no oracle); prints the device-timed line")
+    ap.add_argument("--profile-prefill", metavar="MATRIX", default=None,
+                    help="for ncu: time one prefill GEMM only, e.g. llama7b_prefill_n2048/lm_head")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    if args.profile_prefill:
+        import torch
+        set_name, matrix = args.profile_prefill.split("/")
+        emit(prefill_measure(torch.device("cuda", 0), reps=2, iters=1, only=(set_name, matrix)))
+        return
     from block_quantized_matmul_gq_gb300 import workloads
     shapes = workloads.tinyllama_decode_set()
     if args.impl == "reference":

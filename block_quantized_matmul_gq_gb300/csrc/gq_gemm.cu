@@ -14,11 +14,13 @@
 //               (64 k x kBN tokens, 128-byte swizzle) into rings of shared-memory stages.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=kBN, K=16),
 //               four per 64-k stage, and commits each stage back to the producers.
-//   warps 2..5  dequantize: thread = row; per 64-k stage it turns its row's two blocks
-//               into 64 bf16 values, each (c - 8) * d (or c * d) computed exactly in fp32
-//               and rounded once to bf16, and stores them in the 128-byte-swizzled K-major
-//               layout the MMA reads. After the K loop the same warps read the accumulator
-//               out of TMEM (tcgen05.ld, warp w owns lanes 32*(w%4)..) and write Y.
+//   warps 2..9  dequantize: a thread owns one row and one of the two blocks of every 64-k
+//               stage; it turns the block into 32 bf16 values, each (c - 8) * d (or c * d)
+//               computed exactly in fp32 (packed f32x2 arithmetic) and rounded once to
+//               bf16, and stores them in the 128-byte-swizzled K-major layout the MMA
+//               reads. After the K loop the same warps read the accumulator out of TMEM
+//               (tcgen05.ld; warp w owns lanes 32*(w%4).., half the token columns) and
+//               write Y.
 // X is converted to bf16 once per call by x_to_bf16_kernel into caller- or library-owned
 // workspace (N x K bf16), which the tensor map reads.
 // All waits are bounded; a CTA that gives up sets the device status word, lets its own
@@ -41,8 +43,8 @@ namespace {
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBK = 64;           // k per MMA stage: 128 bytes of bf16 = one swizzle row
 constexpr int kSuperK = 256;      // k per raw-weight copy: 8 blocks per row
-constexpr int kRawStages = 2;
-constexpr int kThreads = 192;     // 6 warps
+constexpr int kDequantWarps = 8;  // two per SM sub-partition
+constexpr int kThreads = 64 + 32 * kDequantWarps;   // producer, MMA, dequant/epilogue
 constexpr unsigned long long kDrainNs = 100000000ull;   // 100 ms
 
 template <int kType>
@@ -62,7 +64,12 @@ struct RawFmt<GQ_TYPE_Q8_0> {
 
 template <int kType, int kBN>
 struct Layout {
-    static constexpr int kStages = kBN >= 128 ? 3 : 6;
+    // The dequant warps copy a raw super-step into registers as soon as it lands, so one
+    // raw stage already gives the next copy four MMA stages of lead; Q4_0 then fits four
+    // 48 KB operand stages. Q8_0 (272-byte raw rows) keeps two raw stages and three
+    // operand stages.
+    static constexpr int kRawStages = kType == GQ_TYPE_Q4_0 ? 1 : 2;
+    static constexpr int kStages = kBN >= 128 ? (kType == GQ_TYPE_Q4_0 ? 4 : 3) : 6;
     static constexpr int kA = kBM * kBK * 2;
     static constexpr int kB = kBN * kBK * 2;
     static constexpr int kRaw = kBM * RawFmt<kType>::kRow;
@@ -94,52 +101,80 @@ __device__ __forceinline__ float byte_as_float(uint32_t word) {
     return __int_as_float(static_cast<int>(__byte_perm(word, 0x4B000000u, 0x7540u | k)));
 }
 
-// Dequantizes blocks 2q and 2q+1 of a row's super-step (raw bytes in r) into 64 bf16
-// values, packed in pairs: out[i] holds elements 2i (low half) and 2i+1 (high half).
-// Each value is (c - 8) * d (Q4_0) or c * d (Q8_0), exact in fp32, rounded once to bf16.
-template <int kType, int q>
-__device__ __forceinline__ void dequant_kstep(const uint32_t* r, uint32_t (&out)[32]) {
+// (a - b) * c on two fp32 lanes at once (Blackwell packed fp32), round to nearest.
+__device__ __forceinline__ float2 sub_mul2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, c, t;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "sub.rn.f32x2 t, a, b;\n\tmul.rn.f32x2 t, t, c;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// Dequantizes block `blk` (0..7) of a row's super-step (raw bytes in r) into 32 bf16
+// values packed in pairs: out[i] = elements 2i (low half) and 2i+1 (high half).
+// Each value is (c - 8) * d (Q4_0) or c * d (Q8_0), exact in fp32 (at most 8 + 11
+// significant bits), then rounded once to bf16.
+template <int kType, int blk>
+__device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)[16]) {
     constexpr int kBB = RawFmt<kType>::kBB;
+    constexpr int base = blk * kBB;
+    const float d = half_bits_to_float(u16_at(r, base));
+    const float2 dd = make_float2(d, d);
+    float v[32];
+    if constexpr (kType == GQ_TYPE_Q4_0) {
 #pragma unroll
-    for (int bl = 0; bl < 2; ++bl) {
-        const int base = (2 * q + bl) * kBB;
-        const float d = half_bits_to_float(u16_at(r, base));
-        float v[32];
-        if constexpr (kType == GQ_TYPE_Q4_0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t w = word_at(r, base + 2 + 4 * i);
-                const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 4i..4i+3
-                const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 16+4i..
-                v[4 * i + 0] = byte_as_float<0>(lo);
-                v[4 * i + 1] = byte_as_float<1>(lo);
-                v[4 * i + 2] = byte_as_float<2>(lo);
-                v[4 * i + 3] = byte_as_float<3>(lo);
-                v[16 + 4 * i + 0] = byte_as_float<0>(hi);
-                v[16 + 4 * i + 1] = byte_as_float<1>(hi);
-                v[16 + 4 * i + 2] = byte_as_float<2>(hi);
-                v[16 + 4 * i + 3] = byte_as_float<3>(hi);
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = (v[e] - 8388616.0f) * d;   // 2^23 + 8
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t w = word_at(r, base + 2 + 4 * i) ^ 0x80808080u;   // c + 128
-                v[4 * i + 0] = byte_as_float<0>(w);
-                v[4 * i + 1] = byte_as_float<1>(w);
-                v[4 * i + 2] = byte_as_float<2>(w);
-                v[4 * i + 3] = byte_as_float<3>(w);
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = (v[e] - 8388736.0f) * d;   // 2^23 + 128
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w = word_at(r, base + 2 + 4 * i);
+            const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 4i..4i+3
+            const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 16+4i..
+            v[4 * i + 0] = byte_as_float<0>(lo);
+            v[4 * i + 1] = byte_as_float<1>(lo);
+            v[4 * i + 2] = byte_as_float<2>(lo);
+            v[4 * i + 3] = byte_as_float<3>(lo);
+            v[16 + 4 * i + 0] = byte_as_float<0>(hi);
+            v[16 + 4 * i + 1] = byte_as_float<1>(hi);
+            v[16 + 4 * i + 2] = byte_as_float<2>(hi);
+            v[16 + 4 * i + 3] = byte_as_float<3>(hi);
         }
+        const float2 off = make_float2(8388616.0f, 8388616.0f);   // 2^23 + 8
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-            out[16 * bl + i] = *reinterpret_cast<const uint32_t*>(&p);
+            const float2 p = sub_mul2(make_float2(v[2 * i], v[2 * i + 1]), off, dd);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
+            out[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = word_at(r, base + 2 + 4 * i) ^ 0x80808080u;   // c + 128
+            v[4 * i + 0] = byte_as_float<0>(w);
+            v[4 * i + 1] = byte_as_float<1>(w);
+            v[4 * i + 2] = byte_as_float<2>(w);
+            v[4 * i + 3] = byte_as_float<3>(w);
+        }
+        const float2 off = make_float2(8388736.0f, 8388736.0f);   // 2^23 + 128
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 p = sub_mul2(make_float2(v[2 * i], v[2 * i + 1]), off, dd);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
+            out[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
     }
+}
+
+// Block 2q + h of the super-step, as four 16-byte chunks of the A row (elements
+// 32h .. 32h + 31 of the 64-k stage), stored at chunk (4h + c) ^ (row % 8).
+template <int kType, int q, int h>
+__device__ __forceinline__ void dequant_store(const uint32_t* r, uint8_t* arow, int row) {
+    uint32_t packed[16];
+    dequant_block<kType, 2 * q + h>(r, packed);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(arow + (((4 * h + c) ^ (row & 7)) << 4)) =
+            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
 }
 
 template <int kType, int kBN>
@@ -165,8 +200,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     auto b_full = [&](int s) { return bar0 + 8u * (S + s); };
     auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
     auto raw_full = [&](int r) { return bar0 + 8u * (3 * S + r); };
-    auto raw_empty = [&](int r) { return bar0 + 8u * (3 * S + kRawStages + r); };
-    const uint32_t acc_full = bar0 + 8u * (3 * S + 2 * kRawStages);
+    auto raw_empty = [&](int r) { return bar0 + 8u * (3 * S + L::kRawStages + r); };
+    const uint32_t acc_full = bar0 + 8u * (3 * S + 2 * L::kRawStages);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
 
     const int m0 = blockIdx.x * kBM;
@@ -176,13 +211,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(a_full(s), 128);
+            mbar_init(a_full(s), 32 * kDequantWarps);
             mbar_init(b_full(s), 1);
             mbar_init(empty(s), 1);
         }
-        for (int r = 0; r < kRawStages; ++r) {
+        for (int r = 0; r < L::kRawStages; ++r) {
             mbar_init(raw_full(r), 1);
-            mbar_init(raw_empty(r), 128);
+            mbar_init(raw_empty(r), 32 * kDequantWarps);
         }
         mbar_init(acc_full, 1);
         fence_mbar_init();
@@ -207,8 +242,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                 // Raw weights run one super-step ahead of the k-stages that use them.
                 const int want = min(ks / 4 + 2, nsuper);
                 while (raw_issued < want) {
-                    const int j = raw_issued, r = j % kRawStages;
-                    if (!mbar_wait(raw_empty(r), ((j / kRawStages) & 1) ^ 1)) {
+                    const int j = raw_issued, r = j % L::kRawStages;
+                    if (!mbar_wait(raw_empty(r), ((j / L::kRawStages) & 1) ^ 1)) {
                         ok = false;
                         break;
                     }
@@ -231,8 +266,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             // Every copy this thread issued must land before the CTA's memory is released.
             for (int i = max(0, b_issued - S); i < b_issued; ++i)
                 mbar_wait(b_full(i % S), (i / S) & 1, kDrainNs);
-            for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
-                mbar_wait(raw_full(j % kRawStages), (j / kRawStages) & 1, kDrainNs);
+            for (int j = max(0, raw_issued - L::kRawStages); j < raw_issued; ++j)
+                mbar_wait(raw_full(j % L::kRawStages), (j / L::kRawStages) & 1, kDrainNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -260,12 +295,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         }
     } else {
         // ---------------- dequantize, then epilogue ----------------
-        const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
-        const int row = quad * 32 + lane;       // tile row = TMEM lane
+        // Eight warps: warp w takes TMEM lane quadrant w % 4 (tile rows 32*(w%4)..), and
+        // half h = (w - 2) / 4: block 2q + h of every 64-k stage q, then token columns
+        // [h*kBN/2, (h+1)*kBN/2) in the epilogue.
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int row = quad * 32 + lane;
         bool ok = true;
         for (int j = 0; j < nsuper && ok; ++j) {
-            const int r = j % kRawStages;
-            if (!mbar_wait(raw_full(r), (j / kRawStages) & 1)) {
+            const int r = j % L::kRawStages;
+            if (!mbar_wait(raw_full(r), (j / L::kRawStages) & 1)) {
                 ok = false;
                 break;
             }
@@ -288,18 +327,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                uint32_t packed[32];
-                if (q == 0) dequant_kstep<kType, 0>(raw, packed);
-                if (q == 1) dequant_kstep<kType, 1>(raw, packed);
-                if (q == 2) dequant_kstep<kType, 2>(raw, packed);
-                if (q == 3) dequant_kstep<kType, 3>(raw, packed);
-                // Row of 64 bf16 = eight 16-byte chunks; chunk c lands at c ^ (row % 8).
-                uint8_t* dst = base + L::kOffA + s * L::kA + row * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
-                                   packed[4 * c + 3]);
+                uint8_t* arow = base + L::kOffA + s * L::kA + row * 128;
+                if (half == 0) {
+                    if (q == 0) dequant_store<kType, 0, 0>(raw, arow, row);
+                    if (q == 1) dequant_store<kType, 1, 0>(raw, arow, row);
+                    if (q == 2) dequant_store<kType, 2, 0>(raw, arow, row);
+                    if (q == 3) dequant_store<kType, 3, 0>(raw, arow, row);
+                } else {
+                    if (q == 0) dequant_store<kType, 0, 1>(raw, arow, row);
+                    if (q == 1) dequant_store<kType, 1, 1>(raw, arow, row);
+                    if (q == 2) dequant_store<kType, 2, 1>(raw, arow, row);
+                    if (q == 3) dequant_store<kType, 3, 1>(raw, arow, row);
+                }
                 fence_proxy_async_smem();
                 mbar_arrive(a_full(s));
             }
@@ -311,8 +350,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         if (done && ok) {
             const int m = m0 + row;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-            const int ncols = min(kBN, N - n0);
-            for (int c = 0; c < ncols; c += 16) {
+            const int c_begin = half * (kBN / 2);
+            const int c_end = min(c_begin + kBN / 2, N - n0);
+            for (int c = c_begin; c < c_end; c += 16) {
                 uint32_t v[16];
                 tmem_ld16(tbase + c, v);
                 if (m < M) {
