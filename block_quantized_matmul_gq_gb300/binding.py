@@ -33,7 +33,8 @@ STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
 # Every symbol declared in include/gq.h.
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
            "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
-           "gq_mul_mat_ws", "gq_mul_mat_batched", "gq_get_last_error", "gq_status_string")
+           "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched", "gq_get_last_error",
+           "gq_status_string")
 
 
 class Problem(ctypes.Structure):
@@ -61,6 +62,8 @@ def load(path: str = LIB_PATH):
     L.gq_mul_mat_workspace_size.restype = ctypes.c_size_t
     L.gq_mul_mat_ws.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp, ctypes.c_size_t, vp]
     L.gq_mul_mat_ws.restype = ctypes.c_int
+    L.gq_mul_mat_noalloc.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp]
+    L.gq_mul_mat_noalloc.restype = ctypes.c_int
     L.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
     L.gq_mul_mat_batched.restype = ctypes.c_int
     L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
@@ -170,6 +173,22 @@ def mul_mat_ws(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
     _check(lib.gq_mul_mat_ws(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
                              _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
                              wp, wn, _stream(stream)), "gq_mul_mat_ws")
+    return out
+
+
+def mul_mat_noalloc(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """mul_mat through gq_mul_mat_noalloc: the library allocates nothing (its tensor-core
+    path uses a fixed 64 MiB device array). `out` lets the caller own Y as well."""
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    N = X.shape[0]
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    _check(lib.gq_mul_mat_noalloc(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
+                                  _dev(X, torch.float32, "X"), N,
+                                  _dev(out, torch.float32, "Y"), _stream(stream)),
+           "gq_mul_mat_noalloc")
     return out
 
 

@@ -141,6 +141,26 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                         const float* X, int64_t N, float* Y, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/*
+ * gq_mul_mat that never allocates device memory, for callers that cannot: code being
+ * recorded into a CUDA graph, engines that reserve all device memory up front in their own
+ * arena, and real-time loops that must not stall or fail on an allocation mid-run. (The
+ * pages have no counterpart: their engine allocates once from an arena; this entry point
+ * exists for users of this library.)
+ * Same arguments, results and accuracy as gq_mul_mat. On the tensor-core path (N >= 64,
+ * K % 256 == 0) its workspace is a fixed 64 MiB device array compiled into the library,
+ * which every GPU that loads the library holds until the process exits:
+ *   - shapes whose workspace N * K * 2 exceeds 64 MiB (N * K > 32 Mi) return GQ_ERR_SHAPE;
+ *   - the first call on a device looks up that array's device address (set-up); make that
+ *     first call before any stream capture on the device;
+ *   - every call shares the array (each call rewrites all of it before use), so calls that
+ *     overlap on the GPU -- on different streams or devices' concurrent work sharing a
+ *     device -- race: serialize them.
+ * The decode path (N < 64) needs no workspace and behaves exactly like gq_mul_mat.
+ */
+gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                             const float* X, int64_t N, float* Y, void* stream);
+
 /* One independent problem of gq_mul_mat_batched. */
 typedef struct gq_mul_mat_problem {
     const void* W_blocks;   /* M rows of K/32 blocks, 16-byte aligned */
