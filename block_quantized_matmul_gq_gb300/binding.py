@@ -34,7 +34,7 @@ STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
            "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
            "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched", "gq_get_last_error",
-           "gq_status_string")
+           "gq_selftest_wait_timeout", "gq_status_string")
 
 
 class Problem(ctypes.Structure):
@@ -67,6 +67,8 @@ def load(path: str = LIB_PATH):
     L.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
     L.gq_mul_mat_batched.restype = ctypes.c_int
     L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
+    L.gq_selftest_wait_timeout.argtypes = [i64, vp]
+    L.gq_selftest_wait_timeout.restype = ctypes.c_int
     L.gq_status_string.argtypes, L.gq_status_string.restype = [ctypes.c_int], ctypes.c_char_p
     lib = L
     return L
@@ -211,6 +213,11 @@ def mul_mat_batched(problems, t, N: int, stream=None) -> None:
         problems = make_problems(problems)
     _check(lib.gq_mul_mat_batched(problems, problems._count, _type(t), N, _stream(stream)),
            "gq_mul_mat_batched")
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> None:
+    """Launches the bounded-wait self-test (a wait that can only run out)."""
+    _check(lib.gq_selftest_wait_timeout(limit_us, _stream(stream)), "gq_selftest_wait_timeout")
 
 
 def get_last_error(stream=None) -> int:

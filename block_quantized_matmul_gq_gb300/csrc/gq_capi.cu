@@ -272,3 +272,31 @@ const char* gq_status_string(gq_status s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Self-test of the bounded-wait machinery: one thread waits on an mbarrier that nothing
+// ever arrives on, with the given limit, through the same mbar_wait / report_status the
+// streaming and tensor-core kernels use. The kernel returns normally; the host sees
+// GQ_ERR_TIMEOUT from gq_get_last_error and the context stays usable.
+// ---------------------------------------------------------------------------------------
+namespace gq {
+namespace {
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns, unsigned* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t a = smem_addr(&bar);
+    mbar_init(a, 1);
+    fence_mbar_init();
+    if (!mbar_wait(a, 0, limit_ns)) report_status(status, kStatusTimeout);
+}
+}  // namespace
+}  // namespace gq
+
+extern "C" gq_status gq_selftest_wait_timeout(int64_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 10000000) return GQ_ERR_SHAPE;
+    gq::DeviceInfo* info = nullptr;
+    if (gq::current_device_info(&info) != cudaSuccess) return GQ_ERR_CUDA;
+    gq::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned long long>(limit_us) * 1000ull, info->status);
+    return from_cuda(cudaGetLastError());
+}

@@ -187,6 +187,16 @@ gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count,
  */
 gq_status gq_get_last_error(void* stream);
 
+/*
+ * Self-test of failure detection: launches one thread that waits on a device barrier that
+ * nothing ever completes, with a limit of `limit_us` microseconds (1 .. 10^7), using the
+ * same bounded wait as every kernel here. The wait runs out, the kernel records it in the
+ * status word and returns; the next gq_get_last_error() on this device reports
+ * GQ_ERR_TIMEOUT (and clears it). No fault, no trap, no hang. GQ_ERR_SHAPE for a limit
+ * out of range. (The pages' engine only asserts; this is the library's own check.)
+ */
+gq_status gq_selftest_wait_timeout(int64_t limit_us, void* stream);
+
 /* Static English text for a status code. */
 const char* gq_status_string(gq_status s);
 

@@ -103,3 +103,8 @@ def test_binding_refuses_cpu_tensors(gq_lib):
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError, match="CUDA"):
         gq_lib.quantize(torch.zeros(4, 64), "q4_0", out=torch.zeros(4, 36, dtype=torch.uint8))
+
+
+def test_selftest_limit_checked_on_host(gq_lib):
+    assert gq_lib.lib.gq_selftest_wait_timeout(0, None) == -2
+    assert gq_lib.lib.gq_selftest_wait_timeout(20_000_000, None) == -2
