@@ -122,6 +122,16 @@ cudaError_t internal_workspace(cudaStream_t s, size_t bytes, void** out) {
 // else the decode kernels. `ws` may be NULL (library workspace is used then).
 gq_status run_one(gq_type t, const gq::MatProblem& p, int64_t N, void* ws, size_t ws_bytes,
                   cudaStream_t s) {
+    if (gq::gemv_tc_eligible(p, N)) {
+        const size_t need = static_cast<size_t>(gq::gemv_tc_workspace_bytes(&p, 1, N));
+        void* w = ws;
+        if (w == nullptr) {
+            if (internal_workspace(s, need, &w) != cudaSuccess) return GQ_ERR_CUDA;
+        } else if (ws_bytes < need || !aligned(ws, 256)) {
+            return ws_bytes < need ? GQ_ERR_SHAPE : GQ_ERR_ALIGN;
+        }
+        return from_cuda(gq::launch_gemv_tc(t, &p, 1, N, w, s));
+    }
     if (gq::gemm_eligible(t, p, N)) {
         const size_t need = static_cast<size_t>(gq::gemm_workspace_bytes(p.K, N));
         void* w = ws;
@@ -184,7 +194,10 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K, cons
 
 size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N) {
     if (!known_type(t) || check_shape(M, K, N) != GQ_OK || M == 0 || N == 0 || K == 0) return 0;
-    gq::MatProblem p{reinterpret_cast<const uint8_t*>(uintptr_t(256)), nullptr, nullptr, M, K};
+    gq::MatProblem p{reinterpret_cast<const uint8_t*>(uintptr_t(256)),
+                     reinterpret_cast<const float*>(uintptr_t(256)), nullptr, M, K};
+    if (gq::gemv_tc_eligible(p, N))
+        return static_cast<size_t>(gq::gemv_tc_workspace_bytes(&p, 1, N));
     return gq::gemm_eligible(t, p, N) ? static_cast<size_t>(gq::gemm_workspace_bytes(K, N)) : 0;
 }
 
@@ -197,7 +210,8 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return from_cuda(cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s));
     gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
-    if (gq::gemm_eligible(t, p, N) && workspace == nullptr) return GQ_ERR_NULL;
+    if ((gq::gemm_eligible(t, p, N) || gq::gemv_tc_eligible(p, N)) && workspace == nullptr)
+        return GQ_ERR_NULL;
     return run_one(t, p, N, workspace, workspace_bytes, s);
 }
 
@@ -226,16 +240,27 @@ gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, 
             run[n_launch++] = run[i];
         }
     }
-    // Problems that qualify for the tensor-core path run one after another on the stream
-    // (sharing the library workspace); the rest share one decode launch.
-    int n_decode = 0;
+    // Problems that qualify for the tensor-core GEMM run one after another on the stream
+    // (sharing the library workspace); those for tensor-core decode share one grouped
+    // launch; the rest share one CUDA-core decode launch.
+    gq::MatProblem tc[GQ_MAX_BATCH];
+    int n_decode = 0, n_tc = 0;
     for (int i = 0; i < n_launch; ++i) {
         if (gq::gemm_eligible(t, run[i], N)) {
             gq_status st = run_one(t, run[i], N, nullptr, 0, s);
             if (st != GQ_OK) return st;
+        } else if (gq::gemv_tc_eligible(run[i], N)) {
+            tc[n_tc++] = run[i];
         } else {
             run[n_decode++] = run[i];
         }
+    }
+    if (n_tc > 0) {
+        void* w = nullptr;
+        const size_t need = static_cast<size_t>(gq::gemv_tc_workspace_bytes(tc, n_tc, N));
+        if (internal_workspace(s, need, &w) != cudaSuccess) return GQ_ERR_CUDA;
+        gq_status st = from_cuda(gq::launch_gemv_tc(t, tc, n_tc, N, w, s));
+        if (st != GQ_OK) return st;
     }
     if (n_decode == 0) return GQ_OK;
     return from_cuda(gq::launch_mul_mat(t, run, n_decode, N, s));

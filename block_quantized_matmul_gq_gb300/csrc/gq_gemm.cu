@@ -33,6 +33,7 @@
 #include <mutex>
 #include <utility>
 
+#include "gq_dequant.cuh"
 #include "gq_device.cuh"
 #include "gq_internal.h"
 #include "gq_umma.cuh"
@@ -40,27 +41,14 @@
 namespace gq {
 namespace {
 
+using namespace dq;
+
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBK = 64;           // k per MMA stage: 128 bytes of bf16 = one swizzle row
 constexpr int kSuperK = 256;      // k per raw-weight copy: 8 blocks per row
 constexpr int kDequantWarps = 8;  // two per SM sub-partition
 constexpr int kThreads = 64 + 32 * kDequantWarps;   // producer, MMA, dequant/epilogue
 constexpr unsigned long long kDrainNs = 100000000ull;   // 100 ms
-
-template <int kType>
-struct RawFmt;
-template <>
-struct RawFmt<GQ_TYPE_Q4_0> {
-    static constexpr int kBB = kQ4Bytes;
-    static constexpr int kRow = 8 * kQ4Bytes;   // 144 bytes per row per super-step
-    static constexpr int kElem = 1;             // tensor-map element size (uint8)
-};
-template <>
-struct RawFmt<GQ_TYPE_Q8_0> {
-    static constexpr int kBB = kQ8Bytes;
-    static constexpr int kRow = 8 * kQ8Bytes;   // 272 bytes
-    static constexpr int kElem = 2;             // uint16 elements keep the box <= 256
-};
 
 template <int kType, int kBN>
 struct Layout {
@@ -84,98 +72,6 @@ struct Layout {
     static constexpr int kTmemCols = kBN < 32 ? 32 : kBN;
     static_assert(kB % 1024 == 0 && kA % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned stages");
 };
-
-__device__ __forceinline__ uint32_t word_at(const uint32_t* r, int byte_off) {
-    const int w = byte_off >> 2;
-    return (byte_off & 3) ? __funnelshift_r(r[w], r[w + 1], 16) : r[w];
-}
-
-__device__ __forceinline__ uint32_t u16_at(const uint32_t* r, int byte_off) {
-    const int w = byte_off >> 2;
-    return (byte_off & 3) ? (r[w] >> 16) : (r[w] & 0xFFFFu);
-}
-
-// Byte k (0..3) of `word` as the float 2^23 + byte: the byte lands in the low mantissa.
-template <int k>
-__device__ __forceinline__ float byte_as_float(uint32_t word) {
-    return __int_as_float(static_cast<int>(__byte_perm(word, 0x4B000000u, 0x7540u | k)));
-}
-
-// (a - b) * c on two fp32 lanes at once (Blackwell packed fp32), round to nearest.
-__device__ __forceinline__ float2 sub_mul2(float2 a, float2 b, float2 c) {
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, c, t;\n\t"
-        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-        "sub.rn.f32x2 t, a, b;\n\tmul.rn.f32x2 t, t, c;\n\t"
-        "mov.b64 {%0, %1}, t;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
-
-// Dequantizes block `blk` (0..7) of a row's super-step (raw bytes in r) into 32 bf16
-// values packed in pairs: out[i] = elements 2i (low half) and 2i+1 (high half).
-// Each value is (c - 8) * d (Q4_0) or c * d (Q8_0), exact in fp32 (at most 8 + 11
-// significant bits), then rounded once to bf16.
-template <int kType, int blk>
-__device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)[16]) {
-    constexpr int kBB = RawFmt<kType>::kBB;
-    constexpr int base = blk * kBB;
-    const float d = half_bits_to_float(u16_at(r, base));
-    const float2 dd = make_float2(d, d);
-    float v[32];
-    if constexpr (kType == GQ_TYPE_Q4_0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = word_at(r, base + 2 + 4 * i);
-            const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 4i..4i+3
-            const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 16+4i..
-            v[4 * i + 0] = byte_as_float<0>(lo);
-            v[4 * i + 1] = byte_as_float<1>(lo);
-            v[4 * i + 2] = byte_as_float<2>(lo);
-            v[4 * i + 3] = byte_as_float<3>(lo);
-            v[16 + 4 * i + 0] = byte_as_float<0>(hi);
-            v[16 + 4 * i + 1] = byte_as_float<1>(hi);
-            v[16 + 4 * i + 2] = byte_as_float<2>(hi);
-            v[16 + 4 * i + 3] = byte_as_float<3>(hi);
-        }
-        const float2 off = make_float2(8388616.0f, 8388616.0f);   // 2^23 + 8
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 p = sub_mul2(make_float2(v[2 * i], v[2 * i + 1]), off, dd);
-            const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
-            out[i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w = word_at(r, base + 2 + 4 * i) ^ 0x80808080u;   // c + 128
-            v[4 * i + 0] = byte_as_float<0>(w);
-            v[4 * i + 1] = byte_as_float<1>(w);
-            v[4 * i + 2] = byte_as_float<2>(w);
-            v[4 * i + 3] = byte_as_float<3>(w);
-        }
-        const float2 off = make_float2(8388736.0f, 8388736.0f);   // 2^23 + 128
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 p = sub_mul2(make_float2(v[2 * i], v[2 * i + 1]), off, dd);
-            const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
-            out[i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-    }
-}
-
-// Block 2q + h of the super-step, as four 16-byte chunks of the A row (elements
-// 32h .. 32h + 31 of the 64-k stage), stored at chunk (4h + c) ^ (row % 8).
-template <int kType, int q, int h>
-__device__ __forceinline__ void dequant_store(const uint32_t* r, uint8_t* arow, int row) {
-    uint32_t packed[16];
-    dequant_block<kType, 2 * q + h>(r, packed);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(arow + (((4 * h + c) ^ (row & 7)) << 4)) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-}
 
 template <int kType, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)

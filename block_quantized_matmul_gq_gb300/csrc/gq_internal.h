@@ -46,10 +46,20 @@ cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_
 
 // Prefill path: tcgen05 tensor-core GEMM. Needs gemm_workspace_bytes(K, N) bytes of
 // device workspace (a bf16 copy of X), 256-byte aligned.
-constexpr int64_t kGemmMinTokens = 64;
+constexpr int64_t kGemmMinTokens = 65;
 int64_t gemm_workspace_bytes(int64_t K, int64_t N);
 bool gemm_eligible(gq_type t, const MatProblem& p, int64_t N);
 cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspace,
                         cudaStream_t s);
+
+// Decode on tensor cores for kGemvTcMinTokens..kGemvTcMaxTokens tokens (K % 256 == 0):
+// grouped like launch_mul_mat. Needs gemv_tc_workspace_bytes of workspace (pre-arranged
+// bf16 X tiles, 16 / 32 / 64 token rows per problem), 256-byte aligned.
+constexpr int64_t kGemvTcMinTokens = 5;
+constexpr int64_t kGemvTcMaxTokens = 64;
+bool gemv_tc_eligible(const MatProblem& p, int64_t N);
+int64_t gemv_tc_workspace_bytes(const MatProblem* probs, int count, int64_t N);
+cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_t N,
+                           void* workspace, cudaStream_t s);
 
 }  // namespace gq

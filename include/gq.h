@@ -23,8 +23,8 @@
  *   - Pointers. Every array pointer is a DEVICE pointer owned by the caller; the library
  *     keeps none of them after the call returns. W_blocks must be 16-byte aligned, fp32
  *     arrays 4-byte aligned (16-byte alignment of X is used when present). A pointer may
- *     be NULL only when its array is empty. The decode path (N < 64) allocates nothing;
- *     the tensor-core path needs a workspace (see gq_mul_mat_ws).
+ *     be NULL only when its array is empty. The CUDA-core decode path (N <= 4) allocates
+ *     nothing; the tensor-core paths need a workspace (see gq_mul_mat_ws).
  *   - Streams. `stream` is a cudaStream_t (NULL = the legacy default stream) passed as
  *     void* so that this header needs no CUDA include. Calls only enqueue work: they do
  *     not synchronize, and results are ready when the stream reaches them.
@@ -109,9 +109,11 @@ gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * ("No Python! ...", sections 6 and 7.2; "A Complete Guide ...", section 2.1: N = 1 at
  * decode makes this a matrix-vector product.) The weights are dequantized inside the
  * kernel right after they are loaded and never written back.
- * N < 64: decode kernels (CUDA cores, exact integer block products on a 16-bit
- * fixed-point copy of X). N >= 64 and K % 256 == 0: tensor cores, bf16 operands
- * (dequantized weights and X each rounded once to bf16), fp32 accumulation.
+ * N <= 4 (or K % 256 != 0): decode kernels on CUDA cores (exact integer block products
+ * on a 16-bit fixed-point copy of X). 5 <= N <= 64 and K % 256 == 0: decode on tensor
+ * cores; N >= 65 and K % 256 == 0: the prefill tensor-core GEMM. Both tensor-core paths
+ * use bf16 operands (dequantized weights and X each rounded once to bf16) and fp32
+ * accumulation.
  * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element (for the bf16
  * path, at the K >= 256 it runs on, by a wide margin for non-adversarial data). Results
  * are deterministic: the same inputs give the same bits on every call.
@@ -121,9 +123,11 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                      const float* X, int64_t N, float* Y, void* stream);
 
 /*
- * Device workspace (bytes) that gq_mul_mat_ws needs for this shape: 0 on the decode path,
- * N * K * 2 (a bf16 copy of X, rounded up to 256) when the tensor-core path runs
- * (N >= 64 tokens and K a multiple of 256). 0 for invalid arguments.
+ * Device workspace (bytes) that gq_mul_mat_ws needs for this shape: 0 on the CUDA-core
+ * decode path (N <= 4); P * K * 2 on the tensor-core decode path (5 <= N <= 64, P = 16,
+ * 32 or 64 token rows of pre-arranged bf16 X); N * K * 2 (a bf16 copy of X, rounded up to
+ * 256) on the prefill path (N >= 65). Tensor-core paths need K a multiple of 256.
+ * 0 for invalid arguments.
  */
 size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N);
 
@@ -147,8 +151,9 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * arena, and real-time loops that must not stall or fail on an allocation mid-run. (The
  * pages have no counterpart: their engine allocates once from an arena; this entry point
  * exists for users of this library.)
- * Same arguments, results and accuracy as gq_mul_mat. On the tensor-core path (N >= 64,
- * K % 256 == 0) its workspace is a fixed 64 MiB device array compiled into the library,
+ * Same arguments, results and accuracy as gq_mul_mat, except that 5 <= N <= 64 runs on
+ * the CUDA-core decode kernels. On the prefill path (N >= 65, K % 256 == 0) its workspace
+ * is a fixed 64 MiB device array compiled into the library,
  * which every GPU that loads the library holds until the process exits:
  *   - shapes whose workspace N * K * 2 exceeds 64 MiB (N * K > 32 Mi) return GQ_ERR_SHAPE;
  *   - the first call on a device looks up that array's device address (set-up); make that
@@ -156,7 +161,7 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  *   - every call shares the array (each call rewrites all of it before use), so calls that
  *     overlap on the GPU -- on different streams or devices' concurrent work sharing a
  *     device -- race: serialize them.
- * The decode path (N < 64) needs no workspace and behaves exactly like gq_mul_mat.
+ * Up to 64 tokens it uses the CUDA-core decode kernels, which need no workspace.
  */
 gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                              const float* X, int64_t N, float* Y, void* stream);

@@ -121,15 +121,22 @@ def test_mul_mat_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
 @pytest.mark.parametrize("t", ["q4_0", "q8_0"])
 @pytest.mark.parametrize("K", [2048, 96])
 def test_mul_mat_one_hot_is_exact(gq_lib, oracle_mod, cuda_dev, t, K):
-    """X = e_k returns column k of What bit for bit, on both kernels."""
+    """X = e_k returns column k of What bit for bit on the CUDA-core decode kernels (the
+    streaming one for K = 2048, the generic one for K = 96), called with <= 4 tokens."""
     M = 77
     ks = [0, 1, 15, 16, 31, 32, K - 1] + ([255, 256, 1000] if K > 1000 else [])
-    X = np.zeros((len(ks), K), np.float32)
-    for n, k in enumerate(ks):
-        X[n, k] = 1.0
-    Y, Y_ref, What, _ = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, len(ks), X=X)
-    for n, k in enumerate(ks):
-        assert np.array_equal(Y[n], What[:, k]), k
+    W = _np_weights(M, K, seed=5)
+    q = oracle_mod.quantize(t, W)
+    What = oracle_mod.dequantize(t, q, M, K)
+    qd = torch.from_numpy(q).to(cuda_dev)
+    for i in range(0, len(ks), 4):
+        group = ks[i:i + 4]
+        X = np.zeros((len(group), K), np.float32)
+        for n, k in enumerate(group):
+            X[n, k] = 1.0
+        Y = gq_lib.mul_mat(qd, t, M, K, torch.from_numpy(X).to(cuda_dev)).cpu().numpy()
+        for n, k in enumerate(group):
+            assert np.array_equal(Y[n], What[:, k]), k
 
 
 @pytest.mark.parametrize("t", ["q4_0", "q8_0"])
@@ -257,7 +264,7 @@ def test_llama7b_shapes_full_size(gq_lib, oracle_mod, cuda_dev, N):
 
 
 # ------------------------------------------------------------------------------------
-# Tensor-core path (N >= 64, K % 256 == 0): bf16 operands, fp32 accumulation
+# Tensor-core paths (N >= 5, K % 256 == 0): bf16 operands, fp32 accumulation
 # ------------------------------------------------------------------------------------
 GEMM = [(128, 256, 64), (7, 256, 64), (300, 512, 100), (129, 768, 300), (1000, 2048, 257),
         (256, 5632, 64)]
@@ -293,7 +300,8 @@ def test_gemm_workspace_entry_point(gq_lib, oracle_mod, cuda_dev):
     X = workloads.activations(N, K, seed=22).to(cuda_dev)
     need = gq_lib.workspace_size("q4_0", M, K, N)
     assert need == N * K * 2
-    assert gq_lib.workspace_size("q4_0", M, K, 8) == 0          # decode path: none
+    assert gq_lib.workspace_size("q4_0", M, K, 4) == 0          # CUDA-core decode: none
+    assert gq_lib.workspace_size("q4_0", M, K, 8) == 16 * K * 2  # tensor-core decode
     ws = torch.empty(need, dtype=torch.uint8, device=cuda_dev)
     y1 = gq_lib.mul_mat_ws(q, "q4_0", M, K, X, ws)
     y2 = gq_lib.mul_mat(q, "q4_0", M, K, X)
@@ -326,3 +334,61 @@ def test_tinyllama_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
 def test_llama7b_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
     _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 5, "q4_0", 2048, workloads.llama7b_set(),
                         rows_per_mat=2)
+
+
+# ------------------------------------------------------------------------------------
+# Tensor-core decode (5 <= N <= 64, K % 256 == 0): grouped, bf16 operands
+# ------------------------------------------------------------------------------------
+DECODE_TC = [(1, 256, 5), (7, 2048, 8), (129, 2048, 16), (1000, 2048, 17), (300, 5632, 32),
+             (200, 11008, 33), (128, 512, 64), (2048, 4096, 16)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", DECODE_TC)
+def test_decode_tc_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    Y, Y_ref, What, X = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, N, seed=3 * M + K + N)
+    check_tolerance(Y, Y_ref, What, X, f"decode-tc {t} M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("N", [16, 40])
+def test_decode_tc_one_hot_returns_bf16_weights(gq_lib, oracle_mod, cuda_dev, t, N):
+    M, K = 300, 1024
+    ks = [(37 * n) % K for n in range(N)]
+    X = np.zeros((N, K), np.float32)
+    for n, k in enumerate(ks):
+        X[n, k] = 1.0
+    Y, _, What, _ = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, N, X=X)
+    wb = torch.from_numpy(What).to(torch.bfloat16).float().numpy()
+    for n, k in enumerate(ks):
+        assert np.array_equal(Y[n], wb[:, k]), (n, k)
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_decode_tc_batched_mixed_shapes(gq_lib, oracle_mod, cuda_dev, t):
+    """One grouped tensor-core launch over problems of different M and K, with a
+    CUDA-core-only shape (K % 256 != 0) mixed in."""
+    shapes = [(256, 2048), (2048, 2048), (7, 256), (300, 5632), (1, 1024), (64, 11008),
+              (33, 96)]
+    N = 16
+    items, refs = [], []
+    for i, (M, K) in enumerate(shapes):
+        q = oracle_mod.quantize(t, _np_weights(M, K, seed=90 + i))
+        X = workloads.activations(N, K, seed=95 + i).numpy()
+        items.append((torch.from_numpy(q).to(cuda_dev), M, K, torch.from_numpy(X).to(cuda_dev),
+                      torch.full((N, M), 9.0, device=cuda_dev)))
+        refs.append((q, X))
+    gq_lib.mul_mat_batched(items, t, N)
+    for (M, K), (q, X), it in zip(shapes, refs, items):
+        check_tolerance(it[4].cpu().numpy(), oracle_mod.mul_mat(t, q, M, K, X),
+                        oracle_mod.dequantize(t, q, M, K), X, f"M={M} K={K}")
+    assert gq_lib.get_last_error() == 0
+
+
+def test_decode_tc_deterministic(gq_lib, cuda_dev):
+    M, K, N = 3000, 5632, 16
+    q = gq_lib.quantize(workloads.weights(M, K, 41, device=cuda_dev), "q8_0")
+    X = workloads.activations(N, K, 42, device=cuda_dev)
+    y1 = gq_lib.mul_mat(q, "q8_0", M, K, X)
+    y2 = gq_lib.mul_mat(q, "q8_0", M, K, X)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
