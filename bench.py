@@ -291,6 +291,37 @@ def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None):
     return out
 
 
+def profile_decode(spec: str, steps: int) -> dict:
+    """For ncu: the TinyLLaMA decode step with N tokens (spec "q8_0/16"), one batched call
+    per step with a caller-owned workspace, 3 warm-up steps then `steps` timed ones."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    from block_quantized_matmul_gq_gb300.weightset import QuantizedWeightSet
+    btype, n = spec.split("/")
+    N = int(n)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shapes = workloads.tinyllama_decode_set()
+    ws = QuantizedWeightSet.synthetic(WORKLOAD_ID, shapes, btype, dev)
+    xs, ys = ws.make_io(N, WORKLOAD_ID, dev)
+    arrays = ws.problem_arrays(xs, ys)
+    work = ws.workspace(arrays, N, dev)
+    for _ in range(3):
+        ws.run(arrays, N, workspace=work)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        ws.run(arrays, N, workspace=work)
+    end.record()
+    torch.cuda.synchronize(dev)
+    if binding.get_last_error() != 0:
+        raise RuntimeError("device status word set")
+    ms = start.elapsed_time(end) / steps
+    return {"profile_decode": spec, "ms_per_step": round(ms, 5),
+            "weight_GBps": round(ws.weight_bytes / ms / 1e6, 1)}
+
+
 def measured_bf16_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -472,8 +503,13 @@ def main(argv=None):
                          "no clock sampling, no oracle); prints the device-timed line")
     ap.add_argument("--profile-prefill", metavar="MATRIX", default=None,
                     help="for ncu: time one prefill GEMM only, e.g. llama7b_prefill_n2048/lm_head")
+    ap.add_argument("--profile-decode", metavar="TYPE/N", default=None,
+                    help="for ncu: the TinyLLaMA decode step at N tokens, e.g. q8_0/16")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    if args.profile_decode:
+        emit(profile_decode(args.profile_decode, steps=min(args.steps, 20)))
+        return
     if args.profile_prefill:
         import torch
         set_name, matrix = args.profile_prefill.split("/")

@@ -33,7 +33,8 @@ STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
 # Every symbol declared in include/gq.h.
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
            "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
-           "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched", "gq_get_last_error",
+           "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched",
+           "gq_mul_mat_batched_workspace_size", "gq_mul_mat_batched_ws", "gq_get_last_error",
            "gq_selftest_wait_timeout", "gq_status_string")
 
 
@@ -66,6 +67,11 @@ def load(path: str = LIB_PATH):
     L.gq_mul_mat_noalloc.restype = ctypes.c_int
     L.gq_mul_mat_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
     L.gq_mul_mat_batched.restype = ctypes.c_int
+    L.gq_mul_mat_batched_workspace_size.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64]
+    L.gq_mul_mat_batched_workspace_size.restype = ctypes.c_size_t
+    L.gq_mul_mat_batched_ws.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp,
+                                        ctypes.c_size_t, vp]
+    L.gq_mul_mat_batched_ws.restype = ctypes.c_int
     L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
     L.gq_selftest_wait_timeout.argtypes = [i64, vp]
     L.gq_selftest_wait_timeout.restype = ctypes.c_int
@@ -218,6 +224,22 @@ def mul_mat_batched(problems, t, N: int, stream=None) -> None:
 def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> None:
     """Launches the bounded-wait self-test (a wait that can only run out)."""
     _check(lib.gq_selftest_wait_timeout(limit_us, _stream(stream)), "gq_selftest_wait_timeout")
+
+
+def batched_workspace_size(problems, t, N: int) -> int:
+    if not isinstance(problems, ctypes.Array):
+        problems = make_problems(problems)
+    return int(lib.gq_mul_mat_batched_workspace_size(problems, problems._count, _type(t), N))
+
+
+def mul_mat_batched_ws(problems, t, N: int, workspace: torch.Tensor | None, stream=None) -> None:
+    """mul_mat_batched with a caller-owned workspace (uint8 CUDA tensor)."""
+    if not isinstance(problems, ctypes.Array):
+        problems = make_problems(problems)
+    wp = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    wn = workspace.numel() if workspace is not None else 0
+    _check(lib.gq_mul_mat_batched_ws(problems, problems._count, _type(t), N, wp, wn,
+                                     _stream(stream)), "gq_mul_mat_batched_ws")
 
 
 def get_last_error(stream=None) -> int:

@@ -1,6 +1,7 @@
 // gq_capi.cu -- the extern "C" entry points of include/gq.h: host-side argument checks,
 // dispatch to the kernels, and the per-device status word that kernels set when a
 // bounded wait runs out.
+#include <algorithm>
 #include <climits>
 #include <cstring>
 #include <map>
@@ -215,55 +216,107 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K, c
     return run_one(t, p, N, workspace, workspace_bytes, s);
 }
 
-gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
-                             int64_t N, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validated problems of a batched call, split by path. `run` holds the non-empty K > 0
+// problems; K == 0 ones are zeroed on the stream here.
+struct BatchPlan {
+    gq::MatProblem gemm[GQ_MAX_BATCH], tc[GQ_MAX_BATCH], cc[GQ_MAX_BATCH];
+    int n_gemm = 0, n_tc = 0, n_cc = 0;
+    size_t ws_bytes = 0;   // max(largest GEMM workspace, sum of tensor-core decode tiles)
+};
+
+gq_status plan_batch(const gq_mul_mat_problem* problems, int32_t count, gq_type t, int64_t N,
+                     BatchPlan* plan, cudaStream_t s, bool zero_k0) {
     if (count < 0 || count > GQ_MAX_BATCH) return GQ_ERR_SHAPE;
     if (!known_type(t)) return GQ_ERR_TYPE;
     if (count == 0) return GQ_OK;
     if (!problems) return GQ_ERR_NULL;
-    gq::MatProblem run[GQ_MAX_BATCH];
-    int n_run = 0;
     for (int i = 0; i < count; ++i) {
         const gq_mul_mat_problem& p = problems[i];
         bool empty = false;
         gq_status st = check_problem(p.W_blocks, t, p.M, p.K, p.X, N, p.Y, &empty);
         if (st != GQ_OK) return st;
-        if (!empty) run[n_run++] = {static_cast<const uint8_t*>(p.W_blocks), p.X, p.Y, p.M, p.K};
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int n_launch = 0;
-    for (int i = 0; i < n_run; ++i) {
-        if (run[i].K == 0) {
-            cudaError_t e = cudaMemsetAsync(run[i].Y, 0, sizeof(float) * N * run[i].M, s);
-            if (e != cudaSuccess) return GQ_ERR_CUDA;
+    size_t gemm_max = 0;
+    for (int i = 0; i < count; ++i) {
+        const gq_mul_mat_problem& p = problems[i];
+        if (p.M == 0 || N == 0) continue;
+        if (p.K == 0) {
+            if (zero_k0 && cudaMemsetAsync(p.Y, 0, sizeof(float) * N * p.M, s) != cudaSuccess)
+                return GQ_ERR_CUDA;
+            continue;
+        }
+        const gq::MatProblem mp{static_cast<const uint8_t*>(p.W_blocks), p.X, p.Y, p.M, p.K};
+        if (gq::gemm_eligible(t, mp, N)) {
+            plan->gemm[plan->n_gemm++] = mp;
+            gemm_max = std::max(gemm_max, static_cast<size_t>(gq::gemm_workspace_bytes(p.K, N)));
+        } else if (gq::gemv_tc_eligible(mp, N)) {
+            plan->tc[plan->n_tc++] = mp;
         } else {
-            run[n_launch++] = run[i];
+            plan->cc[plan->n_cc++] = mp;
         }
     }
-    // Problems that qualify for the tensor-core GEMM run one after another on the stream
-    // (sharing the library workspace); those for tensor-core decode share one grouped
-    // launch; the rest share one CUDA-core decode launch.
-    gq::MatProblem tc[GQ_MAX_BATCH];
-    int n_decode = 0, n_tc = 0;
-    for (int i = 0; i < n_launch; ++i) {
-        if (gq::gemm_eligible(t, run[i], N)) {
-            gq_status st = run_one(t, run[i], N, nullptr, 0, s);
-            if (st != GQ_OK) return st;
-        } else if (gq::gemv_tc_eligible(run[i], N)) {
-            tc[n_tc++] = run[i];
-        } else {
-            run[n_decode++] = run[i];
+    const size_t tc_sum =
+        plan->n_tc ? static_cast<size_t>(gq::gemv_tc_workspace_bytes(plan->tc, plan->n_tc, N)) : 0;
+    plan->ws_bytes = std::max(gemm_max, tc_sum);
+    return GQ_OK;
+}
+
+// GEMM problems run one after another, then one grouped tensor-core decode launch, then
+// one CUDA-core decode launch; all on `s`, all sharing workspace `ws` in stream order.
+gq_status run_batch(gq_type t, int64_t N, BatchPlan* plan, void* ws, size_t ws_bytes,
+                    cudaStream_t s) {
+    if (plan->ws_bytes > 0) {
+        if (ws == nullptr) {
+            if (internal_workspace(s, plan->ws_bytes, &ws) != cudaSuccess) return GQ_ERR_CUDA;
+        } else if (ws_bytes < plan->ws_bytes || !aligned(ws, 256)) {
+            return ws_bytes < plan->ws_bytes ? GQ_ERR_SHAPE : GQ_ERR_ALIGN;
         }
     }
-    if (n_tc > 0) {
-        void* w = nullptr;
-        const size_t need = static_cast<size_t>(gq::gemv_tc_workspace_bytes(tc, n_tc, N));
-        if (internal_workspace(s, need, &w) != cudaSuccess) return GQ_ERR_CUDA;
-        gq_status st = from_cuda(gq::launch_gemv_tc(t, tc, n_tc, N, w, s));
+    for (int i = 0; i < plan->n_gemm; ++i) {
+        gq_status st = from_cuda(gq::launch_gemm(t, plan->gemm[i], N, ws, s));
         if (st != GQ_OK) return st;
     }
-    if (n_decode == 0) return GQ_OK;
-    return from_cuda(gq::launch_mul_mat(t, run, n_decode, N, s));
+    if (plan->n_tc > 0) {
+        gq_status st = from_cuda(gq::launch_gemv_tc(t, plan->tc, plan->n_tc, N, ws, s));
+        if (st != GQ_OK) return st;
+    }
+    if (plan->n_cc > 0) return from_cuda(gq::launch_mul_mat(t, plan->cc, plan->n_cc, N, s));
+    return GQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
+                             int64_t N, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    BatchPlan plan;
+    gq_status st = plan_batch(problems, count, t, N, &plan, s, true);
+    if (st != GQ_OK) return st;
+    return run_batch(t, N, &plan, nullptr, 0, s);
+}
+
+size_t gq_mul_mat_batched_workspace_size(const gq_mul_mat_problem* problems, int32_t count,
+                                         gq_type t, int64_t N) {
+    BatchPlan plan;
+    if (plan_batch(problems, count, t, N, &plan, nullptr, false) != GQ_OK) return 0;
+    return plan.ws_bytes;
+}
+
+gq_status gq_mul_mat_batched_ws(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
+                                int64_t N, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    BatchPlan plan;
+    gq_status st = plan_batch(problems, count, t, N, &plan, s, true);
+    if (st != GQ_OK) return st;
+    if (plan.ws_bytes > 0 && workspace == nullptr) return GQ_ERR_NULL;
+    return run_batch(t, N, &plan, workspace, workspace_bytes, s);
 }
 
 gq_status gq_get_last_error(void* stream) {

@@ -104,6 +104,15 @@ __device__ __forceinline__ void bulk_g2s_evict_first(uint32_t dst, const void* s
         : "memory");
 }
 
+// Before a shared-memory buffer that this thread has just read with ordinary loads is
+// handed back for an async-proxy write (a bulk / TMA copy): waits for the loaded values
+// (the dummy register depends on all of them) and orders the generic-proxy reads before
+// later async-proxy accesses.
+__device__ __forceinline__ void release_to_async_proxy(uint32_t depends_on_loads) {
+    asm volatile("" ::"r"(depends_on_loads) : "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void report_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }

@@ -214,6 +214,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                 raw[4 * i + 2] = v.z;
                 raw[4 * i + 3] = v.w;
             }
+            {
+                uint32_t dep = 0;
+#pragma unroll
+                for (int i = 0; i < kRawWords; ++i) dep ^= raw[i];
+                release_to_async_proxy(dep);
+            }
             mbar_arrive(raw_empty(r));
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

@@ -71,6 +71,15 @@ class QuantizedWeightSet:
         return [binding.make_problems(items[i:i + binding.MAX_BATCH])
                 for i in range(0, len(items), binding.MAX_BATCH)]
 
-    def run(self, arrays, N: int, stream=None) -> None:
+    def workspace(self, arrays, N: int, device):
+        """A caller-owned workspace big enough for every array (None if none is needed);
+        with it, run() allocates nothing and can be recorded into a CUDA graph."""
+        need = max([binding.batched_workspace_size(a, self.btype, N) for a in arrays] + [0])
+        return torch.empty(need, dtype=torch.uint8, device=device) if need else None
+
+    def run(self, arrays, N: int, stream=None, workspace=None) -> None:
         for arr in arrays:
-            binding.mul_mat_batched(arr, self.btype, N, stream=stream)
+            if workspace is None:
+                binding.mul_mat_batched(arr, self.btype, N, stream=stream)
+            else:
+                binding.mul_mat_batched_ws(arr, self.btype, N, workspace, stream=stream)

@@ -186,6 +186,24 @@ gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count,
                              gq_type t, int64_t N, void* stream);
 
 /*
+ * Workspace (bytes) gq_mul_mat_batched_ws needs for these problems: the largest prefill
+ * workspace among them, or the sum of their tensor-core decode tiles, whichever is larger;
+ * 0 if every problem runs on the CUDA-core decode path, and for invalid arguments.
+ */
+size_t gq_mul_mat_batched_workspace_size(const gq_mul_mat_problem* problems, int32_t count,
+                                         gq_type t, int64_t N);
+
+/*
+ * gq_mul_mat_batched with caller-owned workspace (256-byte aligned, at least
+ * gq_mul_mat_batched_workspace_size bytes, not used by other work in flight); allocates
+ * nothing, so it is the form to record into a CUDA graph. gq_mul_mat_batched uses the
+ * library-owned per-(device, stream) workspace instead (see gq_mul_mat_ws).
+ */
+gq_status gq_mul_mat_batched_ws(const gq_mul_mat_problem* problems, int32_t count,
+                                gq_type t, int64_t N, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * Device-side status of the current device: synchronizes `stream`, then returns and
  * clears the status word (GQ_OK, or GQ_ERR_TIMEOUT if a kernel gave up waiting), or
  * GQ_ERR_CUDA if the stream itself reports an error.

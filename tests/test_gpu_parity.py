@@ -392,3 +392,34 @@ def test_decode_tc_deterministic(gq_lib, cuda_dev):
     y1 = gq_lib.mul_mat(q, "q8_0", M, K, X)
     y2 = gq_lib.mul_mat(q, "q8_0", M, K, X)
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+@pytest.mark.parametrize("N", [16, 96])
+def test_batched_ws_records_into_a_graph(gq_lib, cuda_dev, N):
+    """The caller-owned-workspace batched call allocates nothing, so it can be captured into
+    a CUDA graph on any stream; replays give the same bits as a direct call."""
+    shapes = [(256, 2048), (640, 5632), (33, 96)]
+    items = []
+    for i, (M, K) in enumerate(shapes):
+        q = gq_lib.quantize(workloads.weights(M, K, 60 + i, device=cuda_dev), "q4_0")
+        items.append((q, M, K, workloads.activations(N, K, 70 + i, device=cuda_dev),
+                      torch.empty((N, M), device=cuda_dev)))
+    arr = gq_lib.make_problems(items)
+    need = gq_lib.batched_workspace_size(arr, "q4_0", N)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device=cuda_dev)
+    gq_lib.mul_mat_batched_ws(arr, "q4_0", N, ws)
+    torch.cuda.synchronize()
+    direct = [it[4].clone() for it in items]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gq_lib.mul_mat_batched_ws(arr, "q4_0", N, ws)
+    for it in items:
+        it[4].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for d, it in zip(direct, items):
+        assert torch.equal(d.view(torch.int32), it[4].view(torch.int32))
+    with pytest.raises(gq_lib.GQError):
+        gq_lib.mul_mat_batched_ws(arr, "q4_0", N, None)
+    assert gq_lib.get_last_error() == 0
