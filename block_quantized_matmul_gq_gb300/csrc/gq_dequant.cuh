@@ -58,14 +58,14 @@ __device__ __forceinline__ float2 sub_mul2(float2 a, float2 b, float2 c) {
     return r;
 }
 
-// Dequantizes block `blk` (0..7) of a row's super-step (raw bytes in r) into 32 bf16
-// values packed in pairs: out[i] = elements 2i (low half) and 2i+1 (high half).
+// Dequantizes the block that starts at byte kOff of the raw bytes in r (kOff even) into
+// 32 bf16 values packed in pairs: out[i] = elements 2i (low half) and 2i+1 (high half).
 // Each value is (c - 8) * d (Q4_0) or c * d (Q8_0), exact in fp32 (at most 8 + 11
 // significant bits), then rounded once to bf16.
-template <int kType, int blk>
-__device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)[16]) {
-    constexpr int kBB = RawFmt<kType>::kBB;
-    constexpr int base = blk * kBB;
+template <int kType, int kOff>
+__device__ __forceinline__ void dequant_block_at(const uint32_t* r, uint32_t (&out)[16]) {
+    static_assert(kOff % 2 == 0, "blocks start on 2-byte boundaries");
+    constexpr int base = kOff;
     const float d = half_bits_to_float(u16_at(r, base));
     const float2 dd = make_float2(d, d);
     float v[32];
@@ -108,6 +108,12 @@ __device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)
             out[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
     }
+}
+
+// Block `blk` (0..7) of a row's super-step, raw bytes in r from the super-step's start.
+template <int kType, int blk>
+__device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)[16]) {
+    dequant_block_at<kType, blk * RawFmt<kType>::kBB>(r, out);
 }
 
 // Block 2q + h of the super-step, as four 16-byte chunks of the A row (elements

@@ -48,36 +48,43 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;                   // width of one pre-arranged X tile
 constexpr int kSuperK = 256;              // k per raw stage
 constexpr int kHalfK = 128;               // k per A slot (one dequantize group's half)
+constexpr int kQuarters = kSuperK / kBK;  // 64-k quarters of a super-step
+constexpr int kMmaWarps = kQuarters;      // warps 1..4: one MMA issuer per quarter
 constexpr int kDequantWarps = 8;          // two groups of four warps (all 128 rows each)
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * (kDequantWarps + kEpiWarps);   // 448
-constexpr int kGroupSlots = 3;            // A slots in TMEM per dequantize group
-constexpr int kAccCols = 128;             // TMEM columns [0, 128): two accumulators
+constexpr int kFirstDequantWarp = 1 + kMmaWarps;
+constexpr int kThreads = 32 * (1 + kMmaWarps + kDequantWarps);   // 416
 constexpr int kSlotCols = kHalfK / 2;     // 64 columns: 128 bf16 per lane
-constexpr int kTmemCols = 512;            // accumulators + 2 x 3 A slots
+constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 232448;        // opt-in dynamic shared memory per CTA
 constexpr unsigned long long kDrainNs = 100000000ull;
-static_assert(kAccCols + 2 * kGroupSlots * kSlotCols <= kTmemCols, "TMEM budget");
 
 template <int kType, int kNPad>
 struct TcLayout {
+    // TMEM: kAccBufs sets of four accumulators (one per quarter) of kNPad columns, then
+    // two groups x kGroupSlots A slots of 64 columns. Two sets let a tile's epilogue
+    // overlap the next tile's MMAs; at 64 tokens only one set fits next to the A slots.
+    static constexpr int kAccBufs = kNPad <= 32 ? 2 : 1;
+    static constexpr int kAccCols = kAccBufs * kQuarters * kNPad;          // 128 / 256 / 256
+    static constexpr int kGroupSlots = (kTmemCols - kAccCols) / (2 * kSlotCols);   // 3 / 2 / 2
+    static_assert(kGroupSlots >= 2, "TMEM budget");
     static constexpr int kB = kNPad * kBK * 2;              // one 64-k X tile: 2 / 4 / 8 KB
     static constexpr int kRawRow = RawFmt<kType>::kRow;     // 144 / 272
     static constexpr int kRaw = kBM * kRawRow;              // 18 / 34 KB of raw blocks
     static constexpr int kStage = kRaw + 4 * kB;            // raw blocks + the super-step's X
     static constexpr int kOffRaw = 0;
-    static constexpr int kFixed = 1024 + 256;               // alignment slack, barriers, slot
+    static constexpr int kFixed = 1024 + 512;               // alignment slack, barriers, slot
     static constexpr int kRawFit = (kSmemLimit - kFixed) / kStage;
     static constexpr int kRawStages = kRawFit > 8 ? 8 : kRawFit;
     static constexpr int kOffBar = kOffRaw + kRawStages * kStage;
-    // raw_full[R], raw_empty[R], a_full[2][G], a_empty[2][G], acc_full[2], acc_empty[2],
+    // raw_full[R], raw_empty[R], a_full[2][G], a_empty[2][G], acc_full[B], acc_empty[B],
     // mma_done
-    static constexpr int kNumBars = 2 * kRawStages + 4 * kGroupSlots + 5;
+    static constexpr int kNumBars = 2 * kRawStages + 4 * kGroupSlots + 2 * kAccBufs + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kB % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned tiles");
     static_assert(kRawStages >= 2 && kAlloc <= kSmemLimit, "shared memory budget");
+    static_assert(kNumBars * 8 + 16 <= kFixed - 1024, "barrier space");
 };
 
 struct TcProb {
@@ -87,79 +94,90 @@ struct TcProb {
     float* Y;
     int64_t M;
     int64_t row_bytes;
-    int64_t byte_begin;
+    int64_t unit_begin;   // index of the problem's first work unit in the launch
     int32_t K;
-    int32_t pad_;
+    int32_t nsuper;       // super-steps per tile: K / 256
 };
 
 // Largest number of problems one launch takes: the tensor maps and the problem table
 // travel as kernel parameters (128 x (128 + 64) bytes here).
 constexpr int kMaxLaunchProbs = 128;
+// Largest grid: the split-tile partial sums are sized for it.
+constexpr int kMaxTcGrid = 256;
 
 template <int kMaxProbs>
 struct TcParams {
     CUtensorMap maps[kMaxProbs];   // raw weight bytes per problem: rows x row bytes
     int32_t count;
     int32_t n_tok;
-    int64_t total_bytes;
+    int64_t total_units;   // work units (one 128-row tile x one 256-k super-step) in all
+    float* part;           // per CTA two 128 x kNPad partial-sum tiles of split tiles
+    int* counters;         // per CTA boundary and TMEM lane quadrant: partials delivered
     unsigned* status;
     TcProb p[kMaxProbs];
 };
 
-// First tile start (problem p, row r, r a multiple of 128) at or after byte `byte` of the
-// launch's row sequence; (count, 0) = end.
-template <int kMaxProbs>
-__device__ void tc_row_at_byte(const TcParams<kMaxProbs>& P, int64_t byte, int& p, int64_t& r) {
-    p = 0;
-    while (p + 1 < P.count && P.p[p + 1].byte_begin <= byte) ++p;
-    const int64_t off = byte - P.p[p].byte_begin;
-    const int64_t tile_bytes = P.p[p].row_bytes * kBM;
-    r = off <= 0 ? 0 : (off + tile_bytes - 1) / tile_bytes * kBM;
-    if (r >= P.p[p].M) {
-        ++p;
-        r = 0;
-    }
-}
-
-// Walk of one CTA's share, one 256-k super-step at a time: problem p, tile rows
-// [row0, row0 + rows), super-step j of nsuper. Every role walks the same sequence.
+// The work of a launch is a sequence of units, problem by problem, tile by tile, super-step
+// by super-step; every unit moves and multiplies the same bytes, so CTA c takes units
+// [U c / grid, U (c + 1) / grid): shares differ by at most one unit. A tile whose units
+// fall to two or more CTAs is "split": each of them leaves a partial sum, and the last to
+// deliver adds them all in CTA order (tc_finish_split). Every role of a CTA walks the same
+// sequence.
 struct TcWalk {
-    int p;
-    int64_t row0, re;     // tile start, end of this problem's part of the share
-    int rows;
-    int j, nsuper;
+    int p;                // problem
+    int64_t row0;         // first row of the tile
+    int rows;             // rows of the tile that exist (<= 128)
+    int j;                // current super-step of the tile
+    int jbeg, jend;       // this share's super-steps of the tile: [jbeg, jend)
+    int nsuper;
+    int64_t u, u_end;     // current unit, end of the share
     bool valid;
 };
 
+// The problem that unit u belongs to: the last p with unit_begin <= u (binary search: the
+// table lives in kernel-parameter space, where each probe can miss the constant cache).
 template <int kMaxProbs>
-__device__ void tc_walk_open(const TcParams<kMaxProbs>& P, TcWalk& w, int p, int64_t rb,
-                             int p_end, int64_t r_end) {
-    for (; p < P.count && p <= p_end; ++p, rb = 0) {
-        const int64_t re = (p == p_end) ? r_end : P.p[p].M;
-        if (re > rb) {
-            w.p = p;
-            w.row0 = rb;
-            w.re = re;
-            w.rows = static_cast<int>(min(static_cast<int64_t>(kBM), re - rb));
-            w.j = 0;
-            w.nsuper = P.p[p].K / kSuperK;
-            w.valid = true;
-            return;
-        }
+__device__ int tc_problem_of(const TcParams<kMaxProbs>& P, int64_t u) {
+    int lo = 0, hi = P.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.p[mid].unit_begin <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
     }
-    w.valid = false;
+    return lo;
 }
 
 template <int kMaxProbs>
-__device__ void tc_walk_next(const TcParams<kMaxProbs>& P, TcWalk& w, int p_end, int64_t r_end) {
-    if (++w.j < w.nsuper) return;
-    w.j = 0;
-    w.row0 += kBM;
-    if (w.row0 < w.re) {
-        w.rows = static_cast<int>(min(static_cast<int64_t>(kBM), w.re - w.row0));
+__device__ void tc_walk_tile(const TcParams<kMaxProbs>& P, TcWalk& w, int p, int64_t u) {
+    const int64_t off = u - P.p[p].unit_begin;
+    w.p = p;
+    w.nsuper = P.p[p].nsuper;
+    w.row0 = off / w.nsuper * kBM;
+    w.rows = static_cast<int>(min(static_cast<int64_t>(kBM), P.p[p].M - w.row0));
+    w.j = w.jbeg = static_cast<int>(off % w.nsuper);
+    w.jend = static_cast<int>(min(static_cast<int64_t>(w.nsuper), w.jbeg + (w.u_end - u)));
+    w.u = u;
+}
+
+template <int kMaxProbs>
+__device__ void tc_walk_open(const TcParams<kMaxProbs>& P, TcWalk& w, int64_t u0, int64_t u1) {
+    w.u_end = u1;
+    w.valid = u0 < u1;
+    if (w.valid) tc_walk_tile(P, w, tc_problem_of(P, u0), u0);
+}
+
+template <int kMaxProbs>
+__device__ void tc_walk_next(const TcParams<kMaxProbs>& P, TcWalk& w) {
+    ++w.u;
+    if (++w.j < w.jend) return;
+    if (w.u >= w.u_end) {
+        w.valid = false;
         return;
     }
-    tc_walk_open(P, w, w.p + 1, 0, p_end, r_end);
+    const int p = (w.row0 + kBM < P.p[w.p].M) ? w.p : w.p + 1;   // next tile or problem
+    tc_walk_tile(P, w, p, w.u);
 }
 
 // One dequantize group's half of a row's raw super-step (kWords 32-bit words) from shared
@@ -183,12 +201,70 @@ __device__ __forceinline__ void load_half_row(const uint8_t* src, uint32_t (&raw
     }
 }
 
+// A split tile (problem p, rows [row0, row0 + rows)): this CTA's warp for TMEM lane quadrant
+// `quad` has written its 32 rows of partial sum to slot `slot` (0: the share starts inside
+// the tile, 1: it ends inside). The contributors are CTA c - 1 (slot 1) and CTAs c ..
+// c_end - 1 (slot 0), c the first CTA boundary inside the tile. Each contributor's warp
+// counts itself in; the last one adds the partials in that CTA order (so the sum does not
+// depend on who finishes last), writes Y and resets the counter for the next launch.
+// Nothing waits for another CTA.
+template <int kNPad, int kMaxProbs>
+__device__ void tc_finish_split(const TcParams<kMaxProbs>& P, int p, int64_t row0, int rows,
+                                int slot, int quad, int lane) {
+    const TcProb& pr = P.p[p];
+    const int64_t U = P.total_units;
+    const int G = gridDim.x;
+    const int64_t tile_u0 = pr.unit_begin + row0 / kBM * pr.nsuper;
+    const int64_t tile_u1 = tile_u0 + pr.nsuper;
+    int c = static_cast<int>(blockIdx.x) + slot;   // a boundary inside the tile
+    while (c > 1 && U * (c - 1) / G > tile_u0) --c;
+    int c_end = c + 1;
+    while (c_end < G && U * c_end / G < tile_u1) ++c_end;
+    int* counter = P.counters + c * 4 + quad;
+    __threadfence();   // this lane's partial rows, before the count below
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(counter, 1) == c_end - c;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    const int row = quad * 32 + lane;
+    if (row < rows) {
+        // all loads of a contributor are issued before its adds, and all stores come last
+        const int64_t tile_elems = static_cast<int64_t>(kNPad) * kBM;
+        float y[kNPad];
+        const float* first = P.part + (static_cast<int64_t>(c - 1) * 2 + 1) * tile_elems + row;
+#pragma unroll
+        for (int n = 0; n < kNPad; ++n) y[n] = __ldcg(first + n * kBM);
+        for (int cc = c; cc < c_end; ++cc) {
+            const float* src = P.part + static_cast<int64_t>(cc) * 2 * tile_elems + row;
+            float v[kNPad];
+#pragma unroll
+            for (int n = 0; n < kNPad; ++n) v[n] = __ldcg(src + n * kBM);
+#pragma unroll
+            for (int n = 0; n < kNPad; ++n) y[n] += v[n];
+        }
+        float* Y = pr.Y + row0 + row;
+#pragma unroll
+        for (int n = 0; n < kNPad; ++n)
+            if (n < P.n_tok) Y[n * pr.M] = y[n];
+    }
+    __syncwarp();
+    if (lane == 0) *counter = 0;
+}
+
+// Waits on an mbarrier phase with every lane of the warp; true only if all lanes saw it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int kType, int kNPad, int kMaxProbs>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
     using L = TcLayout<kType, kNPad>;
     constexpr int R = L::kRawStages;
-    constexpr int G = kGroupSlots;
+    constexpr int G = L::kGroupSlots;
+    constexpr int B = L::kAccBufs;
     constexpr int kHalfWords = L::kRawRow / 8;   // one group's half of a row: 18 / 34 words
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -204,30 +280,30 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
     auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
     auto a_empty = [&](int g, int i) { return bar0 + 8u * (2 * R + 2 * G + g * G + i); };
     auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
-    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + 2 + b); };
-    const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 4);
+    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
+    const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
 
     if (threadIdx.x == 0) {
         for (int r = 0; r < R; ++r) {
             mbar_init(raw_full(r), 1);
-            // every dequantize thread once its half row is in registers, and the MMA
-            // issuer's commit once the super-step's MMAs (the readers of its X) completed
-            mbar_init(raw_empty(r), 32 * kDequantWarps + 1);
+            // every dequantize thread once its half row is in registers, and each MMA
+            // issuer's commit once its quarter's MMAs (the readers of its X) completed
+            mbar_init(raw_empty(r), 32 * kDequantWarps + kMmaWarps);
         }
         for (int g = 0; g < 2; ++g)
             for (int i = 0; i < G; ++i) {
                 mbar_init(a_full(g, i), 32 * kDequantWarps / 2);
-                mbar_init(a_empty(g, i), 1);
+                mbar_init(a_empty(g, i), 2);   // the two issuers of the group's quarters
             }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(acc_full(b), 1);
-            mbar_init(acc_empty(b), 32 * kEpiWarps);
+        for (int b = 0; b < B; ++b) {
+            mbar_init(acc_full(b), kMmaWarps);
+            mbar_init(acc_empty(b), 32 * kMmaWarps);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, kMmaWarps);
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 0) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -236,18 +312,15 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    int p0, p1;
-    int64_t r0, r1;
-    tc_row_at_byte(P, P.total_bytes * blockIdx.x / gridDim.x, p0, r0);
-    tc_row_at_byte(P, P.total_bytes * (blockIdx.x + 1) / gridDim.x, p1, r1);
     TcWalk w;
-    tc_walk_open(P, w, p0, r0, p1, r1);
+    tc_walk_open(P, w, P.total_units * blockIdx.x / gridDim.x,
+                 P.total_units * (blockIdx.x + 1) / gridDim.x);
 
     if (warp == 0) {
         // ---------------- producer (whole warp; lane 0 arms the barriers) ----------------
         int raw_n = 0;
         bool ok = true;
-        for (; w.valid; tc_walk_next(P, w, p1, r1), ++raw_n) {
+        for (; w.valid; tc_walk_next(P, w), ++raw_n) {
             const int r = raw_n % R;
             if (!mbar_wait(raw_empty(r), ((raw_n / R) & 1) ^ 1)) {
                 ok = false;
@@ -269,70 +342,155 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             for (int i = max(0, raw_n - R); i < raw_n; ++i)
                 mbar_wait(raw_full(i % R), (i / R) & 1, kDrainNs);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kNPad);
-            int tile = 0, raw_n = 0;
-            bool ok = true;
-            for (; w.valid && ok; tc_walk_next(P, w, p1, r1), ++raw_n) {
-                const int b = tile & 1;
-                if (w.j == 0) {
-                    if (!mbar_wait(acc_empty(b), ((tile >> 1) & 1) ^ 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+    } else if (warp < kFirstDequantWarp) {
+        // ---------------- MMA issuers, then epilogue ----------------
+        // Issuer q (warps 1..4) owns the 64-k quarter q of every super-step and its own
+        // accumulator per set, so the four issue in parallel (a single issuing thread
+        // cannot keep the tensor core busy with N <= 64 MMAs). The four accumulators of
+        // a tile are added in a fixed order by the same warps afterwards, each warp for
+        // the TMEM lane quadrant it may access (warp % 4); with two sets this epilogue
+        // runs after the next tile's first MMAs have been queued.
+        const int q = warp - 1;
+        const int g = q >> 1;                      // dequantize group that fills quarter q
+        const int quad = warp & 3;
+        const uint32_t tlane = static_cast<uint32_t>(quad * 32) << 16;
+        constexpr uint32_t idesc = idesc_bf16_f32(kBM, kNPad);
+        int tile = 0, raw_n = 0;
+        bool ok = true;
+        // epilogue of a finished tile; `slot` < 0: the whole tile, write Y; else a split
+        // tile's partial sum, written to partial slot `slot` of this CTA
+        int pend_p = -1, pend_rows = 0, pend_tile = 0, pend_slot = -1;
+        int64_t pend_row0 = 0;
+        int head_p = -1, head_rows = 0;
+        int64_t head_row0 = 0;
+        auto epilogue = [&](int p, int64_t row0, int rows, int t, int slot) -> bool {
+            const int b = t % B;
+            if (!warp_wait(acc_full(b), (t / B) & 1)) return false;
+            tc_fence_after();
+            const TcProb& pr = P.p[p];
+            const int row = quad * 32 + lane;
+            float* part = P.part + (static_cast<int64_t>(blockIdx.x) * 2 + max(slot, 0)) *
+                                       (kNPad * kBM);
+            const uint32_t acc = tmem + tlane + static_cast<uint32_t>(b * kQuarters * kNPad);
+#pragma unroll
+            for (int c = 0; c < kNPad; c += 16) {
+                // y = (acc0 + acc1) + (acc2 + acc3), the same order for every element
+                float y[16];
+                {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld16(acc + 0 * kNPad + c, v0);
+                    tmem_ld16(acc + 1 * kNPad + c, v1);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        y[jj] = __uint_as_float(v0[jj]) + __uint_as_float(v1[jj]);
                 }
-                const int r = raw_n % R;
-                if (!mbar_wait(raw_full(r), (raw_n / R) & 1)) {   // the super-step's X landed
+                {
+                    uint32_t v2[16], v3[16];
+                    tmem_ld16(acc + 2 * kNPad + c, v2);
+                    tmem_ld16(acc + 3 * kNPad + c, v3);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        y[jj] += __uint_as_float(v2[jj]) + __uint_as_float(v3[jj]);
+                }
+                if (row < rows) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int n = c + jj;
+                        if (n >= P.n_tok) continue;
+                        if (slot < 0)
+                            pr.Y[n * pr.M + row0 + row] = y[jj];
+                        else
+                            part[n * kBM + row] = y[jj];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty(b));
+            if (slot == 1) {
+                tc_finish_split<kNPad>(P, p, row0, rows, 1, quad, lane);
+            } else if (slot == 0) {   // the share's first tile: finished after the last one
+                head_p = p;
+                head_row0 = row0;
+                head_rows = rows;
+            }
+            return true;
+        };
+        for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
+            const int b = tile % B;
+            if (w.j == w.jbeg) {   // a new tile: its accumulator set must have been read out
+                if (!warp_wait(acc_empty(b), ((tile / B) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
-                const uint32_t sX = sRaw + r * L::kStage + L::kRaw;
-                const int gi = raw_n % G;
-                for (int g = 0; g < 2; ++g) {
-                    if (!mbar_wait(a_full(g, gi), (raw_n / G) & 1)) {
+                tc_fence_after();
+            }
+            const int r = raw_n % R;
+            const int gi = raw_n % G;
+            if (!warp_wait(raw_full(r), (raw_n / R) & 1) ||      // the super-step's X landed
+                !warp_wait(a_full(g, gi), (raw_n / G) & 1)) {    // quarter q dequantized
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t sX = sRaw + r * L::kStage + L::kRaw + q * L::kB;
+                const uint32_t a_col =
+                    tmem + L::kAccCols + (g * G + gi) * kSlotCols + (q & 1) * (kBK / 2);
+                const uint32_t d = tmem + static_cast<uint32_t>((b * kQuarters + q) * kNPad);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    umma_bf16_tmem_a(d, a_col + kk * 8, sw128_kmajor_desc(sX + kk * 32), idesc,
+                                     (w.j != w.jbeg || kk != 0) ? 1u : 0u);
+                umma_commit(a_empty(g, gi));
+                umma_commit(raw_empty(r));
+                if (w.j == w.jend - 1) umma_commit(acc_full(b));
+            }
+            __syncwarp();
+            if (B == 2 && w.j == w.jbeg && pend_p >= 0) {
+                if (!epilogue(pend_p, pend_row0, pend_rows, pend_tile, pend_slot)) {
+                    ok = false;
+                    break;
+                }
+                pend_p = -1;
+            }
+            if (w.j == w.jend - 1) {
+                // a tile cut by this share's start (jbeg > 0) is partial slot 0, one cut by
+                // its end slot 1
+                const int slot = w.jbeg > 0 ? 0 : (w.jend < w.nsuper ? 1 : -1);
+                if (B == 1) {
+                    if (!epilogue(w.p, w.row0, w.rows, tile, slot)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t a_col = tmem + kAccCols + (g * G + gi) * kSlotCols;
-#pragma unroll
-                    for (int kk = 0; kk < kHalfK / 16; ++kk) {
-                        // k = 128 g + 16 kk: X tile 2 g + kk / 4, 32 bytes per 16 k inside it
-                        const uint64_t bdesc =
-                            sw128_kmajor_desc(sX + (2 * g + kk / 4) * L::kB + (kk % 4) * 32);
-                        umma_bf16_tmem_a(tmem + b * kNPad, a_col + kk * 8, bdesc, idesc,
-                                         (w.j | g | kk) != 0 ? 1u : 0u);
-                    }
-                    umma_commit(a_empty(g, gi));
+                } else {
+                    pend_p = w.p;
+                    pend_row0 = w.row0;
+                    pend_rows = w.rows;
+                    pend_tile = tile;
+                    pend_slot = slot;
                 }
-                if (!ok) break;
-                umma_commit(raw_empty(r));
-                if (w.j == w.nsuper - 1) {
-                    umma_commit(acc_full(b));
-                    ++tile;
-                }
+                ++tile;
             }
-            // Completes when every MMA issued has finished (also after a timeout), so the
-            // TMEM release below never races an MMA in flight.
-            umma_commit(mma_done);
-            if (!ok) report_status(P.status, kStatusTimeout);
         }
-    } else if (warp < 2 + kDequantWarps) {
+        if (ok && pend_p >= 0) ok = epilogue(pend_p, pend_row0, pend_rows, pend_tile, pend_slot);
+        if (ok && head_p >= 0) tc_finish_split<kNPad>(P, head_p, head_row0, head_rows, 0, quad, lane);
+        // Completes when every MMA this thread issued has finished (also after a timeout),
+        // so the TMEM release below never races an MMA in flight.
+        if (lane == 0) umma_commit(mma_done);
+        if (!ok && lane == 0) report_status(P.status, kStatusTimeout);
+    } else {
         // ---------------- dequantize ----------------
-        // Group g (warps 2..5 or 6..9) takes k [128 g, 128 g + 128) of every super-step for
-        // all 128 rows; each warp its TMEM lane quadrant 32 * (warp % 4) + i, one row per
-        // thread, written to the group's A slot with tcgen05.st.
-        const int g = (warp - 2) >> 2;
+        // Group g (warps 5..8 or 9..12) takes k [128 g, 128 g + 128) of every super-step
+        // for all 128 rows; each warp its TMEM lane quadrant 32 * (warp % 4) + i, one row
+        // per thread, written to the group's A slot with tcgen05.st.
+        const int g = (warp - kFirstDequantWarp) >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCols;
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCols;
         int raw_n = 0;
         bool ok = true;
         uint32_t raw[kHalfWords];
-        for (; w.valid && ok; tc_walk_next(P, w, p1, r1), ++raw_n) {
+        for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
             const int r = raw_n % R;
             if (!mbar_wait(raw_full(r), (raw_n / R) & 1)) {
                 ok = false;
@@ -385,44 +543,10 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             mbar_arrive(a_full(g, gi));
         }
         if (!ok) report_status(P.status, kStatusTimeout);
-    } else {
-        // ---------------- epilogue ----------------
-        // A warp may only touch the TMEM lanes of its own quadrant: 32 * (warp % 4) + i.
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const uint32_t tlane = static_cast<uint32_t>(quad * 32) << 16;
-        int tile = 0;
-        bool ok = true;
-        for (; w.valid && ok; tc_walk_next(P, w, p1, r1)) {
-            if (w.j != w.nsuper - 1) continue;   // act once per tile
-            const int b = tile & 1;
-            if (!mbar_wait(acc_full(b), (tile >> 1) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const TcProb& pr = P.p[w.p];
-#pragma unroll
-            for (int c = 0; c < kNPad; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem + tlane + b * kNPad + c, v);
-                if (row < w.rows) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int n = c + jj;
-                        if (n < P.n_tok) pr.Y[n * pr.M + w.row0 + row] = __uint_as_float(v[jj]);
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(acc_empty(b));
-            ++tile;
-        }
-        if (!ok) report_status(P.status, kStatusTimeout);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 0) {
         if (lane == 0) mbar_wait(mma_done, 0, kDrainNs);
         __syncwarp();
         tc_fence_after();
@@ -430,27 +554,60 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
     }
 }
 
+// Arguments of x_tiles_kernel: every tensor-core decode problem of a call.
+struct XtProb {
+    const float* X;
+    uint8_t* Xt;
+    int64_t K;
+    int32_t block_begin;   // first block of x_tiles_kernel that works on this problem
+    int32_t x_aligned;     // X is 16-byte aligned: vector loads
+};
+constexpr int kXtChunksPerBlock = 1024;   // 4 per thread
+struct XtParams {
+    int32_t count;
+    int32_t n_tok;
+    int* counters;
+    int32_t n_counters;
+    XtProb p[GQ_MAX_BATCH];
+};
+
 // X (n_tok x K fp32, rows of K) -> kNPad x 64 bf16 tiles per 64-k stage, each row 128 bytes
-// with 16-byte chunk c stored at c ^ (row % 8); tokens >= n_tok are zero.
-// grid.y = problem; each thread writes one 16-byte chunk.
-template <int kNPad, int kMaxProbs>
+// with 16-byte chunk c stored at c ^ (row % 8); tokens >= n_tok are zero. One launch for
+// all problems: each problem gets a run of blocks, each block 1024 of its 16-byte output
+// chunks. Block 0 also clears the split-tile counters of the decode kernels that follow.
+template <int kNPad>
 __global__ void __launch_bounds__(256)
-x_tiles_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
-    const int p = blockIdx.y;
-    const int K = P.p[p].K;
-    const float* X = P.p[p].X;
-    uint8_t* out = const_cast<uint8_t*>(P.p[p].Xt);
-    const int64_t chunks = static_cast<int64_t>(K / kBK) * kNPad * 8;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < chunks;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int c = static_cast<int>(i & 7);
-        const int n = static_cast<int>((i >> 3) % kNPad);
-        const int64_t ks = (i >> 3) / kNPad;
+x_tiles_kernel(const __grid_constant__ XtParams P) {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < P.n_counters; i += blockDim.x) P.counters[i] = 0;
+    int lo = 0, hi = P.count - 1;   // the problem of this block: last block_begin <= block
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.p[mid].block_begin <= static_cast<int>(blockIdx.x))
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const XtProb& pr = P.p[lo];
+    const int64_t chunks = pr.K / kBK * kNPad * 8;
+    const int64_t first = static_cast<int64_t>(blockIdx.x - pr.block_begin) * kXtChunksPerBlock;
+    const int64_t last = min(chunks, first + kXtChunksPerBlock);
+    for (int64_t li = first + threadIdx.x; li < last; li += blockDim.x) {
+        const int c = static_cast<int>(li & 7);
+        const int n = static_cast<int>((li >> 3) % kNPad);
+        const int64_t ks = (li >> 3) / kNPad;
         float v[8];
         if (n < P.n_tok) {
-            const float* x = X + static_cast<int64_t>(n) * K + ks * kBK + 8 * c;
+            const float* x = pr.X + n * pr.K + ks * kBK + 8 * c;
+            if (pr.x_aligned) {
+                const float4 a = *reinterpret_cast<const float4*>(x);
+                const float4 b = *reinterpret_cast<const float4*>(x + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = x[e];
+                for (int e = 0; e < 8; ++e) v[e] = x[e];
+            }
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = 0.0f;
@@ -461,7 +618,7 @@ x_tiles_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
             packed[e] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        *reinterpret_cast<uint4*>(out + ks * (kNPad * 128) + n * 128 + ((c ^ (n & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(pr.Xt + ks * (kNPad * 128) + n * 128 + ((c ^ (n & 7)) << 4)) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
 }
@@ -536,63 +693,89 @@ cudaError_t weight_map(const uint8_t* W, int64_t M, int64_t K, CUtensorMap* out)
 
 int npad_for(int64_t N) { return N <= 16 ? 16 : (N <= 32 ? 32 : 64); }
 
+// Start of the workspace: two 128 x kNPad fp32 partial-sum tiles per CTA, then the
+// split-tile counters (one per CTA boundary and lane quadrant), then the X tiles.
+int64_t tc_part_bytes(int npad) { return int64_t(2) * kMaxTcGrid * kBM * npad * 4; }
+constexpr int kCounters = kMaxTcGrid * 4;
+constexpr int64_t kCounterBytes = kCounters * 4;   // 4 KB, keeps the X tiles 256-aligned
+
+template <int kNPad>
+cudaError_t launch_x_tiles(const MatProblem* probs, int count, int64_t N, uint8_t* part,
+                           uint8_t* xt, const DeviceInfo* info, cudaStream_t s) {
+    XtParams P{};
+    P.count = count;
+    P.n_tok = static_cast<int32_t>(N);
+    P.counters = reinterpret_cast<int*>(part + tc_part_bytes(kNPad));
+    P.n_counters = kCounters;
+    (void)info;
+    int64_t blocks = 0, off = 0;
+    for (int i = 0; i < count; ++i) {
+        P.p[i].X = probs[i].X;
+        P.p[i].Xt = xt + off;
+        P.p[i].K = probs[i].K;
+        P.p[i].block_begin = static_cast<int32_t>(blocks);
+        P.p[i].x_aligned = reinterpret_cast<uintptr_t>(probs[i].X) % 16 == 0 && probs[i].K % 4 == 0;
+        blocks += (probs[i].K / kBK * kNPad * 8 + kXtChunksPerBlock - 1) / kXtChunksPerBlock;
+        off += static_cast<int64_t>(kNPad) * probs[i].K * 2;
+    }
+    x_tiles_kernel<kNPad><<<static_cast<unsigned>(blocks), 256, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
 template <int kType, int kNPad, int kMaxProbs>
-cudaError_t launch_tc_t(const MatProblem* probs, int count, int64_t N, uint8_t* ws,
-                        const DeviceInfo* info, cudaStream_t s) {
+cudaError_t launch_tc_t(const MatProblem* probs, int count, int64_t N, uint8_t* part,
+                        uint8_t* xt, const DeviceInfo* info, cudaStream_t s) {
     using L = TcLayout<kType, kNPad>;
     static_assert(sizeof(TcParams<kMaxProbs>) <= 32000, "kernel parameter space");
     TcParams<kMaxProbs> P{};
     P.count = count;
     P.n_tok = static_cast<int32_t>(N);
     P.status = info->status;
-    int64_t bytes = 0, ws_off = 0;
-    int64_t max_chunks = 0;
+    P.part = reinterpret_cast<float*>(part);
+    P.counters = reinterpret_cast<int*>(part + tc_part_bytes(kNPad));
+    int64_t units = 0, xt_off = 0;
     for (int i = 0; i < count; ++i) {
         TcProb& g = P.p[i];
         g.W = probs[i].W;
         g.X = probs[i].X;
-        g.Xt = ws + ws_off;
+        g.Xt = xt + xt_off;
         g.Y = probs[i].Y;
         g.M = probs[i].M;
         g.K = static_cast<int32_t>(probs[i].K);
         g.row_bytes = (probs[i].K / 32) * RawFmt<kType>::kBB;
-        g.byte_begin = bytes;
-        bytes += g.M * g.row_bytes;
-        ws_off += static_cast<int64_t>(kNPad) * probs[i].K * 2;
-        max_chunks = std::max<int64_t>(max_chunks, probs[i].K / kBK * kNPad * 8);
+        g.nsuper = static_cast<int32_t>(probs[i].K / kSuperK);
+        g.unit_begin = units;
+        units += (g.M + kBM - 1) / kBM * g.nsuper;
+        xt_off += static_cast<int64_t>(kNPad) * probs[i].K * 2;
         cudaError_t e = weight_map<kType>(probs[i].W, probs[i].M, probs[i].K, &P.maps[i]);
         if (e != cudaSuccess) return e;
     }
-    P.total_bytes = bytes;
-    const unsigned gx = static_cast<unsigned>(std::min<int64_t>((max_chunks + 255) / 256, 64));
-    x_tiles_kernel<kNPad, kMaxProbs><<<dim3(gx, count), 256, 0, s>>>(P);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    P.total_units = units;
     auto kernel = gemv_tc_kernel<kType, kNPad, kMaxProbs>;
-    e = ensure_smem(kernel, info->device, L::kAlloc);
+    cudaError_t e = ensure_smem(kernel, info->device, L::kAlloc);
     if (e != cudaSuccess) return e;
-    int64_t grid = (bytes + 65535) / 65536;
-    grid = std::max<int64_t>(1, std::min<int64_t>(grid, info->sm_count));
-    kernel<<<static_cast<int>(grid), kThreads, L::kAlloc, s>>>(P);
+    const int grid = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>({units, info->sm_count, kMaxTcGrid})));
+    kernel<<<grid, kThreads, L::kAlloc, s>>>(P);
     return cudaGetLastError();
 }
 
 template <int kType, int kMaxProbs>
-cudaError_t launch_tc_np(const MatProblem* probs, int count, int64_t N, uint8_t* ws,
-                         const DeviceInfo* info, cudaStream_t s) {
+cudaError_t launch_tc_np(const MatProblem* probs, int count, int64_t N, uint8_t* part,
+                         uint8_t* xt, const DeviceInfo* info, cudaStream_t s) {
     switch (npad_for(N)) {
-        case 16: return launch_tc_t<kType, 16, kMaxProbs>(probs, count, N, ws, info, s);
-        case 32: return launch_tc_t<kType, 32, kMaxProbs>(probs, count, N, ws, info, s);
-        default: return launch_tc_t<kType, 64, kMaxProbs>(probs, count, N, ws, info, s);
+        case 16: return launch_tc_t<kType, 16, kMaxProbs>(probs, count, N, part, xt, info, s);
+        case 32: return launch_tc_t<kType, 32, kMaxProbs>(probs, count, N, part, xt, info, s);
+        default: return launch_tc_t<kType, 64, kMaxProbs>(probs, count, N, part, xt, info, s);
     }
 }
 
 template <int kType>
-cudaError_t launch_tc_type(const MatProblem* probs, int count, int64_t N, uint8_t* ws,
-                           const DeviceInfo* info, cudaStream_t s) {
-    if (count == 1) return launch_tc_np<kType, 1>(probs, count, N, ws, info, s);
-    if (count <= 16) return launch_tc_np<kType, 16>(probs, count, N, ws, info, s);
-    return launch_tc_np<kType, kMaxLaunchProbs>(probs, count, N, ws, info, s);
+cudaError_t launch_tc_type(const MatProblem* probs, int count, int64_t N, uint8_t* part,
+                           uint8_t* xt, const DeviceInfo* info, cudaStream_t s) {
+    if (count == 1) return launch_tc_np<kType, 1>(probs, count, N, part, xt, info, s);
+    if (count <= 16) return launch_tc_np<kType, 16>(probs, count, N, part, xt, info, s);
+    return launch_tc_np<kType, kMaxLaunchProbs>(probs, count, N, part, xt, info, s);
 }
 
 }  // namespace
@@ -604,7 +787,7 @@ bool gemv_tc_eligible(const MatProblem& p, int64_t N) {
 }
 
 int64_t gemv_tc_workspace_bytes(const MatProblem* probs, int count, int64_t N) {
-    int64_t b = 0;
+    int64_t b = tc_part_bytes(npad_for(N)) + kCounterBytes;
     for (int i = 0; i < count; ++i) b += static_cast<int64_t>(npad_for(N)) * probs[i].K * 2;
     return b;
 }
@@ -614,14 +797,23 @@ cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_
     DeviceInfo* info = nullptr;
     cudaError_t e = current_device_info(&info);
     if (e != cudaSuccess) return e;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    // Launches of at most kMaxLaunchProbs problems; their X tiles sit one after another.
+    // Workspace: the partial sums (reused by every launch, in stream order), then the X
+    // tiles of all problems one after another. Launches take at most kMaxLaunchProbs.
+    uint8_t* part = static_cast<uint8_t*>(workspace);
+    uint8_t* xt = part + tc_part_bytes(npad_for(N)) + kCounterBytes;
+    switch (npad_for(N)) {
+        case 16: e = launch_x_tiles<16>(probs, count, N, part, xt, info, s); break;
+        case 32: e = launch_x_tiles<32>(probs, count, N, part, xt, info, s); break;
+        default: e = launch_x_tiles<64>(probs, count, N, part, xt, info, s); break;
+    }
+    if (e != cudaSuccess) return e;
     for (int i0 = 0; i0 < count; i0 += kMaxLaunchProbs) {
         const int n = std::min(kMaxLaunchProbs, count - i0);
-        e = t == GQ_TYPE_Q4_0 ? launch_tc_type<GQ_TYPE_Q4_0>(probs + i0, n, N, ws, info, s)
-                              : launch_tc_type<GQ_TYPE_Q8_0>(probs + i0, n, N, ws, info, s);
+        e = t == GQ_TYPE_Q4_0
+                ? launch_tc_type<GQ_TYPE_Q4_0>(probs + i0, n, N, part, xt, info, s)
+                : launch_tc_type<GQ_TYPE_Q8_0>(probs + i0, n, N, part, xt, info, s);
         if (e != cudaSuccess) return e;
-        ws += gemv_tc_workspace_bytes(probs + i0, n, N);
+        for (int i = i0; i < i0 + n; ++i) xt += static_cast<int64_t>(npad_for(N)) * probs[i].K * 2;
     }
     return cudaSuccess;
 }

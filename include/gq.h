@@ -124,10 +124,11 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,
 
 /*
  * Device workspace (bytes) that gq_mul_mat_ws needs for this shape: 0 on the CUDA-core
- * decode path (N <= 4); P * K * 2 on the tensor-core decode path (5 <= N <= 64, P = 16,
- * 32 or 64 token rows of pre-arranged bf16 X); N * K * 2 (a bf16 copy of X, rounded up to
- * 256) on the prefill path (N >= 65). Tensor-core paths need K a multiple of 256.
- * 0 for invalid arguments.
+ * decode path (N <= 4); on the tensor-core decode path (5 <= N <= 64) P * K * 2 for
+ * P = 16, 32 or 64 token rows of pre-arranged bf16 X, plus 2 * 256 * 128 * P * 4 + 4096
+ * for the partial sums (and their counters) of tiles whose k range is split between CTAs;
+ * N * K * 2 (a bf16 copy of X, rounded up to 256) on the prefill path (N >= 65).
+ * Tensor-core paths need K a multiple of 256. 0 for invalid arguments.
  */
 size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N);
 
@@ -187,7 +188,8 @@ gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count,
 
 /*
  * Workspace (bytes) gq_mul_mat_batched_ws needs for these problems: the largest prefill
- * workspace among them, or the sum of their tensor-core decode tiles, whichever is larger;
+ * workspace among them, or the tensor-core decode workspace of the problems that take that
+ * path (the partial sums once, plus every problem's X tiles), whichever is larger;
  * 0 if every problem runs on the CUDA-core decode path, and for invalid arguments.
  */
 size_t gq_mul_mat_batched_workspace_size(const gq_mul_mat_problem* problems, int32_t count,

@@ -301,7 +301,9 @@ def test_gemm_workspace_entry_point(gq_lib, oracle_mod, cuda_dev):
     need = gq_lib.workspace_size("q4_0", M, K, N)
     assert need == N * K * 2
     assert gq_lib.workspace_size("q4_0", M, K, 4) == 0          # CUDA-core decode: none
-    assert gq_lib.workspace_size("q4_0", M, K, 8) == 16 * K * 2  # tensor-core decode
+    # tensor-core decode: 16-token X tiles, two 128 x 16 partial tiles per CTA (<= 256) and
+    # 4 KB of split-tile counters
+    assert gq_lib.workspace_size("q4_0", M, K, 8) == 16 * K * 2 + 2 * 256 * 128 * 16 * 4 + 4096
     ws = torch.empty(need, dtype=torch.uint8, device=cuda_dev)
     y1 = gq_lib.mul_mat_ws(q, "q4_0", M, K, X, ws)
     y2 = gq_lib.mul_mat(q, "q4_0", M, K, X)
