@@ -60,38 +60,46 @@ __device__ __forceinline__ float2 sub_mul2(float2 a, float2 b, float2 c) {
 
 // Dequantizes the block that starts at byte kOff of the raw bytes in r (kOff even) into
 // 32 bf16 values packed in pairs: out[i] = elements 2i (low half) and 2i+1 (high half).
-// Each value is (c - 8) * d (Q4_0) or c * d (Q8_0), exact in fp32 (at most 8 + 11
-// significant bits), then rounded once to bf16.
+// Each value is the exact (c - 8) * d (Q4_0) or c * d (Q8_0) (at most 8 + 11 significant
+// bits) rounded once to bf16.
 template <int kType, int kOff>
 __device__ __forceinline__ void dequant_block_at(const uint32_t* r, uint32_t (&out)[16]) {
     static_assert(kOff % 2 == 0, "blocks start on 2-byte boundaries");
     constexpr int base = kOff;
     const float d = half_bits_to_float(u16_at(r, base));
-    const float2 dd = make_float2(d, d);
-    float v[32];
     if constexpr (kType == GQ_TYPE_Q4_0) {
+        // In bf16x2 arithmetic, two elements per instruction. A nibble byte c placed under
+        // the bf16 bit pattern 0x43 is the exact value 128 + c; subtracting 136 gives the
+        // exact c - 8. The scale splits exactly into d = d_hi + d_lo (d_hi = bf16(d); d has
+        // 11 significant bits, so the remainder has at most 4 and is a bf16 value), the
+        // product (c - 8) * d_lo is exact in bf16, and fma(c - 8, d_hi, (c - 8) * d_lo)
+        // rounds the exact (c - 8) * d once: the same bf16 as rounding it from fp32.
+        const __nv_bfloat16 dh = __float2bfloat16_rn(d);
+        const __nv_bfloat16 dl = __float2bfloat16_rn(d - __bfloat162float(dh));
+        const __nv_bfloat162 dh2 = __halves2bfloat162(dh, dh);
+        const __nv_bfloat162 dl2 = __halves2bfloat162(dl, dl);
+        const __nv_bfloat162 off = __float2bfloat162_rn(136.0f);
+        auto pair = [&](uint32_t bytes4, uint32_t sel) {
+            const uint32_t v = __byte_perm(bytes4, 0x43434343u, sel);   // (128 + c, 128 + c')
+            const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+            const __nv_bfloat162 a = __hfma2(q, dh2, __hmul2(q, dl2));
+            return *reinterpret_cast<const uint32_t*>(&a);
+        };
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t w = word_at(r, base + 2 + 4 * i);
             const uint32_t lo = w & 0x0F0F0F0Fu;           // elements 4i..4i+3
             const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;    // elements 16+4i..
-            v[4 * i + 0] = byte_as_float<0>(lo);
-            v[4 * i + 1] = byte_as_float<1>(lo);
-            v[4 * i + 2] = byte_as_float<2>(lo);
-            v[4 * i + 3] = byte_as_float<3>(lo);
-            v[16 + 4 * i + 0] = byte_as_float<0>(hi);
-            v[16 + 4 * i + 1] = byte_as_float<1>(hi);
-            v[16 + 4 * i + 2] = byte_as_float<2>(hi);
-            v[16 + 4 * i + 3] = byte_as_float<3>(hi);
-        }
-        const float2 off = make_float2(8388616.0f, 8388616.0f);   // 2^23 + 8
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 p = sub_mul2(make_float2(v[2 * i], v[2 * i + 1]), off, dd);
-            const __nv_bfloat162 b = __floats2bfloat162_rn(p.x, p.y);
-            out[i] = *reinterpret_cast<const uint32_t*>(&b);
+            out[2 * i] = pair(lo, 0x4140u);
+            out[2 * i + 1] = pair(lo, 0x4342u);
+            out[8 + 2 * i] = pair(hi, 0x4140u);
+            out[8 + 2 * i + 1] = pair(hi, 0x4342u);
         }
     } else {
+        // fp32: each code byte under the pattern of 2^23 is 2^23 + c + 128 exactly; the
+        // exact c * d (packed f32x2) is rounded once to bf16.
+        const float2 dd = make_float2(d, d);
+        float v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t w = word_at(r, base + 2 + 4 * i) ^ 0x80808080u;   // c + 128

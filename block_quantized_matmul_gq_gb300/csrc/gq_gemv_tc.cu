@@ -1,4 +1,4 @@
-// gq_gemv_tc.cu -- decode mul_mat for 5..64 tokens on the tensor cores:
+// gq_gemv_tc.cu -- decode mul_mat for 3..64 tokens on the tensor cores:
 //     Y[n][m] = sum_k What[m][k] * X[n][k]
 //
 // Small-batch decode still streams every weight once, so it stays bound by memory

@@ -23,7 +23,7 @@
  *   - Pointers. Every array pointer is a DEVICE pointer owned by the caller; the library
  *     keeps none of them after the call returns. W_blocks must be 16-byte aligned, fp32
  *     arrays 4-byte aligned (16-byte alignment of X is used when present). A pointer may
- *     be NULL only when its array is empty. The CUDA-core decode path (N <= 4) allocates
+ *     be NULL only when its array is empty. The CUDA-core decode path (N <= 2) allocates
  *     nothing; the tensor-core paths need a workspace (see gq_mul_mat_ws).
  *   - Streams. `stream` is a cudaStream_t (NULL = the legacy default stream) passed as
  *     void* so that this header needs no CUDA include. Calls only enqueue work: they do
@@ -109,8 +109,8 @@ gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * ("No Python! ...", sections 6 and 7.2; "A Complete Guide ...", section 2.1: N = 1 at
  * decode makes this a matrix-vector product.) The weights are dequantized inside the
  * kernel right after they are loaded and never written back.
- * N <= 4 (or K % 256 != 0): decode kernels on CUDA cores (exact integer block products
- * on a 16-bit fixed-point copy of X). 5 <= N <= 64 and K % 256 == 0: decode on tensor
+ * N <= 2 (or K % 256 != 0): decode kernels on CUDA cores (exact integer block products
+ * on a 16-bit fixed-point copy of X). 3 <= N <= 64 and K % 256 == 0: decode on tensor
  * cores; N >= 65 and K % 256 == 0: the prefill tensor-core GEMM. Both tensor-core paths
  * use bf16 operands (dequantized weights and X each rounded once to bf16) and fp32
  * accumulation.
@@ -124,7 +124,7 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,
 
 /*
  * Device workspace (bytes) that gq_mul_mat_ws needs for this shape: 0 on the CUDA-core
- * decode path (N <= 4); on the tensor-core decode path (5 <= N <= 64) P * K * 2 for
+ * decode path (N <= 2); on the tensor-core decode path (3 <= N <= 64) P * K * 2 for
  * P = 16, 32 or 64 token rows of pre-arranged bf16 X, plus 2 * 256 * 128 * P * 4 + 4096
  * for the partial sums (and their counters) of tiles whose k range is split between CTAs;
  * N * K * 2 (a bf16 copy of X, rounded up to 256) on the prefill path (N >= 65).
@@ -152,7 +152,7 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * arena, and real-time loops that must not stall or fail on an allocation mid-run. (The
  * pages have no counterpart: their engine allocates once from an arena; this entry point
  * exists for users of this library.)
- * Same arguments, results and accuracy as gq_mul_mat, except that 5 <= N <= 64 runs on
+ * Same arguments, results and accuracy as gq_mul_mat, except that 3 <= N <= 64 runs on
  * the CUDA-core decode kernels. On the prefill path (N >= 65, K % 256 == 0) its workspace
  * is a fixed 64 MiB device array compiled into the library,
  * which every GPU that loads the library holds until the process exits:

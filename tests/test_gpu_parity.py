@@ -122,15 +122,15 @@ def test_mul_mat_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
 @pytest.mark.parametrize("K", [2048, 96])
 def test_mul_mat_one_hot_is_exact(gq_lib, oracle_mod, cuda_dev, t, K):
     """X = e_k returns column k of What bit for bit on the CUDA-core decode kernels (the
-    streaming one for K = 2048, the generic one for K = 96), called with <= 4 tokens."""
+    streaming one for K = 2048, the generic one for K = 96), called with <= 2 tokens."""
     M = 77
     ks = [0, 1, 15, 16, 31, 32, K - 1] + ([255, 256, 1000] if K > 1000 else [])
     W = _np_weights(M, K, seed=5)
     q = oracle_mod.quantize(t, W)
     What = oracle_mod.dequantize(t, q, M, K)
     qd = torch.from_numpy(q).to(cuda_dev)
-    for i in range(0, len(ks), 4):
-        group = ks[i:i + 4]
+    for i in range(0, len(ks), 2):
+        group = ks[i:i + 2]
         X = np.zeros((len(group), K), np.float32)
         for n, k in enumerate(group):
             X[n, k] = 1.0
@@ -264,7 +264,7 @@ def test_llama7b_shapes_full_size(gq_lib, oracle_mod, cuda_dev, N):
 
 
 # ------------------------------------------------------------------------------------
-# Tensor-core paths (N >= 5, K % 256 == 0): bf16 operands, fp32 accumulation
+# Tensor-core paths (N >= 3, K % 256 == 0): bf16 operands, fp32 accumulation
 # ------------------------------------------------------------------------------------
 GEMM = [(128, 256, 64), (7, 256, 64), (300, 512, 100), (129, 768, 300), (1000, 2048, 257),
         (256, 5632, 64)]
@@ -300,7 +300,7 @@ def test_gemm_workspace_entry_point(gq_lib, oracle_mod, cuda_dev):
     X = workloads.activations(N, K, seed=22).to(cuda_dev)
     need = gq_lib.workspace_size("q4_0", M, K, N)
     assert need == N * K * 2
-    assert gq_lib.workspace_size("q4_0", M, K, 4) == 0          # CUDA-core decode: none
+    assert gq_lib.workspace_size("q4_0", M, K, 2) == 0          # CUDA-core decode: none
     # tensor-core decode: 16-token X tiles, two 128 x 16 partial tiles per CTA (<= 256) and
     # 4 KB of split-tile counters
     assert gq_lib.workspace_size("q4_0", M, K, 8) == 16 * K * 2 + 2 * 256 * 128 * 16 * 4 + 4096
@@ -339,7 +339,7 @@ def test_llama7b_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
 
 
 # ------------------------------------------------------------------------------------
-# Tensor-core decode (5 <= N <= 64, K % 256 == 0): grouped, bf16 operands
+# Tensor-core decode (3 <= N <= 64, K % 256 == 0): grouped, bf16 operands
 # ------------------------------------------------------------------------------------
 DECODE_TC = [(1, 256, 5), (7, 2048, 8), (129, 2048, 16), (1000, 2048, 17), (300, 5632, 32),
              (200, 11008, 33), (128, 512, 64), (2048, 4096, 16)]
