@@ -138,10 +138,11 @@ gq_status run_one(gq_type t, const gq::MatProblem& p, int64_t N, void* ws, size_
         void* w = ws;
         if (w == nullptr) {
             if (internal_workspace(s, need, &w) != cudaSuccess) return GQ_ERR_CUDA;
+            ws_bytes = need;
         } else if (ws_bytes < need || !aligned(ws, 256)) {
             return ws_bytes < need ? GQ_ERR_SHAPE : GQ_ERR_ALIGN;
         }
-        return from_cuda(gq::launch_gemm(t, p, N, w, s));
+        return from_cuda(gq::launch_gemm(t, p, N, w, static_cast<int64_t>(ws_bytes), s));
     }
     return from_cuda(gq::launch_mul_mat(t, &p, 1, N, s));
 }
@@ -272,12 +273,14 @@ gq_status run_batch(gq_type t, int64_t N, BatchPlan* plan, void* ws, size_t ws_b
     if (plan->ws_bytes > 0) {
         if (ws == nullptr) {
             if (internal_workspace(s, plan->ws_bytes, &ws) != cudaSuccess) return GQ_ERR_CUDA;
+            ws_bytes = plan->ws_bytes;
         } else if (ws_bytes < plan->ws_bytes || !aligned(ws, 256)) {
             return ws_bytes < plan->ws_bytes ? GQ_ERR_SHAPE : GQ_ERR_ALIGN;
         }
     }
     for (int i = 0; i < plan->n_gemm; ++i) {
-        gq_status st = from_cuda(gq::launch_gemm(t, plan->gemm[i], N, ws, s));
+        gq_status st = from_cuda(
+            gq::launch_gemm(t, plan->gemm[i], N, ws, static_cast<int64_t>(ws_bytes), s));
         if (st != GQ_OK) return st;
     }
     if (plan->n_tc > 0) {

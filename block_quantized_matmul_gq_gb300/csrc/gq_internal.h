@@ -44,13 +44,14 @@ cudaError_t launch_dequantize(gq_type t, const uint8_t* blocks, int64_t n_elems,
 cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_t N,
                            cudaStream_t s);
 
-// Prefill path: tcgen05 tensor-core GEMM. Needs gemm_workspace_bytes(K, N) bytes of
-// device workspace (a bf16 copy of X), 256-byte aligned.
+// Prefill path: tcgen05 tensor-core GEMM. Its workspace (256-byte aligned) is the bf16
+// copy of X: gemm_x_bytes(K, N) == gemm_workspace_bytes(K, N) bytes.
 constexpr int64_t kGemmMinTokens = 65;
+int64_t gemm_x_bytes(int64_t K, int64_t N);
 int64_t gemm_workspace_bytes(int64_t K, int64_t N);
 bool gemm_eligible(gq_type t, const MatProblem& p, int64_t N);
 cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspace,
-                        cudaStream_t s);
+                        int64_t workspace_bytes, cudaStream_t s);
 
 // Decode on tensor cores for kGemvTcMinTokens..kGemvTcMaxTokens tokens (K % 256 == 0):
 // grouped like launch_mul_mat. Needs gemv_tc_workspace_bytes of workspace (pre-arranged

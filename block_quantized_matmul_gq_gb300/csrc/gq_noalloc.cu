@@ -74,9 +74,12 @@ extern "C" gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t
     const gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
     if (!gq::gemm_eligible(t, p, N))   // decode path: needs no workspace at all
         return gq::launch_mul_mat(t, &p, 1, N, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
-    if (static_cast<size_t>(gq::gemm_workspace_bytes(K, N)) > gq::kNoAllocScratchBytes)
+    if (static_cast<size_t>(gq::gemm_x_bytes(K, N)) > gq::kNoAllocScratchBytes)
         return GQ_ERR_SHAPE;           // N * K beyond the fixed scratch
     void* scratch = nullptr;
     if (gq::noalloc_scratch(&scratch) != cudaSuccess) return GQ_ERR_CUDA;
-    return gq::launch_gemm(t, p, N, scratch, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+    return gq::launch_gemm(t, p, N, scratch, static_cast<int64_t>(gq::kNoAllocScratchBytes), s) ==
+                   cudaSuccess
+               ? GQ_OK
+               : GQ_ERR_CUDA;
 }
