@@ -291,6 +291,73 @@ def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None):
     return out
 
 
+# Decode workloads reported beside the headline step (N tokens per call):
+# (key, workload id, type, shapes, N values).
+DECODE_SETS = [
+    ("single_q4_0_2048x2048", 1, "q4_0", "single", (1,)),
+    ("tinyllama_decode_q8_0", 3, "q8_0", "tinyllama", (1, 2, 4, 8, 16)),
+    ("llama7b_decode_q4_0", 5, "q4_0", "llama7b", (1, 16)),
+]
+L2_BYTES = 129 * 2 ** 20
+STEPS_PER_GRAPH = 10
+
+
+def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
+    """Each decode set as batched calls (one per step) replayed from a CUDA graph; weight
+    sets smaller than 4x L2 are copied (distinct seeds) and rotated so every step reads
+    its weights from HBM. GB/s counts weights + X + Y once per step."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    from block_quantized_matmul_gq_gb300.weightset import QuantizedWeightSet
+    peak, _ = measured_peaks()
+    out = {}
+    for key, wl, btype, which, Ns in DECODE_SETS:
+        shapes = {"single": [workloads.MatShape("proj", 2048, 2048)],
+                  "tinyllama": workloads.tinyllama_decode_set(),
+                  "llama7b": workloads.llama7b_set()}[which]
+        nb1 = step_bytes(shapes, 1, binding.block_bytes(btype))
+        copies = min(64, max(1, -(-4 * L2_BYTES // nb1["weights"])))
+        sets = [QuantizedWeightSet.synthetic(wl if c == 0 else 100 * wl + c, shapes, btype, dev)
+                for c in range(copies)]
+        rows = []
+        for N in Ns:
+            nb = step_bytes(shapes, N, binding.block_bytes(btype))
+            runs = []
+            for c, ws in enumerate(sets):
+                xs, ys = ws.make_io(N, wl, dev)
+                arrays = ws.problem_arrays(xs, ys)
+                work = ws.workspace(arrays, N, dev)
+                runs.append((ws, arrays, work, xs, ys))
+            for ws, arrays, work, _, _ in runs:
+                ws.run(arrays, N, workspace=work)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for r in range(reps):
+                    ws, arrays, work, _, _ = runs[r % copies]
+                    ws.run(arrays, N, workspace=work)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(iters):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+            gbs = nb["total"] / sec / 1e9
+            rows.append({"N": N, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
+                         "frac": round(gbs / peak, 4),
+                         "path": "CUDA-core decode" if N <= 2 else "tensor-core decode"})
+            del runs, g
+        if binding.get_last_error() != 0:
+            raise RuntimeError("device status word set during the decode sets")
+        out[key] = {"type": btype, "matmuls": len(shapes), "weight_bytes": nb1["weights"],
+                    "weight_copies_rotated": copies, "per_N": rows}
+        del sets
+    return out
+
+
 def profile_decode(spec: str, steps: int) -> dict:
     """For ncu: the TinyLLaMA decode step with N tokens (spec "q8_0/16"), one batched call
     per step with a caller-owned workspace, 3 warm-up steps then `steps` timed ones."""
@@ -400,22 +467,32 @@ def run_gb300(args, shapes):
                   "value": round(nb["total"] / ms / 1e6, 2), "unit": UNIT})
         return
 
+    # Timed steps replay a graph of G consecutive steps (as a decode engine replays one
+    # graph per step holding this launch among others): no host round trip between steps.
+    G = STEPS_PER_GRAPH if args.steps % STEPS_PER_GRAPH == 0 else 1
+    graph_g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_g):
+        for _ in range(G):
+            ws.run(arrays, N)
+    graph_g.replay()
+    torch.cuda.synchronize(dev)
+
     # Load phase (about 1 s) so the clock samples see the GPU busy, then the timed steps.
     t_probe = time.perf_counter()
-    for _ in range(50):
-        graph.replay()
+    for _ in range(5):
+        graph_g.replay()
     torch.cuda.synchronize(dev)
-    per = (time.perf_counter() - t_probe) / 50
+    per = (time.perf_counter() - t_probe) / (5 * G)
     load_steps = int(min(20000, max(10, 1.0 / max(per, 1e-6))))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
-        for _ in range(load_steps):
-            graph.replay()
+        for _ in range(max(1, load_steps // G)):
+            graph_g.replay()
         barrier()
         torch.cuda.synchronize(dev)
         start.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
+        for _ in range(args.steps // G):
+            graph_g.replay()
         end.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -460,7 +537,8 @@ def run_gb300(args, shapes):
         "config": {"workload": WORKLOAD_NAME, "N": N, "matmuls": len(shapes),
                    "weight_bytes": nb["weights"], "algorithmic_bytes_per_step": nb["total"],
                    "l2": "inputs larger than L2: 582 MB of weights streamed per step vs 129 MB L2",
-                   "launch": f"{launches_per_step} gq_mul_mat_batched launch per step, CUDA graph replay",
+                   "launch": f"{launches_per_step} gq_mul_mat_batched launch per step, "
+                             f"CUDA graph of {G} steps replayed",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(per_gpu, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(per_gpu / peak, 4),
@@ -476,6 +554,8 @@ def run_gb300(args, shapes):
         "clocks": clk,
     }
     if rank == 0:
+        line["decode"] = {"unit": "GB/s", "peak": peak, "peak_source": line["roofline"]["peak_source"],
+                          **decode_measure(dev)}
         pf = prefill_measure(dev)
         line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16 operands, fp32 accumulate",
                            "peak": measured_bf16_peak(),

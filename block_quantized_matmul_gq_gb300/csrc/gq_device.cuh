@@ -113,6 +113,16 @@ __device__ __forceinline__ void release_to_async_proxy(uint32_t depends_on_loads
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same hand-back when the whole warp has read the buffer and lane 0 issues the refill:
+// each lane waits for its own loads, the warp synchronises (ordering every lane's reads
+// before lane 0's next instructions), and lane 0 alone fences the generic proxy against
+// the async proxy that its copy writes through. Call with all lanes of the warp.
+__device__ __forceinline__ void release_warp_to_async_proxy(uint32_t depends_on_loads) {
+    asm volatile("" ::"r"(depends_on_loads) : "memory");
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void report_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }

@@ -522,8 +522,7 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
                     chunk_dot<kType, kNT>(ring + s * G::kStageBytes + rrow * rs +
                                               lc * G::kChunkBytes,
                                           xbuf + col * G::kXRec, rec_stride, acc);
-                release_to_async_proxy(__float_as_uint(acc[0]));   // the stage is refilled next
-                __syncwarp();
+                release_warp_to_async_proxy(__float_as_uint(acc[0]));   // lane 0 refills it
                 ++consumed;
                 if (prod.valid) issue(s);   // refill the stage just read
             }
