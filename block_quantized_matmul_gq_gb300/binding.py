@@ -209,6 +209,8 @@ def make_problems(items) -> ctypes.Array:
         arr[i] = Problem(_dev(blocks, torch.uint8, "W_blocks"), _dev(X, torch.float32, "X"),
                          _dev(Y, torch.float32, "Y"), M, K)
     arr._count = len(items)
+    # The array holds raw device pointers: keep the tensors alive as long as it lives.
+    arr._tensors = [(blocks, X, Y) for blocks, _, _, X, Y in items]
     return arr
 
 

@@ -9,8 +9,9 @@
 //
 // GB300 design (not the pages' CPU/SIMD one):
 //  * One persistent CTA per SM. All problems of a launch form one sequence of rows; each
-//    CTA takes a contiguous, row-aligned share of equal bytes, so small matrices (GQA
-//    k/v projections) ride along with large ones and no CTA idles on a tail.
+//    CTA takes a contiguous, row-aligned share of equal estimated time (bytes plus a fixed
+//    cost per ring stage), so small matrices (GQA k/v projections) ride along with large
+//    ones and no CTA idles on a tail.
 //  * Inside a CTA, each warp owns tiles of 4 rows; eight lanes share a row and walk its K
 //    columns eight "chunks" at a time (a chunk is 8 Q4_0 blocks = 144 B = 256 weights, or
 //    4 Q8_0 blocks = 136 B = 128 weights), one chunk per lane. Every warp streams its own
@@ -111,7 +112,8 @@ struct GemvProb {
     float* Y;
     int64_t M;
     int64_t row_bytes;
-    int64_t byte_begin;   // bytes of all earlier problems
+    int64_t row_cost;     // balancing weight of one row (see kGroupCost)
+    int64_t cost_begin;   // weight of all earlier problems
     int32_t C;            // chunks per row
     int32_t K;
 };
@@ -123,17 +125,25 @@ struct GemvParams {
     int32_t max_c;        // largest C: the x buffer holds kNT * max_c records
     int32_t pad_;
     int64_t total_bytes;
+    int64_t total_cost;
     unsigned* status;
     GemvProb p[kMaxProbs];
 };
 
-// First row (problem p, row r) whose first byte is at or after `byte`; (count, 0) = end.
+// CTA shares balance an estimate of time rather than bytes: a row weighs its bytes plus
+// kGroupCost for each column group (one ring stage per 4-row tile), the part of a stage's
+// cost that does not scale with its bytes (waits, refill, shuffles; a partly filled last
+// group costs the same as a full one). 576 was the best of 0 / 576 / 1152 / 2304 / 4608
+// measured on the TinyLLaMA and LLaMA-7B sets (Q4_0 and Q8_0, N = 1 and 2).
+constexpr int64_t kGroupCost = 576;
+
+// First row (problem p, row r) whose weight begins at or after `cost`; (count, 0) = end.
 template <int kMaxProbs>
-__device__ void row_at_byte(const GemvParams<kMaxProbs>& P, int64_t byte, int& p, int64_t& r) {
+__device__ void row_at_cost(const GemvParams<kMaxProbs>& P, int64_t cost, int& p, int64_t& r) {
     p = 0;
-    while (p + 1 < P.count && P.p[p + 1].byte_begin <= byte) ++p;
-    const int64_t off = byte - P.p[p].byte_begin;
-    r = off <= 0 ? 0 : (off + P.p[p].row_bytes - 1) / P.p[p].row_bytes;
+    while (p + 1 < P.count && P.p[p + 1].cost_begin <= cost) ++p;
+    const int64_t off = cost - P.p[p].cost_begin;
+    r = off <= 0 ? 0 : (off + P.p[p].row_cost - 1) / P.p[p].row_cost;
     if (r >= P.p[p].M) {
         ++p;
         r = 0;
@@ -454,8 +464,8 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     // row starting at or after byte (c+1)*T/G.
     int p0, p1;
     int64_t r0, r1;
-    row_at_byte(P, P.total_bytes * blockIdx.x / gridDim.x, p0, r0);
-    row_at_byte(P, P.total_bytes * (blockIdx.x + 1) / gridDim.x, p1, r1);
+    row_at_cost(P, P.total_cost * blockIdx.x / gridDim.x, p0, r0);
+    row_at_cost(P, P.total_cost * (blockIdx.x + 1) / gridDim.x, p1, r1);
     const Segment first = find_segment(P, p0, r0, p1, r1);
 
     // Producer side of this warp's ring: the cursor's tile rows, one column group (up to 8
@@ -682,7 +692,7 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
     const int wpc = t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kWPC : Geo<GQ_TYPE_Q8_0>::kWPC;
     const int cb = t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kChunkBytes
                                      : Geo<GQ_TYPE_Q8_0>::kChunkBytes;
-    int64_t bytes = 0;
+    int64_t bytes = 0, cost = 0;
     int max_c = 1;
     for (int i = 0; i < count; ++i) {
         GemvProb& g = P.p[i];
@@ -693,11 +703,14 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
         g.K = static_cast<int32_t>(probs[i].K);
         g.C = static_cast<int32_t>(probs[i].K / wpc);
         g.row_bytes = static_cast<int64_t>(g.C) * cb;
-        g.byte_begin = bytes;
+        g.row_cost = g.row_bytes + kGroupCost * ((g.C + kLanesPerRow - 1) / kLanesPerRow);
+        g.cost_begin = cost;
         bytes += g.M * g.row_bytes;
+        cost += g.M * g.row_cost;
         max_c = std::max(max_c, g.C);
     }
     P.total_bytes = bytes;
+    P.total_cost = cost;
     P.max_c = max_c;
     if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs>(P, info, s);
     return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs>(P, info, s);

@@ -105,7 +105,8 @@ def run_mul_mat(gq_lib, oracle_mod, dev, t, M, K, N, seed=0, X=None):
 # Fast streaming kernel: K % 256 == 0. Rows of K = 11008 (Q4_0: 43 chunks) straddle the
 # 256-chunk stages, M values leave ragged tails, N covers 1..4 and token groups 4+4+1.
 FAST = [(1, 256, 1), (7, 2048, 1), (300, 2048, 1), (1000, 2048, 2), (129, 5632, 3),
-        (64, 11008, 4), (33, 4096, 5), (257, 1024, 9), (2048, 2048, 1)]
+        (64, 11008, 4), (33, 4096, 5), (257, 1024, 9), (2048, 2048, 1), (200, 11008, 1),
+        (65, 4096, 2)]
 # Generic kernel: K % 256 != 0.
 GENERIC = [(1, 32, 1), (5, 96, 2), (37, 288, 3), (64, 800, 4), (9, 160, 7)]
 
