@@ -12,6 +12,8 @@ Every function follows the pages as cited in ``gq_oracle.c``:
   - dequantize / mul_mat: "Development Guide ...", section 6.2 (load, unpack, dequantize,
     FMA) and "No Python! Building an AI Inference Engine Exclusively in C++", sections 6
     and 7.2 (C = A B; Y = X W^T in the cuBLAS call's layout).
+  - mul_mat_q8x: "A Complete Guide to llama.cpp ...", section 2.2 (x quantized like the
+    weights; y ~= Delta Delta_x sum q q_x with an integer sum per block).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` (IEEE fp16
 conversion against numpy, closed-form blocks, exact-rational brute force, one-hot rows).
@@ -70,6 +72,8 @@ def _load():
         lib.oracle_dequantize.restype = c_int
         lib.oracle_mul_mat.argtypes = [c_int, vp, c_int64, c_int64, vp, c_int64, vp, vp]
         lib.oracle_mul_mat.restype = c_int
+        lib.oracle_mul_mat_q8x.argtypes = [c_int, vp, c_int64, c_int64, vp, c_int64, vp, vp]
+        lib.oracle_mul_mat_q8x.restype = c_int
         _lib = lib
     return _lib
 
@@ -149,6 +153,33 @@ def mul_mat(t, blocks, M: int, K: int, X) -> np.ndarray:
     if rc:
         raise ValueError("oracle_mul_mat rejected its arguments")
     return Y
+
+
+def mul_mat_q8x(t, blocks, M: int, K: int, X) -> np.ndarray:
+    """Y (N x M fp32) with X quantized per 32-block like Q8_0 and each block's dot product
+    an exact integer sum ("A Complete Guide to llama.cpp ...", section 2.2):
+    Y[n][m] = sum_b Delta_w * Delta_x * sum_i q_i q_x,i, in fp64 on one CPU thread."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    X = _f32(X)
+    if X.ndim == 1:
+        X = X.reshape(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K or blocks.size != M * row_bytes(t, K):
+        raise ValueError("shape mismatch")
+    Y = np.empty((N, M), dtype=np.float32)
+    xq = np.empty(max(1, N * (K // 32) * 34), dtype=np.uint8)
+    rc = _load().oracle_mul_mat_q8x(_type(t), blocks.ctypes.data, M, K, X.ctypes.data, N,
+                                    Y.ctypes.data, xq.ctypes.data)
+    if rc:
+        raise ValueError("oracle_mul_mat_q8x rejected its arguments")
+    return Y
+
+
+def mul_mat_q8x_rows(t, blocks, M: int, K: int, X, rows) -> np.ndarray:
+    """mul_mat_q8x on the selected rows only (for sampled checks of large problems)."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(M, row_bytes(t, K))
+    rows = np.asarray(rows, dtype=np.int64)
+    return mul_mat_q8x(t, np.ascontiguousarray(blocks[rows]), len(rows), K, X)
 
 
 def mul_mat_rows(t, blocks, M: int, K: int, X, rows) -> np.ndarray:

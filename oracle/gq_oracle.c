@@ -259,3 +259,51 @@ int oracle_mul_mat(int type, const uint8_t* blocks, int64_t M, int64_t K,
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------------- */
+/* mul_mat with quantized activations ("A Complete Guide to llama.cpp and             */
+/* Customization with C++", section 2.2, the last two displayed formulas): when x is  */
+/* "similarly quantized", x_i ~= Delta_x * q_x,i, the block dot product becomes       */
+/* Delta * Delta_x * sum_i q_i q_x,i with the sum a pure integer operation.           */
+/* Reading (the pages give no x bit width or scale rule): every 32-element block of an */
+/* activation row is quantized exactly like a Q8_0 weight block (Delta_x = fp16 of    */
+/* max |x| / 127, codes round(x / Delta) in [-127, 127]). q_i is the signed weight    */
+/* code: c - 8 (Q4_0) or c (Q8_0). Then                                               */
+/*     Y[n][m] = (float) sum_b (double) Delta_w[m][b] * (double) Delta_x[n][b] * S_b, */
+/* S_b = sum over the block of q_i * q_x,i (an exact integer), b in increasing order. */
+/* `xq` is caller-provided space for the quantized X: N * K / 32 blocks of 34 bytes.  */
+/* ---------------------------------------------------------------------------------- */
+static int weight_code(int type, const uint8_t* blk, int i)
+{
+    if (type == ORACLE_TYPE_Q4_0) {
+        const int byte = blk[2 + (i & 15)];
+        return (i < 16 ? (byte & 0x0F) : (byte >> 4)) - 8;
+    }
+    return (int)(int8_t)blk[2 + i];
+}
+
+int oracle_mul_mat_q8x(int type, const uint8_t* blocks, int64_t M, int64_t K,
+                       const float* X, int64_t N, float* Y, uint8_t* xq)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0 || N < 0) return -1;
+    const int64_t nb = K / 32;
+    if (oracle_quantize(ORACLE_TYPE_Q8_0, X, N, K, xq) != 0) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = blocks + (m * nb + b) * bb;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                int64_t sum = 0;
+                for (int i = 0; i < 32; ++i)
+                    sum += (int64_t)weight_code(type, wb, i) * (int64_t)(int8_t)xb[2 + i];
+                const double dw = (double)oracle_f32_from_fp16(get_u16_le(wb));
+                const double dx = (double)oracle_f32_from_fp16(get_u16_le(xb));
+                acc += dw * dx * (double)sum;
+            }
+            Y[n * M + m] = (float)acc;
+        }
+    }
+    return 0;
+}

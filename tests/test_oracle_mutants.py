@@ -32,6 +32,11 @@ MUTANTS = {
     "fp16_flush_subnormal": ("if (drop > 24) return sign;", "if (drop > 13) return sign;"),
     "fp16_truncate": ("if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;", ""),
     "q8_scale_divisor": ("const float d = amax / 127.0f;", "const float d = amax / 128.0f;"),
+    "q8x_code_offset": ("return (i < 16 ? (byte & 0x0F) : (byte >> 4)) - 8;",
+                        "return (i < 16 ? (byte & 0x0F) : (byte >> 4)) - 7;"),
+    "q8x_scale": ("acc += dw * dx * (double)sum;", "acc += dw * (double)sum;"),
+    "q8x_x_block": ("const uint8_t* xb = xq + (n * nb + b) * 34;",
+                    "const uint8_t* xb = xq + (n * nb + (nb - 1 - b)) * 34;"),
 }
 
 

@@ -316,6 +316,72 @@ def test_mul_mat_rows_subset(oracle_mod):
 
 
 # ------------------------------------------------------------------------------------
+# mul_mat with quantized activations (integer block sums)
+# ------------------------------------------------------------------------------------
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 32), (3, 4, 64), (6, 2, 96)])
+def test_mul_mat_q8x_exact_rational(oracle_mod, t, M, N, K):
+    """Y equals the exact sum over blocks of Delta_w * Delta_x * sum q_i q_x,i, written
+    out here from the block bytes (codes, scales) with rational arithmetic."""
+    W = workloads.weights(M, K, seed=7 * M + K).numpy()
+    X = workloads.activations(N, K, seed=11 * N + K).numpy()
+    q = oracle_mod.quantize(t, W)
+    xq = oracle_mod.quantize("q8_0", X)
+    Y = oracle_mod.mul_mat_q8x(t, q, M, K, X)
+    bb = 18 if t == "q4_0" else 34
+    for n in range(N):
+        for m in range(M):
+            exact = Fraction(0)
+            terms = []
+            for b in range(K // 32):
+                wb = q[m, bb * b: bb * b + bb]
+                xb = xq[n, 34 * b: 34 * b + 34]
+                if t == "q4_0":
+                    codes = [(int(wb[2 + (i & 15)]) >> (4 if i >= 16 else 0) & 0xF) - 8
+                             for i in range(32)]
+                else:
+                    codes = [int(v) - 256 if v > 127 else int(v) for v in wb[2:]]
+                xc = [int(v) - 256 if v > 127 else int(v) for v in xb[2:]]
+                s_b = sum(a * c for a, c in zip(codes, xc))
+                term = (Fraction(float(wb[:2].view(np.float16)[0])) *
+                        Fraction(float(xb[:2].view(np.float16)[0])) * s_b)
+                terms.append(term)
+                exact += term
+            slack = _ulp32(Y[n, m]) / 2 + (K // 32) * Fraction(2) ** -53 * sum(abs(x) for x in terms)
+            assert abs(Fraction(float(Y[n, m])) - exact) <= slack, (n, m)
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_mul_mat_q8x_equals_mul_mat_of_dequantized_x(oracle_mod, t):
+    """Delta_w Delta_x sum q q_x = sum What * Xhat with Xhat the Q8_0-dequantized X, every
+    product exact: the two oracle paths agree to fp32 rounding."""
+    M, N, K = 24, 3, 512
+    W = workloads.weights(M, K, seed=12).numpy()
+    X = workloads.activations(N, K, seed=13).numpy()
+    q = oracle_mod.quantize(t, W)
+    xhat = oracle_mod.dequantize("q8_0", oracle_mod.quantize("q8_0", X), N, K)
+    a = oracle_mod.mul_mat_q8x(t, q, M, K, X).astype(np.float64)
+    b = oracle_mod.mul_mat(t, q, M, K, xhat).astype(np.float64)
+    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -23 + 1e-30)
+
+
+def test_mul_mat_q8x_exact_when_x_is_representable(oracle_mod):
+    """X whose blocks are integers times a power of two with max |code| = 127 quantizes
+    without error, so the quantized-activation product equals the plain one."""
+    M, N, K = 9, 2, 256
+    rng = np.random.default_rng(5)
+    codes = rng.integers(-127, 128, size=(N, K))
+    codes[:, ::32] = 127                                   # every block reaches 127
+    X = (codes * 2.0 ** -7).astype(np.float32)
+    W = workloads.weights(M, K, seed=14).numpy()
+    for t in ("q4_0", "q8_0"):
+        q = oracle_mod.quantize(t, W)
+        a = oracle_mod.mul_mat_q8x(t, q, M, K, X).astype(np.float64)
+        b = oracle_mod.mul_mat(t, q, M, K, X).astype(np.float64)
+        assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -23 + 1e-30), t
+
+
+# ------------------------------------------------------------------------------------
 # Figures the pages print
 # ------------------------------------------------------------------------------------
 def test_page_facts():
