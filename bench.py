@@ -358,6 +358,46 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
     return out
 
 
+def q8x_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2, 4, 8, 16)) -> dict:
+    """The TinyLLaMA Q4_0 decode step through gq_mul_mat_q8x (X quantized per 32-block
+    like Q8_0, integer block sums): batched calls replayed from a CUDA graph. GB/s counts
+    weights + X + Y once per step, as for the exact path."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    from block_quantized_matmul_gq_gb300.weightset import QuantizedWeightSet
+    peak, _ = measured_peaks()
+    shapes = workloads.tinyllama_decode_set()
+    ws = QuantizedWeightSet.synthetic(WORKLOAD_ID, shapes, "q4_0", dev)
+    rows = []
+    for N in Ns:
+        nb = step_bytes(shapes, N, binding.block_bytes("q4_0"))
+        xs, ys = ws.make_io(N, WORKLOAD_ID, dev)
+        arrays = ws.problem_arrays(xs, ys)
+        ws.run_q8x(arrays, N)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                ws.run_q8x(arrays, N)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+        gbs = nb["total"] / sec / 1e9
+        rows.append({"N": N, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
+                     "frac": round(gbs / peak, 4)})
+        del g, xs, ys, arrays
+    if binding.get_last_error() != 0:
+        raise RuntimeError("device status word set during the q8x steps")
+    return {"workload": "TinyLLaMA-1.1B decode step, Q4_0 weights, X quantized like Q8_0",
+            "unit": "GB/s", "per_N": rows}
+
+
 def profile_decode(spec: str, steps: int) -> dict:
     """For ncu: the TinyLLaMA decode step with N tokens (spec "q8_0/16"), one batched call
     per step with a caller-owned workspace, 3 warm-up steps then `steps` timed ones."""
@@ -556,6 +596,7 @@ def run_gb300(args, shapes):
     if rank == 0:
         line["decode"] = {"unit": "GB/s", "peak": peak, "peak_source": line["roofline"]["peak_source"],
                           **decode_measure(dev)}
+        line["decode_q8x"] = q8x_measure(dev)
         pf = prefill_measure(dev)
         line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16 operands, fp32 accumulate",
                            "peak": measured_bf16_peak(),

@@ -34,7 +34,8 @@ STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
            "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
            "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched",
-           "gq_mul_mat_batched_workspace_size", "gq_mul_mat_batched_ws", "gq_get_last_error",
+           "gq_mul_mat_batched_workspace_size", "gq_mul_mat_batched_ws", "gq_mul_mat_q8x",
+           "gq_mul_mat_q8x_batched", "gq_get_last_error",
            "gq_selftest_wait_timeout", "gq_status_string")
 
 
@@ -72,6 +73,10 @@ def load(path: str = LIB_PATH):
     L.gq_mul_mat_batched_ws.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp,
                                         ctypes.c_size_t, vp]
     L.gq_mul_mat_batched_ws.restype = ctypes.c_int
+    L.gq_mul_mat_q8x.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp]
+    L.gq_mul_mat_q8x.restype = ctypes.c_int
+    L.gq_mul_mat_q8x_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
+    L.gq_mul_mat_q8x_batched.restype = ctypes.c_int
     L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
     L.gq_selftest_wait_timeout.argtypes = [i64, vp]
     L.gq_selftest_wait_timeout.restype = ctypes.c_int
@@ -242,6 +247,29 @@ def mul_mat_batched_ws(problems, t, N: int, workspace: torch.Tensor | None, stre
     wn = workspace.numel() if workspace is not None else 0
     _check(lib.gq_mul_mat_batched_ws(problems, problems._count, _type(t), N, wp, wn,
                                      _stream(stream)), "gq_mul_mat_batched_ws")
+
+
+def mul_mat_q8x(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y (N, M) with X quantized per 32-block like Q8_0 and integer block sums."""
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K:
+        raise ValueError("X must be (N, K)")
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    _check(lib.gq_mul_mat_q8x(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
+                              _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
+                              _stream(stream)), "gq_mul_mat_q8x")
+    return out
+
+
+def mul_mat_q8x_batched(problems, t, N: int, stream=None) -> None:
+    if not isinstance(problems, ctypes.Array):
+        problems = make_problems(problems)
+    _check(lib.gq_mul_mat_q8x_batched(problems, problems._count, _type(t), N, _stream(stream)),
+           "gq_mul_mat_q8x_batched")
 
 
 def get_last_error(stream=None) -> int:

@@ -295,6 +295,69 @@ gq_status run_batch(gq_type t, int64_t N, BatchPlan* plan, void* ws, size_t ws_b
 
 extern "C" {
 
+}  // extern "C"
+
+namespace {
+
+// Checks one quantized-activation problem; on success *run tells whether it has work
+// (M, N, K all > 0). K == 0 problems get Y zeroed on the stream when `zero_k0`.
+gq_status check_q8x(const void* W, gq_type t, int64_t M, int64_t K, const float* X, int64_t N,
+                    float* Y, cudaStream_t s, bool zero_k0, bool* run) {
+    bool empty = false;
+    *run = false;
+    gq_status st = check_problem(W, t, M, K, X, N, Y, &empty);
+    if (st != GQ_OK || empty) return st;
+    if (K == 0) {
+        if (zero_k0 && cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s) != cudaSuccess)
+            return GQ_ERR_CUDA;
+        return GQ_OK;
+    }
+    if (!aligned(X, 16)) return GQ_ERR_ALIGN;
+    const gq::MatProblem p{static_cast<const uint8_t*>(W), X, Y, M, K};
+    if (K % 256 != 0 || !gq::q8x_eligible(t, p)) return GQ_ERR_SHAPE;
+    *run = true;
+    return GQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gq_status gq_mul_mat_q8x(const void* W_blocks, gq_type t, int64_t M, int64_t K, const float* X,
+                         int64_t N, float* Y, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool run = false;
+    gq_status st = check_q8x(W_blocks, t, M, K, X, N, Y, s, true, &run);
+    if (st != GQ_OK || !run) return st;
+    const gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
+    return from_cuda(gq::launch_mul_mat_q8x(t, &p, 1, N, s));
+}
+
+gq_status gq_mul_mat_q8x_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
+                                 int64_t N, void* stream) {
+    if (count < 0 || count > GQ_MAX_BATCH) return GQ_ERR_SHAPE;
+    if (!known_type(t)) return GQ_ERR_TYPE;
+    if (count == 0) return GQ_OK;
+    if (!problems) return GQ_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool run = false;
+    for (int i = 0; i < count; ++i) {   // every argument check before any work is queued
+        const gq_mul_mat_problem& p = problems[i];
+        gq_status st = check_q8x(p.W_blocks, t, p.M, p.K, p.X, N, p.Y, s, false, &run);
+        if (st != GQ_OK) return st;
+    }
+    gq::MatProblem runs[GQ_MAX_BATCH];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+        const gq_mul_mat_problem& p = problems[i];
+        gq_status st = check_q8x(p.W_blocks, t, p.M, p.K, p.X, N, p.Y, s, true, &run);
+        if (st != GQ_OK) return st;
+        if (run) runs[n++] = {static_cast<const uint8_t*>(p.W_blocks), p.X, p.Y, p.M, p.K};
+    }
+    if (n == 0) return GQ_OK;
+    return from_cuda(gq::launch_mul_mat_q8x(t, runs, n, N, s));
+}
+
 gq_status gq_mul_mat_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
                              int64_t N, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -65,6 +65,10 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kLanesPerRow = 8;               // one chunk per lane, 8 chunks per row per stage
 constexpr int kTileRows = 32 / kLanesPerRow;   // 4 rows per warp tile
 constexpr int kMaxTok = 4;                     // tokens per pass of the weight stream
+// The same with Q8_0-quantized activations: their records are smaller, but more tokens per
+// pass measured no faster (the per-token block sums bind from 4 tokens on: 212 us for 4,
+// 431 us for 8 on the TinyLLaMA step).
+constexpr int kMaxTokQ8x = 4;
 // Ring depth per warp: deeper while the x16 buffer is small (<= 3 tokens).
 template <int kNT>
 __host__ __device__ constexpr int ring_stages() {
@@ -346,6 +350,170 @@ __device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
     return d;
 }
 
+// ---------------------------------------------------------------------------------------
+// Quantized activations ("A Complete Guide to llama.cpp and Customization with C++",
+// section 2.2: x_i ~= Delta_x q_x,i, and a block's dot product Delta Delta_x sum q q_x is
+// a pure integer operation). Every 32-element block of x is quantized like a Q8_0 weight
+// block: Delta = max |x| / 127 (IEEE division), q_x = round(x / Delta) (halves away from
+// zero) clamped to [-127, 127], Delta_x = the fp16 value of Delta. Per block the integer
+// sum S = sum q_i q_x,i comes from dp4a (four 8-bit products per instruction), and
+// y += (Delta_w * Delta_x) * S: the scale product is exact in fp32 (11 + 11 bits), S is
+// exact (|S| <= 127 * 127 * 32 < 2^24), one rounding per block.
+// Record of one chunk for one token: kWPC int8 codes, then Delta_x per block (float),
+// then for Q4_0 the sum of the block's codes (int; folds in the weights' -8 offset).
+// Strides of 84 / 36 words (20 / 4 mod 32) put the 8 columns a warp reads in different
+// bank groups.
+// ---------------------------------------------------------------------------------------
+template <int kType>
+struct Q8xRec {
+    using G = Geo<kType>;
+    static constexpr int kScaleOff = G::kWPC;
+    static constexpr int kSumOff = kScaleOff + 4 * G::kBPC;
+    static constexpr int kUsed = kSumOff + (kType == GQ_TYPE_Q4_0 ? 4 * G::kBPC : 0);
+    static constexpr int kXRec = kType == GQ_TYPE_Q4_0 ? 336 : 144;
+    static_assert(kUsed <= kXRec && kXRec % 16 == 0, "record layout");
+};
+
+// Bytes of one chunk's activation record: x16 fixed point (kXM = 0) or Q8_0 codes (1).
+template <int kType, int kXM>
+__host__ __device__ constexpr int xrec_bytes() {
+    return kXM ? Q8xRec<kType>::kXRec : Geo<kType>::kXRec;
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <int kType, int kNT>
+__device__ void prepare_x_q8x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbuf) {
+    using G = Geo<kType>;
+    using R = Q8xRec<kType>;
+    constexpr int kPerLane = G::kWPC / 32;         // 8 (Q4_0 chunk) or 4 (Q8_0 chunk)
+    constexpr int kLanesPerBlock = 32 / kPerLane;  // lanes that share one 32-element block
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int C = pr.C;
+    for (int idx = warp; idx < kNT * C; idx += kWarps) {
+        const int t = idx / C;
+        const int col = idx - t * C;
+        uint8_t* rec = xbuf + (t * max_c + col) * R::kXRec;
+        float v[kPerLane];
+        if (t < n_tok) {
+            const float4* src = reinterpret_cast<const float4*>(
+                pr.X + static_cast<int64_t>(t) * pr.K + col * G::kWPC + lane * kPerLane);
+#pragma unroll
+            for (int i = 0; i < kPerLane / 4; ++i) {
+                const float4 f = __ldg(src + i);
+                v[4 * i] = f.x;
+                v[4 * i + 1] = f.y;
+                v[4 * i + 2] = f.z;
+                v[4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int o = 1; o < kLanesPerBlock; o <<= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float d = amax / 127.0f;
+        uint32_t packed[kPerLane / 4];
+        int sum = 0;
+#pragma unroll
+        for (int w = 0; w < kPerLane / 4; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                int c = 0;
+                if (d != 0.0f) c = max(-127, min(127, static_cast<int>(roundf(v[4 * w + i] / d))));
+                sum += c;
+                word |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * i);
+            }
+            packed[w] = word;
+        }
+        if constexpr (kPerLane == 8)
+            *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
+        else
+            *reinterpret_cast<uint32_t*>(rec + lane * 4) = packed[0];
+#pragma unroll
+        for (int o = 1; o < kLanesPerBlock; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (lane % kLanesPerBlock == 0) {
+            const int j = lane / kLanesPerBlock;
+            reinterpret_cast<float*>(rec + R::kScaleOff)[j] = __half2float(__float2half_rn(d));
+            if constexpr (kType == GQ_TYPE_Q4_0) reinterpret_cast<int*>(rec + R::kSumOff)[j] = sum;
+        }
+    }
+}
+
+// One chunk against every token's Q8_0 record: out[t] += sum over the chunk's blocks of
+// (Delta_w * Delta_x) * S.
+template <int kType, int kNT>
+__device__ __forceinline__ void chunk_dot_q8x(const uint8_t* raw, const uint8_t* xrec0,
+                                              int rec_stride, float (&out)[kNT]) {
+    using G = Geo<kType>;
+    using R = Q8xRec<kType>;
+    uint32_t r[G::kChunkWords];
+    if constexpr (kType == GQ_TYPE_Q4_0) {
+#pragma unroll
+        for (int i = 0; i < G::kChunkWords / 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 * i);
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < G::kChunkWords / 2; ++i) {
+            const uint2 v = *reinterpret_cast<const uint2*>(raw + 8 * i);
+            r[2 * i] = v.x;
+            r[2 * i + 1] = v.y;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < G::kBPC; ++j) {
+        const int base = j * G::kBB;
+        const float dw = half_bits_to_float(u16_at(r, base));
+        uint32_t q[8];
+        if constexpr (kType == GQ_TYPE_Q4_0) {
+            // unsigned codes c: elements 4i..4i+3 in the low nibbles, 16+4i.. in the high
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = word_at(r, base + 2 + 4 * i);
+                q[i] = w & 0x0F0F0F0Fu;
+                q[4 + i] = (w >> 4) & 0x0F0F0F0Fu;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = word_at(r, base + 2 + 4 * i);
+        }
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            const uint8_t* rec = xrec0 + t * rec_stride;
+            const int4 x0 = *reinterpret_cast<const int4*>(rec + 32 * j);
+            const int4 x1 = *reinterpret_cast<const int4*>(rec + 32 * j + 16);
+            const int xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            int S;
+            if constexpr (kType == GQ_TYPE_Q4_0) {
+                S = -8 * reinterpret_cast<const int*>(rec + R::kSumOff)[j];   // sum (c - 8) q_x
+#pragma unroll
+                for (int i = 0; i < 8; ++i) S = dp4a_us(q[i], xs[i], S);
+            } else {
+                S = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) S = __dp4a(static_cast<int>(q[i]), xs[i], S);
+            }
+            const float dx = reinterpret_cast<const float*>(rec + R::kScaleOff)[j];
+            out[t] = fmaf(dw * dx, static_cast<float>(S), out[t]);
+        }
+    }
+}
+
 // One chunk against every token's x16 record: out[t] += chunk partial (scaled by 2^e).
 template <int kType, int kNT>
 __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xrec0,
@@ -439,17 +607,20 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xre
     }
 }
 
-template <int kType, int kNT, int kMaxProbs>
+// kXM selects the activation form: 0 = 16-bit block fixed point (exact mul_mat within a
+// proven bound), 1 = Q8_0-quantized activations (the quantized-activation product).
+template <int kType, int kNT, int kMaxProbs, int kXM>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     using G = Geo<kType>;
+    constexpr int kRec = xrec_bytes<kType, kXM>();
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int S = ring_stages<kNT>();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint8_t* ring = smem + warp * S * G::kStageBytes;                    // this warp's stages
     uint8_t* xbuf = smem + kWarps * S * G::kStageBytes;
-    const int rec_stride = P.max_c * G::kXRec;
+    const int rec_stride = P.max_c * kRec;
     // Partial row sums of k-split items: [item < kWarps][row][token].
     float* red = reinterpret_cast<float*>(xbuf + kNT * rec_stride);
     uint64_t* bars = reinterpret_cast<uint64_t*>(red + kWarps * kTileRows * kNT) + warp * S;
@@ -508,7 +679,10 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     for (Segment seg = first; seg.valid; seg = find_segment(P, seg.p + 1, 0, p1, r1)) {
         if (__syncthreads_or(timed_out)) break;   // previous segment done everywhere
         const GemvProb& pr = P.p[seg.p];
-        prepare_x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
+        if constexpr (kXM == 0)
+            prepare_x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
+        else
+            prepare_x_q8x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
         __syncthreads();
         const SegPlan sp = plan_segment(seg.re - seg.rb, pr.C);
         for (int item = warp; item < sp.items && !timed_out; item += kWarps) {
@@ -528,10 +702,13 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
                 const int col = kLanesPerRow * cs + lc;
                 // Whole-row stages hold rows at their global stride; others at kRowStride.
                 const int rs = pr.C <= kLanesPerRow ? static_cast<int>(pr.row_bytes) : G::kRowStride;
-                if (rrow < rows && col < pr.C)
-                    chunk_dot<kType, kNT>(ring + s * G::kStageBytes + rrow * rs +
-                                              lc * G::kChunkBytes,
-                                          xbuf + col * G::kXRec, rec_stride, acc);
+                if (rrow < rows && col < pr.C) {
+                    const uint8_t* raw = ring + s * G::kStageBytes + rrow * rs + lc * G::kChunkBytes;
+                    if constexpr (kXM == 0)
+                        chunk_dot<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                    else
+                        chunk_dot_q8x<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                }
                 release_warp_to_async_proxy(__float_as_uint(acc[0]));   // lane 0 refills it
                 ++consumed;
                 if (prod.valid) issue(s);   // refill the stage just read
@@ -632,12 +809,12 @@ gemv_generic_kernel(const uint8_t* __restrict__ W, int64_t M, int64_t K,
 // ---------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------
-template <int kType>
+template <int kType, int kXM = 0>
 int64_t stream_smem_bytes(int n_tok_template, int max_c) {
     using G = Geo<kType>;
     const int stages = n_tok_template <= 3 ? GQ_GEMV_STAGES : GQ_GEMV_STAGES_N4;
     return static_cast<int64_t>(kWarps) * stages * G::kStageBytes +
-           static_cast<int64_t>(n_tok_template) * max_c * G::kXRec +
+           static_cast<int64_t>(n_tok_template) * max_c * xrec_bytes<kType, kXM>() +
            static_cast<int64_t>(kWarps) * kTileRows * n_tok_template * 4 +
            static_cast<int64_t>(kWarps) * stages * 8;
 }
@@ -658,10 +835,10 @@ cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
     return e;
 }
 
-template <int kType, int kNT, int kMaxProbs>
+template <int kType, int kNT, int kMaxProbs, int kXM>
 cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
-    auto kernel = gemv_stream_kernel<kType, kNT, kMaxProbs>;
-    const int64_t smem = stream_smem_bytes<kType>(kNT, P.max_c);
+    auto kernel = gemv_stream_kernel<kType, kNT, kMaxProbs, kXM>;
+    const int64_t smem = stream_smem_bytes<kType, kXM>(kNT, P.max_c);
     if (smem > info->max_smem_optin) return cudaErrorInvalidValue;   // see stream_eligible
     cudaError_t e = ensure_smem(kernel, info->device, smem);
     if (e != cudaSuccess) return e;
@@ -672,17 +849,17 @@ cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cu
     return cudaGetLastError();
 }
 
-template <int kType, int kMaxProbs>
+template <int kType, int kMaxProbs, int kXM>
 cudaError_t launch_stream_nt(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
     switch (P.n_tok) {
-        case 1: return launch_stream_t<kType, 1, kMaxProbs>(P, info, s);
-        case 2: return launch_stream_t<kType, 2, kMaxProbs>(P, info, s);
-        case 3: return launch_stream_t<kType, 3, kMaxProbs>(P, info, s);
-        default: return launch_stream_t<kType, 4, kMaxProbs>(P, info, s);
+        case 1: return launch_stream_t<kType, 1, kMaxProbs, kXM>(P, info, s);
+        case 2: return launch_stream_t<kType, 2, kMaxProbs, kXM>(P, info, s);
+        case 3: return launch_stream_t<kType, 3, kMaxProbs, kXM>(P, info, s);
+        default: return launch_stream_t<kType, 4, kMaxProbs, kXM>(P, info, s);
     }
 }
 
-template <int kMaxProbs>
+template <int kMaxProbs, int kXM = 0>
 cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t tok0,
                           int n_tok, const DeviceInfo* info, cudaStream_t s) {
     GemvParams<kMaxProbs> P{};
@@ -712,8 +889,8 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
     P.total_bytes = bytes;
     P.total_cost = cost;
     P.max_c = max_c;
-    if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs>(P, info, s);
-    return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs>(P, info, s);
+    if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs, kXM>(P, info, s);
+    return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs, kXM>(P, info, s);
 }
 
 cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_tok,
@@ -737,10 +914,11 @@ bool stream_shape_ok(const MatProblem& p) {
 }
 
 // Whether the shared-memory plan for `n_tok` tokens of this problem fits the device.
+template <int kXM = 0>
 bool stream_fits(gq_type t, const MatProblem& p, int n_tok, const DeviceInfo* info) {
     const int c = static_cast<int>(p.K / (t == GQ_TYPE_Q4_0 ? 256 : 128));
-    const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0>(n_tok, c)
-                                           : stream_smem_bytes<GQ_TYPE_Q8_0>(n_tok, c);
+    const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0, kXM>(n_tok, c)
+                                           : stream_smem_bytes<GQ_TYPE_Q8_0, kXM>(n_tok, c);
     return smem <= info->max_smem_optin;
 }
 
@@ -782,6 +960,36 @@ cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_
             e = launch_stream<16>(t, fast, n_fast, tok0, n_tok, info, s);
         else
             e = launch_stream<GQ_MAX_BATCH>(t, fast, n_fast, tok0, n_tok, info, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+bool q8x_eligible(gq_type t, const MatProblem& p) {
+    DeviceInfo* info = nullptr;
+    if (current_device_info(&info) != cudaSuccess) return false;
+    return stream_shape_ok(p) && stream_fits<1>(t, p, 1, info);
+}
+
+cudaError_t launch_mul_mat_q8x(gq_type t, const MatProblem* probs, int count, int64_t N,
+                               cudaStream_t s) {
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    int64_t step = 0;
+    for (int64_t tok0 = 0; tok0 < N; tok0 += step) {
+        // As many tokens per pass (<= kMaxTokQ8x) as every problem's records allow.
+        int n_tok = static_cast<int>(std::min<int64_t>(kMaxTokQ8x, N - tok0));
+        for (; n_tok > 1; --n_tok) {
+            bool all_fit = true;
+            for (int i = 0; i < count && all_fit; ++i) all_fit = stream_fits<1>(t, probs[i], n_tok, info);
+            if (all_fit) break;
+        }
+        step = n_tok;
+        if (count == 1)
+            e = launch_stream<1, 1>(t, probs, count, tok0, n_tok, info, s);
+        else
+            e = launch_stream<GQ_MAX_BATCH, 1>(t, probs, count, tok0, n_tok, info, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -44,6 +44,14 @@ cudaError_t launch_dequantize(gq_type t, const uint8_t* blocks, int64_t n_elems,
 cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_t N,
                            cudaStream_t s);
 
+// Quantized-activation mul_mat (X quantized per 32-block like Q8_0, integer block sums):
+// the streaming decode kernel with Q8_0 activation records, up to 4 tokens per pass over
+// the weights. Needs K % 256 == 0, 16-byte aligned W and X, and records that fit shared
+// memory (q8x_eligible).
+bool q8x_eligible(gq_type t, const MatProblem& p);
+cudaError_t launch_mul_mat_q8x(gq_type t, const MatProblem* probs, int count, int64_t N,
+                               cudaStream_t s);
+
 // Prefill path: tcgen05 tensor-core GEMM. Its workspace (256-byte aligned) is the bf16
 // copy of X: gemm_x_bytes(K, N) == gemm_workspace_bytes(K, N) bytes.
 constexpr int64_t kGemmMinTokens = 65;

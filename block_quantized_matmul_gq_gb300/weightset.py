@@ -83,3 +83,8 @@ class QuantizedWeightSet:
                 binding.mul_mat_batched(arr, self.btype, N, stream=stream)
             else:
                 binding.mul_mat_batched_ws(arr, self.btype, N, workspace, stream=stream)
+
+    def run_q8x(self, arrays, N: int, stream=None) -> None:
+        """The same products with X quantized per 32-block like Q8_0 (gq_mul_mat_q8x)."""
+        for arr in arrays:
+            binding.mul_mat_q8x_batched(arr, self.btype, N, stream=stream)

@@ -206,6 +206,32 @@ gq_status gq_mul_mat_batched_ws(const gq_mul_mat_problem* problems, int32_t coun
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * Quantized-activation mul_mat ("A Complete Guide to llama.cpp and Customization with
+ * C++", section 2.2: with x quantized like the weights, x_i ~= Delta_x q_x,i, a block's
+ * dot product is Delta Delta_x sum_i q_i q_x,i and the sum is a pure integer operation):
+ *   - every 32-element block of each X row is quantized exactly like a Q8_0 weight block
+ *     (Delta = max |x| / 127, q_x = round(x / Delta) with halves away from zero, clamped to
+ *     [-127, 127]; Delta_x is the fp16 value of Delta, held as fp32);
+ *   - Y[n][m] = sum over blocks b of Delta_w[m][b] * Delta_x[n][b] * S_b, S_b = the exact
+ *     integer sum of q_i * q_x,i (q_i = c - 8 for Q4_0, c for Q8_0), accumulated in fp32.
+ * The result differs from gq_mul_mat by the quantization of X (an approximation the caller
+ * opts into); against the definition above it is exact up to fp32 accumulation.
+ * Same argument contract as gq_mul_mat, plus: K a multiple of 256 and X 16-byte aligned
+ * (else GQ_ERR_SHAPE / GQ_ERR_ALIGN; GQ_ERR_SHAPE also when K is too large for the
+ * activation records in shared memory). Any N: up to 4 tokens per pass over the weights.
+ * Allocates nothing.
+ */
+gq_status gq_mul_mat_q8x(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                         const float* X, int64_t N, float* Y, void* stream);
+
+/*
+ * gq_mul_mat_q8x over up to GQ_MAX_BATCH independent problems (same type and N) in one
+ * launch per pass. Every problem is checked before anything is queued.
+ */
+gq_status gq_mul_mat_q8x_batched(const gq_mul_mat_problem* problems, int32_t count,
+                                 gq_type t, int64_t N, void* stream);
+
+/*
  * Device-side status of the current device: synchronizes `stream`, then returns and
  * clears the status word (GQ_OK, or GQ_ERR_TIMEOUT if a kernel gave up waiting), or
  * GQ_ERR_CUDA if the stream itself reports an error.

@@ -108,3 +108,20 @@ def test_binding_refuses_cpu_tensors(gq_lib):
 def test_selftest_limit_checked_on_host(gq_lib):
     assert gq_lib.lib.gq_selftest_wait_timeout(0, None) == -2
     assert gq_lib.lib.gq_selftest_wait_timeout(20_000_000, None) == -2
+
+
+def test_mul_mat_q8x_argument_checks(gq_lib):
+    f = gq_lib.lib.gq_mul_mat_q8x
+    assert f(A16, 7, 4, 256, A16, 1, A16, None) == -3              # unknown type
+    assert f(A16, 2, 4, 96, A16, 1, A16, None) == -2               # K % 256 (needs whole chunks)
+    assert f(A16, 2, 4, 48, A16, 1, A16, None) == -2               # K % 32
+    assert f(A16, 2, 4, 256, A4, 1, A16, None) == -4               # X not 16-byte aligned
+    assert f(A4, 2, 4, 256, A16, 1, A16, None) == -4               # W not 16-byte aligned
+    assert f(None, 2, 4, 256, A16, 1, A16, None) == -1             # NULL W
+    assert f(A16, 2, 0, 256, A16, 1, A16, None) == 0               # empty: nothing to do
+    fb = gq_lib.lib.gq_mul_mat_q8x_batched
+    assert fb(None, 0, 2, 1, None) == 0
+    assert fb(None, 1, 2, 1, None) == -1
+    assert fb(None, 300, 2, 1, None) == -2
+    arr = gq_lib.make_problems([])
+    assert fb(arr, 1, 7, 1, None) == -3

@@ -426,3 +426,84 @@ def test_batched_ws_records_into_a_graph(gq_lib, cuda_dev, N):
     with pytest.raises(gq_lib.GQError):
         gq_lib.mul_mat_batched_ws(arr, "q4_0", N, None)
     assert gq_lib.get_last_error() == 0
+
+
+# ------------------------------------------------------------------------------------
+# Quantized activations (gq_mul_mat_q8x): X quantized per 32-block like Q8_0, integer
+# block sums ("A Complete Guide to llama.cpp ...", section 2.2)
+# ------------------------------------------------------------------------------------
+Q8X = [(7, 256, 1), (300, 2048, 3), (129, 5632, 8), (64, 11008, 5), (1000, 2048, 16),
+       (33, 4096, 9), (257, 1024, 2)]
+
+
+def _q8x_bound(oracle_mod, t, q, M, K, X):
+    """Worst-case fp32 accumulation bound of the block sums: (blocks + 8) * 2^-24 times
+    sum |What| |Xhat| (Xhat the Q8_0-dequantized X), per element."""
+    wa = np.abs(oracle_mod.dequantize(t, q, M, K).astype(np.float64))
+    N = X.shape[0]
+    xa = np.abs(oracle_mod.dequantize("q8_0", oracle_mod.quantize("q8_0", X), N, K)
+                .astype(np.float64))
+    return (K // 32 + 8) * 2.0 ** -24 * (xa @ wa.T) + 1e-30
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", Q8X)
+def test_q8x_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    W = _np_weights(M, K, seed=M + 3 * K)
+    q = oracle_mod.quantize(t, W)
+    X = workloads.activations(N, K, seed=N + 5 * K).numpy()
+    Y = gq_lib.mul_mat_q8x(torch.from_numpy(q).to(cuda_dev), t, M, K,
+                           torch.from_numpy(X).to(cuda_dev)).cpu().numpy()
+    Y_ref = oracle_mod.mul_mat_q8x(t, q, M, K, X)
+    err = np.abs(Y.astype(np.float64) - Y_ref.astype(np.float64))
+    assert np.all(err <= _q8x_bound(oracle_mod, t, q, M, K, X)), f"q8x {t} M={M} K={K} N={N}"
+    assert gq_lib.get_last_error() == 0
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_q8x_accuracy_against_exact_product(gq_lib, oracle_mod, cuda_dev, t):
+    """Quantizing X moves the result by far less than the mul_mat tolerance on the
+    seeded N(0, 1) activations (the method's own error, measured)."""
+    M, K, N = 512, 2048, 4
+    W = _np_weights(M, K, seed=91)
+    q = oracle_mod.quantize(t, W)
+    X = workloads.activations(N, K, seed=92).numpy()
+    Y = gq_lib.mul_mat_q8x(torch.from_numpy(q).to(cuda_dev), t, M, K,
+                           torch.from_numpy(X).to(cuda_dev)).cpu().numpy()
+    check_tolerance(Y, oracle_mod.mul_mat(t, q, M, K, X), oracle_mod.dequantize(t, q, M, K), X,
+                    f"q8x vs exact {t}")
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_q8x_batched_matches_oracle(gq_lib, oracle_mod, cuda_dev, t):
+    shapes = [(256, 2048), (1000, 5632), (33, 256), (2048, 11008)]
+    N = 6
+    items, refs = [], []
+    for i, (M, K) in enumerate(shapes):
+        q = oracle_mod.quantize(t, _np_weights(M, K, seed=200 + i))
+        X = workloads.activations(N, K, seed=300 + i).numpy()
+        items.append((torch.from_numpy(q).to(cuda_dev), M, K, torch.from_numpy(X).to(cuda_dev),
+                      torch.full((N, M), float("nan"), device=cuda_dev)))
+        refs.append((q, X))
+    gq_lib.mul_mat_q8x_batched(items, t, N)
+    torch.cuda.synchronize()
+    for (qd, M, K, Xd, Y), (q, X) in zip(items, refs):
+        rows = np.arange(M) if M <= 1000 else np.array([0, 1, 127, 128, 1000, M - 1])
+        Y_ref = oracle_mod.mul_mat_q8x_rows(t, q, M, K, X, rows)
+        got = Y.cpu().numpy()[:, rows].astype(np.float64)
+        bound = _q8x_bound(oracle_mod, t, q.reshape(M, -1)[rows].copy(), len(rows), K, X)
+        assert np.all(np.abs(got - Y_ref) <= bound), f"batched q8x {t} M={M} K={K}"
+    assert gq_lib.get_last_error() == 0
+
+
+def test_q8x_rejects_unsupported_shapes(gq_lib, cuda_dev):
+    q = torch.zeros((4, 96 // 32 * 18), dtype=torch.uint8, device=cuda_dev)
+    X = torch.zeros((1, 96), device=cuda_dev)
+    with pytest.raises(gq_lib.GQError) as e:
+        gq_lib.mul_mat_q8x(q, "q4_0", 4, 96, X)
+    assert e.value.status == -2
+    q = torch.zeros((4, 256 // 32 * 18), dtype=torch.uint8, device=cuda_dev)
+    Xb = torch.zeros(257 * 2, device=cuda_dev)
+    with pytest.raises(gq_lib.GQError) as e:
+        gq_lib.mul_mat_q8x(q, "q4_0", 4, 256, Xb[1:257].view(1, 256))
+    assert e.value.status == -4
