@@ -21,6 +21,10 @@
 //               reads. After the K loop the same warps read the accumulator out of TMEM
 //               (tcgen05.ld; warp w owns lanes 32*(w%4).., half the token columns) and
 //               write Y.
+// With fewer tiles than half the SMs, a tile is shared by a cluster of 2 or 4 CTAs along
+// grid z, each taking a contiguous share of K; each parks its fp32 partial in its own
+// shared memory and, after a cluster barrier, sums a quarter (or half) of the tile's token
+// columns over the cluster through distributed shared memory, in rank order, into Y.
 // X is converted to bf16 once per call by x_to_bf16_kernel into caller- or library-owned
 // workspace (N x K bf16), which the tensor map reads.
 // All waits are bounded; a CTA that gives up sets the device status word, lets its own
@@ -31,6 +35,7 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "gq_dequant.cuh"
@@ -71,9 +76,11 @@ struct Layout {
     static constexpr int kAlloc = kBytes + 1024;   // room to align the base to 1024
     static constexpr int kTmemCols = kBN < 32 ? 32 : kBN;
     static_assert(kB % 1024 == 0 && kA % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned stages");
+    // A split-K CTA parks its fp32 partial tile in the operand stages.
+    static_assert(kBM * kBN * 4 <= kOffRaw, "partial tile fits the operand stages");
 };
 
-template <int kType, int kBN>
+template <int kType, int kBN, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
             int M, int N, int K, float* __restrict__ Y, unsigned* status) {
@@ -102,8 +109,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
     const int m0 = blockIdx.x * kBM;
     const int n0 = blockIdx.y * kBN;
-    const int nk = K / kBK;
-    const int nsuper = K / kSuperK;
+    // Split K: the gridDim.z CTAs of a cluster share the tile, CTA z taking super-steps
+    // [j0, j0 + nsuper) of the whole K (every CTA gets at least one).
+    const int nsuper_all = K / kSuperK;
+    const int j0 = kSplit ? nsuper_all * static_cast<int>(blockIdx.z) / static_cast<int>(gridDim.z) : 0;
+    const int nsuper =
+        kSplit ? nsuper_all * static_cast<int>(blockIdx.z + 1) / static_cast<int>(gridDim.z) - j0
+               : nsuper_all;
+    const int nk = kSplit ? nsuper * (kSuperK / kBK) : K / kBK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -145,7 +158,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     }
                     mbar_arrive_expect_tx(raw_full(r), L::kRaw);
                     tma_load_2d(sRaw + r * L::kRaw, &tmap_w,
-                                j * (RawFmt<kType>::kRow / RawFmt<kType>::kElem), m0, raw_full(r));
+                                (j0 + j) * (RawFmt<kType>::kRow / RawFmt<kType>::kElem), m0,
+                                raw_full(r));
                     ++raw_issued;
                 }
                 if (!ok) break;
@@ -155,7 +169,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     break;
                 }
                 mbar_arrive_expect_tx(b_full(s), L::kB);
-                tma_load_2d(sB + s * L::kB, &tmap_x, ks * kBK, n0, b_full(s));
+                tma_load_2d(sB + s * L::kB, &tmap_x, (j0 * (kSuperK / kBK) + ks) * kBK, n0, b_full(s));
                 ++b_issued;
             }
             if (!ok) report_status(status, kStatusTimeout);
@@ -249,7 +263,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         // Epilogue: accumulator rows are TMEM lanes, token columns are TMEM columns.
         const bool done = mbar_wait(acc_full, 0);
         tc_fence_after();
-        if (done && ok) {
+        if constexpr (kSplit) {
+            if (!done) report_status(status, kStatusTimeout);
+            // Split K: this CTA's partial tile goes to its own shared memory, the operand
+            // stages being free once every MMA has completed: part[column][row] fp32.
+            float* part = reinterpret_cast<float*>(base + L::kOffA);
+            if (done) {
+                const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+                const int c_begin = half * (kBN / 2);
+                for (int c = c_begin; c < c_begin + kBN / 2; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c, v);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) part[(c + jj) * kBM + row] = __uint_as_float(v[jj]);
+                }
+            }
+        } else if (done && ok) {
             const int m = m0 + row;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             const int c_begin = half * (kBN / 2);
@@ -268,6 +297,47 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         } else if (!done) {
             report_status(status, kStatusTimeout);
         }
+    }
+    if constexpr (kSplit) {
+        // Every CTA of the cluster has its partial in shared memory. CTA r then sums token
+        // columns [r C / Z, (r + 1) C / Z) over the cluster's CTAs in rank order (the same
+        // order whoever finishes first) and writes them to Y; a second barrier keeps every
+        // CTA's shared memory alive until all reads of it are done. All threads take part
+        // in both barriers; the CTAs of a cluster are co-scheduled, so neither waits on
+        // work that cannot run.
+        __syncwarp();
+        cluster_sync();
+        if (warp >= 2) {
+            const int Z = static_cast<int>(gridDim.z);
+            const int rank = static_cast<int>(cluster_ctarank());
+            const int c_lo = kBN * rank / Z, c_hi = kBN * (rank + 1) / Z;
+            const uint32_t part = smem_addr(base + L::kOffA);
+            const int t = threadIdx.x - 64;                      // 0..255
+            const bool vec = (M % 4 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
+            for (int idx = t; idx < (c_hi - c_lo) * (kBM / 4); idx += 32 * kDequantWarps) {
+                const int c = c_lo + idx / (kBM / 4);
+                const int r4 = 4 * (idx % (kBM / 4));
+                const uint32_t off = static_cast<uint32_t>((c * kBM + r4) * 4);
+                float4 acc = ld_shared_cluster_f4(map_shared_rank(part + off, 0));
+                for (int z = 1; z < Z; ++z) {
+                    const float4 v = ld_shared_cluster_f4(map_shared_rank(part + off, z));
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                const int n = n0 + c, m = m0 + r4;
+                if (n >= N || m >= M) continue;
+                float* y = Y + static_cast<int64_t>(n) * M + m;
+                if (vec) {
+                    *reinterpret_cast<float4*>(y) = acc;
+                } else {
+                    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+                    for (int i = 0; i < 4 && m + i < M; ++i) y[i] = a[i];
+                }
+            }
+        }
+        cluster_sync();
     }
     tc_fence_before();
     __syncthreads();
@@ -332,6 +402,48 @@ cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
     return e;
 }
 
+// Split-K ways for a GEMM of `tiles` output tiles and `nsuper` 256-k super-steps. With
+// fewer tiles than half the SMs, each tile is shared by a cluster of Z CTAs (Z = 2 or 4)
+// that split K and sum their partials through distributed shared memory; Z is the largest
+// that keeps every cluster resident at once (cudaOccupancyMaxActiveClusters, cached).
+template <typename KernelT>
+int split_k_ways(KernelT kernel, int smem_bytes, const DeviceInfo* info, int64_t tiles,
+                 int64_t nsuper) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, int>, int> max_clusters;
+    for (int Z = 4; Z >= 2; Z /= 2) {
+        if (tiles * Z > info->sm_count || nsuper < Z) continue;
+        int active = 0;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            const auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), info->device, Z);
+            auto it = max_clusters.find(key);
+            if (it != max_clusters.end()) {
+                active = it->second;
+            } else {
+                cudaLaunchConfig_t cfg{};
+                cfg.gridDim = dim3(1, 1, static_cast<unsigned>(Z));
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 1;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = static_cast<unsigned>(Z);
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    active = 0;
+                }
+                max_clusters[key] = active;
+            }
+        }
+        if (tiles <= active) return Z;
+    }
+    return 1;
+}
+
 template <int kType, int kBN>
 cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* xb,
                           const DeviceInfo* info, cudaStream_t s) {
@@ -365,14 +477,36 @@ cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* x
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    auto kernel = gemm_kernel<kType, kBN>;
+    auto kernel = gemm_kernel<kType, kBN, false>;
+    auto split_kernel = gemm_kernel<kType, kBN, true>;
     cudaError_t e = ensure_smem(kernel, info->device, L::kAlloc);
+    if (e == cudaSuccess) e = ensure_smem(split_kernel, info->device, L::kAlloc);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>((p.M + kBM - 1) / kBM),
-                    static_cast<unsigned>((N + kBN - 1) / kBN));
-    kernel<<<grid, kThreads, L::kAlloc, s>>>(tw, tx, static_cast<int>(p.M), static_cast<int>(N),
-                                             static_cast<int>(p.K), p.Y, info->status);
-    return cudaGetLastError();
+    const int64_t mt = (p.M + kBM - 1) / kBM, nt = (N + kBN - 1) / kBN;
+    const int Z = split_k_ways(split_kernel, L::kAlloc, info, mt * nt, p.K / kSuperK);
+    if (Z == 1) {
+        kernel<<<dim3(static_cast<unsigned>(mt), static_cast<unsigned>(nt)), kThreads, L::kAlloc, s>>>(
+            tw, tx, static_cast<int>(p.M), static_cast<int>(N), static_cast<int>(p.K), p.Y,
+            info->status);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(mt), static_cast<unsigned>(nt), static_cast<unsigned>(Z));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(Z);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int M = static_cast<int>(p.M), n = static_cast<int>(N), K = static_cast<int>(p.K);
+    float* Y = p.Y;
+    unsigned* status = info->status;
+    void* args[] = {&tw, &tx, &M, &n, &K, &Y, &status};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(split_kernel), args);
 }
 
 }  // namespace

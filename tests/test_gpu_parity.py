@@ -267,8 +267,12 @@ def test_llama7b_shapes_full_size(gq_lib, oracle_mod, cuda_dev, N):
 # ------------------------------------------------------------------------------------
 # Tensor-core paths (N >= 3, K % 256 == 0): bf16 operands, fp32 accumulation
 # ------------------------------------------------------------------------------------
+# Few-tile shapes also run the cluster split-K form: (300, 512, 100) and (129, 768, 300) split
+# K two ways (the latter unevenly, ragged M), (1000, 2048, 257), (520, 1792, 130) and
+# (1001, 1280, 70) four ways (7 and 5 super-steps: uneven shares; M % 4 != 0 in the last);
+# (128, 256, 65) has one super-step and does not split.
 GEMM = [(128, 256, 64), (7, 256, 64), (300, 512, 100), (129, 768, 300), (1000, 2048, 257),
-        (256, 5632, 64)]
+        (256, 5632, 64), (128, 256, 65), (520, 1792, 130), (1001, 1280, 70)]
 
 
 @pytest.mark.parametrize("t", ["q4_0", "q8_0"])
