@@ -16,6 +16,16 @@ constexpr unsigned kStatusTimeout = 1u;
 // records kStatusTimeout and leaves. Legitimate waits last microseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
+// Programmatic dependent launch. launch_dependents lets the next kernel of the stream
+// (launched with the programmatic-serialization attribute) be scheduled once every CTA
+// of this grid has executed it; its CTAs then take SMs as this grid's CTAs leave.
+// griddep_wait blocks until every prerequisite grid has completed and its memory
+// operations are visible. Both are no-ops in a grid launched without the attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -630,6 +630,8 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
         fence_mbar_init();
     }
     __syncwarp();
+    // The next mul_mat of the stream may start on SMs this grid leaves and fill its rings.
+    griddep_launch_dependents();
 
     // This CTA's rows: from the first row starting at or after byte c*T/G to the first
     // row starting at or after byte (c+1)*T/G.
@@ -669,6 +671,9 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
         ++issued;
     };
     for (int s = 0; s < S && prod.valid; ++s) issue(s);
+    // Only the weights, which no kernel of the call sequence writes, are read above; X and
+    // Y may belong to the previous kernel of the stream, so everything after waits for it.
+    griddep_wait();
 
     // Consumer side: all warps walk the CTA's segments together (x16 is per problem);
     // inside a segment each warp works through its own tiles.
@@ -845,8 +850,21 @@ cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cu
     // Enough CTAs that each streams at least ~32 KB, at most one per SM.
     int64_t grid = (P.total_bytes + 32767) / 32768;
     grid = std::max<int64_t>(1, std::min<int64_t>(grid, info->sm_count));
-    kernel<<<static_cast<int>(grid), kThreads, static_cast<size_t>(smem), s>>>(P);
-    return cudaGetLastError();
+    // Programmatic dependent launch: this grid's CTAs may start filling their weight rings
+    // while the previous kernel of the stream finishes (the kernel waits for it before it
+    // touches X or Y).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&P};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
 }
 
 template <int kType, int kMaxProbs, int kXM>

@@ -164,6 +164,40 @@ def test_mul_mat_deterministic(gq_lib, cuda_dev):
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
 
 
+@pytest.mark.parametrize("N", [1, 2])
+def test_back_to_back_calls_see_previous_results(gq_lib, cuda_dev, N):
+    """Decode calls launched back to back on one stream, each call's X being the previous
+    call's Y (read after write) and each call's Y overwriting the X of the call before
+    (write after read), give bitwise the results of the same chain with a synchronize after
+    every call. A call may start streaming its weights while the previous one finishes;
+    this pins that it touches X and Y only after that call is complete."""
+    D = 2048
+    qs = [gq_lib.quantize(workloads.weights(D, D, 40 + i, device=cuda_dev), "q4_0")
+          for i in range(4)]
+    x0 = workloads.activations(N, D, 50, device=cuda_dev)
+
+    def chain(sync):
+        bufs = [x0.clone(), torch.empty_like(x0)]   # ping-pong: call i + 1 writes what call i read
+        for i in range(24):
+            src, dst = bufs[i % 2], bufs[(i + 1) % 2]
+            gq_lib.mul_mat(qs[i % 4], "q4_0", D, D, src, out=dst)
+            # keep the values in range: scale by a power of two with a separate kernel
+            # every few calls (exact, and a different kernel between two mul_mats)
+            if i % 6 == 5:
+                dst.mul_(2.0 ** -4)
+            if sync:
+                torch.cuda.synchronize(cuda_dev)
+        torch.cuda.synchronize(cuda_dev)
+        return bufs[24 % 2]
+
+    ref = chain(True)
+    assert torch.isfinite(ref).all()
+    for _ in range(3):
+        out = chain(False)
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+    assert gq_lib.get_last_error() == 0
+
+
 def test_mul_mat_misaligned_x(gq_lib, oracle_mod, cuda_dev):
     """X 4-byte but not 16-byte aligned: correct through the generic kernel."""
     M, K = 40, 2048
