@@ -311,6 +311,8 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The next kernel of the stream may take SMs as this grid's CTAs leave.
+    griddep_launch_dependents();
 
     TcWalk w;
     tc_walk_open(P, w, P.total_units * blockIdx.x / gridDim.x,
@@ -318,20 +320,38 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
 
     if (warp == 0) {
         // ---------------- producer (whole warp; lane 0 arms the barriers) ----------------
+        // The weights of the first R super-steps go out before the previous kernel of the
+        // stream has completed (they are read-only during the call; the dequantize warps
+        // may already work on them); the X tiles, written by that kernel, after it.
+        int n_pre = 0;
+        {
+            TcWalk pre = w;
+            for (; pre.valid && n_pre < R; tc_walk_next(P, pre), ++n_pre) {
+                if (lane == 0) {
+                    const uint32_t dst = sRaw + n_pre * L::kStage;
+                    mbar_arrive_expect_tx(raw_full(n_pre), L::kStage);   // raw + X bytes
+                    // Whole 128-row box; rows past the matrix end are filled with zeros.
+                    tma_load_2d(dst, &P.maps[pre.p], pre.j * (L::kRawRow / RawFmt<kType>::kElem),
+                                static_cast<int>(pre.row0), raw_full(n_pre));
+                }
+            }
+        }
+        griddep_wait();
         int raw_n = 0;
         bool ok = true;
         for (; w.valid; tc_walk_next(P, w), ++raw_n) {
             const int r = raw_n % R;
-            if (!mbar_wait(raw_empty(r), ((raw_n / R) & 1) ^ 1)) {
+            if (raw_n >= n_pre && !mbar_wait(raw_empty(r), ((raw_n / R) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
                 const uint32_t dst = sRaw + r * L::kStage;
-                mbar_arrive_expect_tx(raw_full(r), L::kStage);
-                // Whole 128-row box; rows past the matrix end are filled with zeros.
-                tma_load_2d(dst, &P.maps[w.p], w.j * (L::kRawRow / RawFmt<kType>::kElem),
-                            static_cast<int>(w.row0), raw_full(r));
+                if (raw_n >= n_pre) {
+                    mbar_arrive_expect_tx(raw_full(r), L::kStage);
+                    tma_load_2d(dst, &P.maps[w.p], w.j * (L::kRawRow / RawFmt<kType>::kElem),
+                                static_cast<int>(w.row0), raw_full(r));
+                }
                 bulk_g2s(dst + L::kRaw, P.p[w.p].Xt + static_cast<int64_t>(w.j) * 4 * L::kB,
                          4 * L::kB, raw_full(r));
             }
@@ -350,6 +370,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
         // a tile are added in a fixed order by the same warps afterwards, each warp for
         // the TMEM lane quadrant it may access (warp % 4); with two sets this epilogue
         // runs after the next tile's first MMAs have been queued.
+        griddep_wait();   // X tiles, Y, partial sums and counters of the previous kernel
         const int q = warp - 1;
         const int g = q >> 1;                      // dequantize group that fills quarter q
         const int quad = warp & 3;
@@ -578,6 +599,10 @@ struct XtParams {
 template <int kNPad>
 __global__ void __launch_bounds__(256)
 x_tiles_kernel(const __grid_constant__ XtParams P) {
+    // The tensor-core kernel after this one may start filling its weight rings already;
+    // the tiles and counters may still be in use by the previous kernel of the stream.
+    griddep_launch_dependents();
+    griddep_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < P.n_counters; i += blockDim.x) P.counters[i] = 0;
     int lo = 0, hi = P.count - 1;   // the problem of this block: last block_begin <= block
@@ -621,6 +646,24 @@ x_tiles_kernel(const __grid_constant__ XtParams P) {
         *reinterpret_cast<uint4*>(pr.Xt + ks * (kNPad * 128) + n * 128 + ((c ^ (n & 7)) << 4)) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
+}
+
+// A launch with the programmatic-stream-serialization attribute: the kernel may be
+// scheduled before the previous kernel of the stream has completed, and orders itself
+// after it with griddepcontrol.wait.
+cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       void** args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
 template <typename KernelT>
@@ -718,8 +761,9 @@ cudaError_t launch_x_tiles(const MatProblem* probs, int count, int64_t N, uint8_
         blocks += (probs[i].K / kBK * kNPad * 8 + kXtChunksPerBlock - 1) / kXtChunksPerBlock;
         off += static_cast<int64_t>(kNPad) * probs[i].K * 2;
     }
-    x_tiles_kernel<kNPad><<<static_cast<unsigned>(blocks), 256, 0, s>>>(P);
-    return cudaGetLastError();
+    void* args[] = {&P};
+    return launch_pdl(reinterpret_cast<const void*>(x_tiles_kernel<kNPad>),
+                      dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, args);
 }
 
 template <int kType, int kNPad, int kMaxProbs>
@@ -756,8 +800,9 @@ cudaError_t launch_tc_t(const MatProblem* probs, int count, int64_t N, uint8_t* 
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(
         std::max<int64_t>(1, std::min<int64_t>({units, info->sm_count, kMaxTcGrid})));
-    kernel<<<grid, kThreads, L::kAlloc, s>>>(P);
-    return cudaGetLastError();
+    void* args[] = {&P};
+    return launch_pdl(reinterpret_cast<const void*>(kernel), dim3(static_cast<unsigned>(grid)),
+                      dim3(kThreads), static_cast<size_t>(L::kAlloc), s, args);
 }
 
 template <int kType, int kMaxProbs>

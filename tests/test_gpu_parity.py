@@ -164,13 +164,15 @@ def test_mul_mat_deterministic(gq_lib, cuda_dev):
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
 
 
-@pytest.mark.parametrize("N", [1, 2])
+@pytest.mark.parametrize("N", [1, 2, 8, 40])
 def test_back_to_back_calls_see_previous_results(gq_lib, cuda_dev, N):
     """Decode calls launched back to back on one stream, each call's X being the previous
     call's Y (read after write) and each call's Y overwriting the X of the call before
     (write after read), give bitwise the results of the same chain with a synchronize after
     every call. A call may start streaming its weights while the previous one finishes;
-    this pins that it touches X and Y only after that call is complete."""
+    this pins that it touches X, Y and its workspace (N = 8, 40: the tensor-core path's X
+    tiles, partial sums and counters, reused by every call) only after that call is
+    complete."""
     D = 2048
     qs = [gq_lib.quantize(workloads.weights(D, D, 40 + i, device=cuda_dev), "q4_0")
           for i in range(4)]
