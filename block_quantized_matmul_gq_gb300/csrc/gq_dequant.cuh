@@ -118,6 +118,30 @@ __device__ __forceinline__ void dequant_block_at(const uint32_t* r, uint32_t (&o
     }
 }
 
+// Codes only: the 32 exact integers c - 8 of the Q4_0 block that starts at byte kOff of r,
+// as bf16 pairs in the order of dequant_block_at (out[i] = elements 2i, 2i + 1). The
+// block's scale is applied to the product afterwards, in fp32.
+template <int kOff>
+__device__ __forceinline__ void q4_codes_at(const uint32_t* r, uint32_t (&out)[16]) {
+    static_assert(kOff % 2 == 0, "blocks start on 2-byte boundaries");
+    const __nv_bfloat162 off = __float2bfloat162_rn(136.0f);
+    auto pair = [&](uint32_t bytes4, uint32_t sel) {
+        const uint32_t v = __byte_perm(bytes4, 0x43434343u, sel);   // (128 + c, 128 + c')
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+        return *reinterpret_cast<const uint32_t*>(&q);
+    };
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w = word_at(r, kOff + 2 + 4 * i);
+        const uint32_t lo = w & 0x0F0F0F0Fu;
+        const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+        out[2 * i] = pair(lo, 0x4140u);
+        out[2 * i + 1] = pair(lo, 0x4342u);
+        out[8 + 2 * i] = pair(hi, 0x4140u);
+        out[8 + 2 * i + 1] = pair(hi, 0x4342u);
+    }
+}
+
 // Block `blk` (0..7) of a row's super-step, raw bytes in r from the super-step's start.
 template <int kType, int blk>
 __device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)[16]) {

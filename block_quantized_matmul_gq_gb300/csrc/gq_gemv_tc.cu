@@ -19,10 +19,18 @@
 //                The ring of raw stages is as deep as shared memory allows, because the
 //                weight bytes in flight per SM decide the bandwidth; a stage is free again
 //                once the dequantize warps have read its rows and the MMAs have read its X.
-//   warp 1       TMEM owner and MMA issuer (one thread); two accumulators of kNPad columns
-//                so a tile's epilogue overlaps the next tile's stream.
-//   warps 2..9   dequantize rows to 128-byte-swizzled bf16 (shared with the prefill GEMM).
-//   warps 10..13 epilogue: TMEM -> registers -> Y (one TMEM lane quadrant each).
+//   warps 1..4   MMA issuers, one per SM sub-partition: issuer q owns the 64-k quarter q
+//                of every super-step (a single issuing thread cannot keep the tensor core
+//                busy with N <= 64 MMAs), its own accumulator per set, and afterwards the
+//                tile epilogue for its TMEM lane quadrant (the four accumulators added in
+//                a fixed order).
+//   warps 5..12  dequantize, two groups of four (one per 128-k half of every super-step),
+//                one row per thread, written to the group's A slot in TMEM (tcgen05.st).
+// Scaled form (Q4_0, up to 16 tokens): the A slots hold the exact codes c - 8, each 32-k
+// block's MMAs write the block's own accumulator, and the dequantize warps add
+// d_blk * acc_blk to a per-row fp32 sum one super-step behind the MMAs; the two groups'
+// halves of a tile meet in shared memory and group 0 writes Y. The weights are never
+// rounded. Other forms dequantize to bf16 ((c - 8) * d or c * d, rounded once).
 // All waits are bounded: a CTA that gives up records a timeout in the status word, lets
 // its copies and MMAs land, frees its TMEM and leaves.
 #include <cuda.h>   // CUtensorMap and its enums (header only; no libcuda link)
@@ -63,8 +71,14 @@ struct TcLayout {
     // TMEM: kAccBufs sets of four accumulators (one per quarter) of kNPad columns, then
     // two groups x kGroupSlots A slots of 64 columns. Two sets let a tile's epilogue
     // overlap the next tile's MMAs; at 64 tokens only one set fits next to the A slots.
+    // Scaled form (Q4_0, up to 16 tokens): A holds the exact codes c - 8 and every 32-k
+    // block has its own accumulator, two buffers of a super-step's eight (256 columns);
+    // the issuer warps apply the block scales in fp32.
+    static constexpr bool kScaled = kType == GQ_TYPE_Q4_0 && kNPad == 16;
     static constexpr int kAccBufs = kNPad <= 32 ? 2 : 1;
-    static constexpr int kAccCols = kAccBufs * kQuarters * kNPad;          // 128 / 256 / 256
+    static constexpr int kUnitCols = (kSuperK / 32) * kNPad;   // scaled: a super-step's blocks
+    static constexpr int kAccCols =
+        kScaled ? 2 * kUnitCols : kAccBufs * kQuarters * kNPad;   // 256 / 256 / 256
     static constexpr int kGroupSlots = (kTmemCols - kAccCols) / (2 * kSlotCols);   // 3 / 2 / 2
     static_assert(kGroupSlots >= 2, "TMEM budget");
     static constexpr int kB = kNPad * kBK * 2;              // one 64-k X tile: 2 / 4 / 8 KB
@@ -72,19 +86,25 @@ struct TcLayout {
     static constexpr int kRaw = kBM * kRawRow;              // 18 / 34 KB of raw blocks
     static constexpr int kStage = kRaw + 4 * kB;            // raw blocks + the super-step's X
     static constexpr int kOffRaw = 0;
-    static constexpr int kFixed = 1024 + 512;               // alignment slack, barriers, slot
+    // Scaled: the two dequantize groups' halves of a tile's y meet in shared memory, two
+    // buffers by tile parity, 128 rows x kNPad (+1 against bank conflicts) fp32.
+    static constexpr int kYStride = kNPad + 1;
+    static constexpr int kYBytes = kScaled ? 2 * kBM * kYStride * 4 : 0;
+    static constexpr int kFixed = 1024 + 512 + kYBytes;     // alignment slack, barriers, slot
     static constexpr int kRawFit = (kSmemLimit - kFixed) / kStage;
     static constexpr int kRawStages = kRawFit > 8 ? 8 : kRawFit;
     static constexpr int kOffBar = kOffRaw + kRawStages * kStage;
     // raw_full[R], raw_empty[R], a_full[2][G], a_empty[2][G], acc_full[B], acc_empty[B],
-    // mma_done
-    static constexpr int kNumBars = 2 * kRawStages + 4 * kGroupSlots + 2 * kAccBufs + 1;
+    // mma_done, and in the scaled form y_full[2], y_free[2]
+    static constexpr int kNumBars =
+        2 * kRawStages + 4 * kGroupSlots + 2 * kAccBufs + 1 + (kScaled ? 4 : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kOffY = kOffMisc + 16;
+    static constexpr int kBytes = kOffY + kYBytes;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kB % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned tiles");
     static_assert(kRawStages >= 2 && kAlloc <= kSmemLimit, "shared memory budget");
-    static_assert(kNumBars * 8 + 16 <= kFixed - 1024, "barrier space");
+    static_assert(kNumBars * 8 + 16 <= kFixed - 1024 - kYBytes, "barrier space");
 };
 
 struct TcProb {
@@ -258,6 +278,262 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// MMA issuer warp of the scaled form (warps 1..4; issuer q owns the 64-k quarter q of
+// every super-step, i.e. blocks 2q and 2q + 1). A holds the exact codes c - 8 and each
+// block's two MMAs (K = 16) write the block's own accumulator, in the super-step's buffer
+// (two buffers by super-step parity): acc_blk = sum over the block of (c - 8) * x. The
+// dequantize warps apply the block scales (tc_dequant_scaled).
+template <int kType, int kNPad, int kMaxProbs>
+__device__ void tc_issue_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_t tmem,
+                                uint32_t sRaw, uint32_t bar0) {
+    using L = TcLayout<kType, kNPad>;
+    static_assert(L::kScaled, "scaled form");
+    constexpr int R = L::kRawStages;
+    constexpr int G = L::kGroupSlots;
+    constexpr int B = L::kAccBufs;
+    auto raw_full = [&](int r) { return bar0 + 8u * r; };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
+    auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
+    auto a_empty = [&](int g, int i) { return bar0 + 8u * (2 * R + 2 * G + g * G + i); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
+    const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int q = warp - 1;
+    const int g = q >> 1;   // dequantize group that fills quarter q
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kNPad);
+    int raw_n = 0;
+    bool ok = true;
+    for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
+        const int b = raw_n & 1;
+        const int r = raw_n % R;
+        const int gi = raw_n % G;
+        if (!warp_wait(acc_empty(b), ((raw_n >> 1) & 1) ^ 1) ||   // buffer b scaled out
+            !warp_wait(raw_full(r), (raw_n / R) & 1) ||            // the super-step's X landed
+            !warp_wait(a_full(g, gi), (raw_n / G) & 1)) {          // quarter q's codes stored
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t sX = sRaw + r * L::kStage + L::kRaw + q * L::kB;
+            const uint32_t a_col =
+                tmem + L::kAccCols + (g * G + gi) * kSlotCols + (q & 1) * (kBK / 2);
+            const uint32_t d0 = tmem + static_cast<uint32_t>(b * L::kUnitCols + 2 * q * kNPad);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)   // blocks 2q (kk 0, 1) and 2q + 1 (kk 2, 3)
+                umma_bf16_tmem_a(d0 + (kk >> 1) * kNPad, a_col + kk * 8,
+                                 sw128_kmajor_desc(sX + kk * 32), idesc,
+                                 static_cast<uint32_t>(kk & 1));
+            umma_commit(a_empty(g, gi));
+            umma_commit(raw_empty(r));
+            umma_commit(acc_full(b));
+        }
+        __syncwarp();
+    }
+    // Completes when every MMA this thread issued has finished (also after a timeout), so
+    // the TMEM release never races an MMA in flight.
+    if (lane == 0) umma_commit(mma_done);
+    if (!ok && lane == 0) report_status(P.status, kStatusTimeout);
+}
+
+// Dequantize warp of the scaled form (warps 5..12; group g takes blocks 4g .. 4g + 3 of
+// every super-step for all 128 rows, one row per thread). Per super-step it stores the
+// codes c - 8 of its half row in the group's A slot, then, one super-step behind the MMAs,
+// adds d_blk * acc_blk of its four blocks to its fp32 y (blocks and super-steps in order).
+// At a tile's end group 1 hands its y to group 0 through shared memory; group 0 writes
+// y0 + y1 to Y, or to this CTA's partial slot of a split tile.
+template <int kType, int kNPad, int kMaxProbs>
+__device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_t tmem,
+                                  const uint8_t* base, uint32_t bar0) {
+    using L = TcLayout<kType, kNPad>;
+    static_assert(L::kScaled, "scaled form");
+    constexpr int R = L::kRawStages;
+    constexpr int G = L::kGroupSlots;
+    constexpr int B = L::kAccBufs;
+    constexpr int kHalfWords = L::kRawRow / 8;   // 18
+    constexpr int kHalfBlocks = 4;
+    auto raw_full = [&](int r) { return bar0 + 8u * r; };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
+    auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
+    auto a_empty = [&](int g, int i) { return bar0 + 8u * (2 * R + 2 * G + g * G + i); };
+    auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
+    const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
+    auto y_full = [&](int t) { return mma_done + 8u * (1 + t); };
+    auto y_free = [&](int t) { return mma_done + 8u * (3 + t); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = (warp - kFirstDequantWarp) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t tlane = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t a_lane = tmem + tlane + L::kAccCols;
+    float* ybuf = reinterpret_cast<float*>(const_cast<uint8_t*>(base) + L::kOffY);
+
+    float y[kNPad];
+#pragma unroll
+    for (int t = 0; t < kNPad; ++t) y[t] = 0.0f;
+    float dprev[kHalfBlocks];
+    int prev_n = -1;                  // super-step whose scaling is due
+    bool prev_last = false;           // ... and it ends its tile
+    int prev_p = 0, prev_rows = 0, prev_slot = -1;
+    int64_t prev_row0 = 0;
+    int head_p = -1, head_rows = 0;
+    int64_t head_row0 = 0;
+    int tile_n = 0;                   // tiles finished by this CTA
+
+    auto scale = [&](int n, const float (&d)[kHalfBlocks]) -> bool {
+        const int b = n & 1;
+        if (!warp_wait(acc_full(b), (n >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t acc =
+            tmem + tlane + static_cast<uint32_t>(b * L::kUnitCols + g * kHalfBlocks * kNPad);
+#pragma unroll
+        for (int blk = 0; blk < kHalfBlocks; blk += 2) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16_async(acc + blk * kNPad, v0);
+            tmem_ld16_async(acc + (blk + 1) * kNPad, v1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk], __uint_as_float(v0[t]), y[t]);
+#pragma unroll
+            for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk + 1], __uint_as_float(v1[t]), y[t]);
+        }
+        tc_fence_before();
+        mbar_arrive(acc_empty(b));
+        return true;
+    };
+    auto finish_tile = [&](int p, int64_t row0, int rows, int slot) -> bool {
+        const int tb = tile_n & 1;
+        const uint32_t ph = (tile_n >> 1) & 1;
+        float* yb = ybuf + (tb * kBM + row) * L::kYStride;
+        ++tile_n;
+        if (g == 1) {
+            if (!mbar_wait(y_free(tb), ph ^ 1)) return false;
+#pragma unroll
+            for (int t = 0; t < kNPad; ++t) yb[t] = y[t];
+            mbar_arrive(y_full(tb));   // release: the stores above before group 0's reads
+#pragma unroll
+            for (int t = 0; t < kNPad; ++t) y[t] = 0.0f;
+            return true;
+        }
+        if (!mbar_wait(y_full(tb), ph)) return false;
+#pragma unroll
+        for (int t = 0; t < kNPad; ++t) y[t] += yb[t];
+        mbar_arrive(y_free(tb));
+        const TcProb& pr = P.p[p];
+        float* part = P.part + (static_cast<int64_t>(blockIdx.x) * 2 + max(slot, 0)) *
+                                   (kNPad * kBM);
+        if (row < rows) {
+#pragma unroll
+            for (int t = 0; t < kNPad; ++t) {
+                if (t >= P.n_tok) continue;
+                if (slot < 0)
+                    pr.Y[t * pr.M + row0 + row] = y[t];
+                else
+                    part[t * kBM + row] = y[t];
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kNPad; ++t) y[t] = 0.0f;
+        if (slot == 1) {
+            tc_finish_split<kNPad>(P, p, row0, rows, 1, quad, lane);
+        } else if (slot == 0) {   // the share's first tile: finished after the last one
+            head_p = p;
+            head_row0 = row0;
+            head_rows = rows;
+        }
+        return true;
+    };
+
+    int raw_n = 0;
+    bool ok = true;
+    uint32_t raw[kHalfWords];
+    for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
+        const int r = raw_n % R;
+        if (!mbar_wait(raw_full(r), (raw_n / R) & 1)) {
+            ok = false;
+            break;
+        }
+        {
+            const uint8_t* src =
+                base + L::kOffRaw + r * L::kStage + row * L::kRawRow + g * (L::kRawRow / 2);
+            if (g == 0)
+                load_half_row<0>(src, raw);
+            else
+                load_half_row<1>(src, raw);
+            uint32_t dep = 0;
+#pragma unroll
+            for (int i = 0; i < kHalfWords; ++i) dep ^= raw[i];
+            release_to_async_proxy(dep);
+        }
+        mbar_arrive(raw_empty(r));
+        float dcur[kHalfBlocks];
+#pragma unroll
+        for (int blk = 0; blk < kHalfBlocks; ++blk)
+            dcur[blk] = half_bits_to_float(u16_at(raw, blk * kQ4Bytes));
+        const int gi = raw_n % G;
+        if (!mbar_wait(a_empty(g, gi), ((raw_n / G) & 1) ^ 1)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t a_slot = a_lane + (g * G + gi) * kSlotCols;
+        {
+            uint32_t packed[16];
+            q4_codes_at<0 * kQ4Bytes>(raw, packed);
+            tmem_st16(a_slot, packed);
+        }
+        {
+            uint32_t packed[16];
+            q4_codes_at<1 * kQ4Bytes>(raw, packed);
+            tmem_st16(a_slot + 16, packed);
+        }
+        {
+            uint32_t packed[16];
+            q4_codes_at<2 * kQ4Bytes>(raw, packed);
+            tmem_st16(a_slot + 32, packed);
+        }
+        {
+            uint32_t packed[16];
+            q4_codes_at<3 * kQ4Bytes>(raw, packed);
+            tmem_st16(a_slot + 48, packed);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(a_full(g, gi));
+        if (prev_n >= 0) {
+            if (!scale(prev_n, dprev) ||
+                (prev_last && !finish_tile(prev_p, prev_row0, prev_rows, prev_slot))) {
+                ok = false;
+                break;
+            }
+        }
+        prev_n = raw_n;
+#pragma unroll
+        for (int blk = 0; blk < kHalfBlocks; ++blk) dprev[blk] = dcur[blk];
+        prev_last = w.j == w.jend - 1;
+        if (prev_last) {
+            // a tile cut by this share's start (jbeg > 0) is partial slot 0, one cut by its
+            // end slot 1
+            prev_p = w.p;
+            prev_row0 = w.row0;
+            prev_rows = w.rows;
+            prev_slot = w.jbeg > 0 ? 0 : (w.jend < w.nsuper ? 1 : -1);
+        }
+    }
+    if (ok && prev_n >= 0) {
+        ok = scale(prev_n, dprev);
+        if (ok && prev_last) ok = finish_tile(prev_p, prev_row0, prev_rows, prev_slot);
+    }
+    if (ok && head_p >= 0) tc_finish_split<kNPad>(P, head_p, head_row0, head_rows, 0, quad, lane);
+    tmem_st_wait();   // no TMEM store of this thread may be in flight when TMEM is freed
+    if (!ok && lane == 0) report_status(P.status, kStatusTimeout);
+}
+
 template <int kType, int kNPad, int kMaxProbs>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
@@ -298,9 +574,13 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             }
         for (int b = 0; b < B; ++b) {
             mbar_init(acc_full(b), kMmaWarps);
-            mbar_init(acc_empty(b), 32 * kMmaWarps);
+            // read out by the issuer warps, or in the scaled form by the dequantize warps
+            mbar_init(acc_empty(b), 32 * (L::kScaled ? kDequantWarps : kMmaWarps));
         }
         mbar_init(mma_done, kMmaWarps);
+        if constexpr (L::kScaled) {
+            for (int i = 0; i < 4; ++i) mbar_init(mma_done + 8u * (1 + i), 32 * kDequantWarps / 2);
+        }
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -371,199 +651,207 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
         // the TMEM lane quadrant it may access (warp % 4); with two sets this epilogue
         // runs after the next tile's first MMAs have been queued.
         griddep_wait();   // X tiles, Y, partial sums and counters of the previous kernel
-        const int q = warp - 1;
-        const int g = q >> 1;                      // dequantize group that fills quarter q
-        const int quad = warp & 3;
-        const uint32_t tlane = static_cast<uint32_t>(quad * 32) << 16;
-        constexpr uint32_t idesc = idesc_bf16_f32(kBM, kNPad);
-        int tile = 0, raw_n = 0;
-        bool ok = true;
-        // epilogue of a finished tile; `slot` < 0: the whole tile, write Y; else a split
-        // tile's partial sum, written to partial slot `slot` of this CTA
-        int pend_p = -1, pend_rows = 0, pend_tile = 0, pend_slot = -1;
-        int64_t pend_row0 = 0;
-        int head_p = -1, head_rows = 0;
-        int64_t head_row0 = 0;
-        auto epilogue = [&](int p, int64_t row0, int rows, int t, int slot) -> bool {
-            const int b = t % B;
-            if (!warp_wait(acc_full(b), (t / B) & 1)) return false;
-            tc_fence_after();
-            const TcProb& pr = P.p[p];
-            const int row = quad * 32 + lane;
-            float* part = P.part + (static_cast<int64_t>(blockIdx.x) * 2 + max(slot, 0)) *
-                                       (kNPad * kBM);
-            const uint32_t acc = tmem + tlane + static_cast<uint32_t>(b * kQuarters * kNPad);
-#pragma unroll
-            for (int c = 0; c < kNPad; c += 16) {
-                // y = (acc0 + acc1) + (acc2 + acc3), the same order for every element
-                float y[16];
-                {
-                    uint32_t v0[16], v1[16];
-                    tmem_ld16(acc + 0 * kNPad + c, v0);
-                    tmem_ld16(acc + 1 * kNPad + c, v1);
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        y[jj] = __uint_as_float(v0[jj]) + __uint_as_float(v1[jj]);
-                }
-                {
-                    uint32_t v2[16], v3[16];
-                    tmem_ld16(acc + 2 * kNPad + c, v2);
-                    tmem_ld16(acc + 3 * kNPad + c, v3);
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        y[jj] += __uint_as_float(v2[jj]) + __uint_as_float(v3[jj]);
-                }
-                if (row < rows) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int n = c + jj;
-                        if (n >= P.n_tok) continue;
-                        if (slot < 0)
-                            pr.Y[n * pr.M + row0 + row] = y[jj];
-                        else
-                            part[n * kBM + row] = y[jj];
+        if constexpr (L::kScaled) {
+            tc_issue_scaled<kType, kNPad, kMaxProbs>(P, w, tmem, sRaw, bar0);
+        } else {
+            const int q = warp - 1;
+            const int g = q >> 1;                      // dequantize group that fills quarter q
+            const int quad = warp & 3;
+            const uint32_t tlane = static_cast<uint32_t>(quad * 32) << 16;
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kNPad);
+            int tile = 0, raw_n = 0;
+            bool ok = true;
+            // epilogue of a finished tile; `slot` < 0: the whole tile, write Y; else a split
+            // tile's partial sum, written to partial slot `slot` of this CTA
+            int pend_p = -1, pend_rows = 0, pend_tile = 0, pend_slot = -1;
+            int64_t pend_row0 = 0;
+            int head_p = -1, head_rows = 0;
+            int64_t head_row0 = 0;
+            auto epilogue = [&](int p, int64_t row0, int rows, int t, int slot) -> bool {
+                const int b = t % B;
+                if (!warp_wait(acc_full(b), (t / B) & 1)) return false;
+                tc_fence_after();
+                const TcProb& pr = P.p[p];
+                const int row = quad * 32 + lane;
+                float* part = P.part + (static_cast<int64_t>(blockIdx.x) * 2 + max(slot, 0)) *
+                                           (kNPad * kBM);
+                const uint32_t acc = tmem + tlane + static_cast<uint32_t>(b * kQuarters * kNPad);
+    #pragma unroll
+                for (int c = 0; c < kNPad; c += 16) {
+                    // y = (acc0 + acc1) + (acc2 + acc3), the same order for every element
+                    float y[16];
+                    {
+                        uint32_t v0[16], v1[16];
+                        tmem_ld16(acc + 0 * kNPad + c, v0);
+                        tmem_ld16(acc + 1 * kNPad + c, v1);
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            y[jj] = __uint_as_float(v0[jj]) + __uint_as_float(v1[jj]);
+                    }
+                    {
+                        uint32_t v2[16], v3[16];
+                        tmem_ld16(acc + 2 * kNPad + c, v2);
+                        tmem_ld16(acc + 3 * kNPad + c, v3);
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            y[jj] += __uint_as_float(v2[jj]) + __uint_as_float(v3[jj]);
+                    }
+                    if (row < rows) {
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int n = c + jj;
+                            if (n >= P.n_tok) continue;
+                            if (slot < 0)
+                                pr.Y[n * pr.M + row0 + row] = y[jj];
+                            else
+                                part[n * kBM + row] = y[jj];
+                        }
                     }
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(acc_empty(b));
-            if (slot == 1) {
-                tc_finish_split<kNPad>(P, p, row0, rows, 1, quad, lane);
-            } else if (slot == 0) {   // the share's first tile: finished after the last one
-                head_p = p;
-                head_row0 = row0;
-                head_rows = rows;
-            }
-            return true;
-        };
-        for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
-            const int b = tile % B;
-            if (w.j == w.jbeg) {   // a new tile: its accumulator set must have been read out
-                if (!warp_wait(acc_empty(b), ((tile / B) & 1) ^ 1)) {
+                tc_fence_before();
+                mbar_arrive(acc_empty(b));
+                if (slot == 1) {
+                    tc_finish_split<kNPad>(P, p, row0, rows, 1, quad, lane);
+                } else if (slot == 0) {   // the share's first tile: finished after the last one
+                    head_p = p;
+                    head_row0 = row0;
+                    head_rows = rows;
+                }
+                return true;
+            };
+            for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
+                const int b = tile % B;
+                if (w.j == w.jbeg) {   // a new tile: its accumulator set must have been read out
+                    if (!warp_wait(acc_empty(b), ((tile / B) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                const int r = raw_n % R;
+                const int gi = raw_n % G;
+                if (!warp_wait(raw_full(r), (raw_n / R) & 1) ||      // the super-step's X landed
+                    !warp_wait(a_full(g, gi), (raw_n / G) & 1)) {    // quarter q dequantized
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-            }
-            const int r = raw_n % R;
-            const int gi = raw_n % G;
-            if (!warp_wait(raw_full(r), (raw_n / R) & 1) ||      // the super-step's X landed
-                !warp_wait(a_full(g, gi), (raw_n / G) & 1)) {    // quarter q dequantized
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t sX = sRaw + r * L::kStage + L::kRaw + q * L::kB;
-                const uint32_t a_col =
-                    tmem + L::kAccCols + (g * G + gi) * kSlotCols + (q & 1) * (kBK / 2);
-                const uint32_t d = tmem + static_cast<uint32_t>((b * kQuarters + q) * kNPad);
-#pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    umma_bf16_tmem_a(d, a_col + kk * 8, sw128_kmajor_desc(sX + kk * 32), idesc,
-                                     (w.j != w.jbeg || kk != 0) ? 1u : 0u);
-                umma_commit(a_empty(g, gi));
-                umma_commit(raw_empty(r));
-                if (w.j == w.jend - 1) umma_commit(acc_full(b));
-            }
-            __syncwarp();
-            if (B == 2 && w.j == w.jbeg && pend_p >= 0) {
-                if (!epilogue(pend_p, pend_row0, pend_rows, pend_tile, pend_slot)) {
-                    ok = false;
-                    break;
+                if (lane == 0) {
+                    const uint32_t sX = sRaw + r * L::kStage + L::kRaw + q * L::kB;
+                    const uint32_t a_col =
+                        tmem + L::kAccCols + (g * G + gi) * kSlotCols + (q & 1) * (kBK / 2);
+                    const uint32_t d = tmem + static_cast<uint32_t>((b * kQuarters + q) * kNPad);
+    #pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_bf16_tmem_a(d, a_col + kk * 8, sw128_kmajor_desc(sX + kk * 32), idesc,
+                                         (w.j != w.jbeg || kk != 0) ? 1u : 0u);
+                    umma_commit(a_empty(g, gi));
+                    umma_commit(raw_empty(r));
+                    if (w.j == w.jend - 1) umma_commit(acc_full(b));
                 }
-                pend_p = -1;
-            }
-            if (w.j == w.jend - 1) {
-                // a tile cut by this share's start (jbeg > 0) is partial slot 0, one cut by
-                // its end slot 1
-                const int slot = w.jbeg > 0 ? 0 : (w.jend < w.nsuper ? 1 : -1);
-                if (B == 1) {
-                    if (!epilogue(w.p, w.row0, w.rows, tile, slot)) {
+                __syncwarp();
+                if (B == 2 && w.j == w.jbeg && pend_p >= 0) {
+                    if (!epilogue(pend_p, pend_row0, pend_rows, pend_tile, pend_slot)) {
                         ok = false;
                         break;
                     }
-                } else {
-                    pend_p = w.p;
-                    pend_row0 = w.row0;
-                    pend_rows = w.rows;
-                    pend_tile = tile;
-                    pend_slot = slot;
+                    pend_p = -1;
                 }
-                ++tile;
+                if (w.j == w.jend - 1) {
+                    // a tile cut by this share's start (jbeg > 0) is partial slot 0, one cut by
+                    // its end slot 1
+                    const int slot = w.jbeg > 0 ? 0 : (w.jend < w.nsuper ? 1 : -1);
+                    if (B == 1) {
+                        if (!epilogue(w.p, w.row0, w.rows, tile, slot)) {
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        pend_p = w.p;
+                        pend_row0 = w.row0;
+                        pend_rows = w.rows;
+                        pend_tile = tile;
+                        pend_slot = slot;
+                    }
+                    ++tile;
+                }
             }
+            if (ok && pend_p >= 0) ok = epilogue(pend_p, pend_row0, pend_rows, pend_tile, pend_slot);
+            if (ok && head_p >= 0) tc_finish_split<kNPad>(P, head_p, head_row0, head_rows, 0, quad, lane);
+            // Completes when every MMA this thread issued has finished (also after a timeout),
+            // so the TMEM release below never races an MMA in flight.
+            if (lane == 0) umma_commit(mma_done);
+            if (!ok && lane == 0) report_status(P.status, kStatusTimeout);
         }
-        if (ok && pend_p >= 0) ok = epilogue(pend_p, pend_row0, pend_rows, pend_tile, pend_slot);
-        if (ok && head_p >= 0) tc_finish_split<kNPad>(P, head_p, head_row0, head_rows, 0, quad, lane);
-        // Completes when every MMA this thread issued has finished (also after a timeout),
-        // so the TMEM release below never races an MMA in flight.
-        if (lane == 0) umma_commit(mma_done);
-        if (!ok && lane == 0) report_status(P.status, kStatusTimeout);
     } else {
-        // ---------------- dequantize ----------------
-        // Group g (warps 5..8 or 9..12) takes k [128 g, 128 g + 128) of every super-step
-        // for all 128 rows; each warp its TMEM lane quadrant 32 * (warp % 4) + i, one row
-        // per thread, written to the group's A slot with tcgen05.st.
-        const int g = (warp - kFirstDequantWarp) >> 2;
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCols;
-        int raw_n = 0;
-        bool ok = true;
-        uint32_t raw[kHalfWords];
-        for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
-            const int r = raw_n % R;
-            if (!mbar_wait(raw_full(r), (raw_n / R) & 1)) {
-                ok = false;
-                break;
+        if constexpr (L::kScaled) {
+            tc_dequant_scaled<kType, kNPad, kMaxProbs>(P, w, tmem, base, bar0);
+        } else {
+            // ---------------- dequantize ----------------
+            // Group g (warps 5..8 or 9..12) takes k [128 g, 128 g + 128) of every super-step
+            // for all 128 rows; each warp its TMEM lane quadrant 32 * (warp % 4) + i, one row
+            // per thread, written to the group's A slot with tcgen05.st.
+            const int g = (warp - kFirstDequantWarp) >> 2;
+            const int quad = warp & 3;
+            const int row = quad * 32 + lane;
+            const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCols;
+            int raw_n = 0;
+            bool ok = true;
+            uint32_t raw[kHalfWords];
+            for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
+                const int r = raw_n % R;
+                if (!mbar_wait(raw_full(r), (raw_n / R) & 1)) {
+                    ok = false;
+                    break;
+                }
+                // Every row of the box is loaded; rows past the matrix end arrive as zeros and
+                // dequantize to zero operands (their outputs are dropped).
+                {
+                    const uint8_t* src = base + L::kOffRaw + r * L::kStage + row * L::kRawRow +
+                                         g * (L::kRawRow / 2);
+                    if (g == 0)
+                        load_half_row<0>(src, raw);
+                    else
+                        load_half_row<1>(src, raw);
+                    uint32_t dep = 0;
+    #pragma unroll
+                    for (int i = 0; i < kHalfWords; ++i) dep ^= raw[i];
+                    release_to_async_proxy(dep);
+                }
+                mbar_arrive(raw_empty(r));
+                const int gi = raw_n % G;
+                if (!mbar_wait(a_empty(g, gi), ((raw_n / G) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_slot = a_lane + (g * G + gi) * kSlotCols;
+                {
+                    uint32_t packed[16];
+                    dequant_block<kType, 0>(raw, packed);
+                    tmem_st16(a_slot, packed);
+                }
+                {
+                    uint32_t packed[16];
+                    dequant_block<kType, 1>(raw, packed);
+                    tmem_st16(a_slot + 16, packed);
+                }
+                {
+                    uint32_t packed[16];
+                    dequant_block<kType, 2>(raw, packed);
+                    tmem_st16(a_slot + 32, packed);
+                }
+                {
+                    uint32_t packed[16];
+                    dequant_block<kType, 3>(raw, packed);
+                    tmem_st16(a_slot + 48, packed);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(a_full(g, gi));
             }
-            // Every row of the box is loaded; rows past the matrix end arrive as zeros and
-            // dequantize to zero operands (their outputs are dropped).
-            {
-                const uint8_t* src = base + L::kOffRaw + r * L::kStage + row * L::kRawRow +
-                                     g * (L::kRawRow / 2);
-                if (g == 0)
-                    load_half_row<0>(src, raw);
-                else
-                    load_half_row<1>(src, raw);
-                uint32_t dep = 0;
-#pragma unroll
-                for (int i = 0; i < kHalfWords; ++i) dep ^= raw[i];
-                release_to_async_proxy(dep);
-            }
-            mbar_arrive(raw_empty(r));
-            const int gi = raw_n % G;
-            if (!mbar_wait(a_empty(g, gi), ((raw_n / G) & 1) ^ 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a_slot = a_lane + (g * G + gi) * kSlotCols;
-            {
-                uint32_t packed[16];
-                dequant_block<kType, 0>(raw, packed);
-                tmem_st16(a_slot, packed);
-            }
-            {
-                uint32_t packed[16];
-                dequant_block<kType, 1>(raw, packed);
-                tmem_st16(a_slot + 16, packed);
-            }
-            {
-                uint32_t packed[16];
-                dequant_block<kType, 2>(raw, packed);
-                tmem_st16(a_slot + 32, packed);
-            }
-            {
-                uint32_t packed[16];
-                dequant_block<kType, 3>(raw, packed);
-                tmem_st16(a_slot + 48, packed);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(a_full(g, gi));
+            if (!ok) report_status(P.status, kStatusTimeout);
         }
-        if (!ok) report_status(P.status, kStatusTimeout);
     }
     tc_fence_before();
     __syncthreads();

@@ -119,8 +119,9 @@ gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * N <= 2 (or K % 256 != 0): decode kernels on CUDA cores (exact integer block products
  * on a 16-bit fixed-point copy of X). 3 <= N <= 64 and K % 256 == 0: decode on tensor
  * cores; N >= 65 and K % 256 == 0: the prefill tensor-core GEMM. Both tensor-core paths
- * use bf16 operands (dequantized weights and X each rounded once to bf16) and fp32
- * accumulation.
+ * round X once to bf16 and accumulate in fp32. The weights enter the MMA as bf16
+ * dequantized values (rounded once), except Q4_0 decode with N <= 16, which multiplies
+ * the exact codes c - 8 and applies each block's scale in fp32.
  * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element (for the bf16
  * path, at the K >= 256 it runs on, by a wide margin for non-adversarial data). Results
  * are deterministic: the same inputs give the same bits on every call.
