@@ -294,7 +294,6 @@ __device__ void tc_issue_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_
     auto raw_full = [&](int r) { return bar0 + 8u * r; };
     auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
     auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
-    auto a_empty = [&](int g, int i) { return bar0 + 8u * (2 * R + 2 * G + g * G + i); };
     auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
     auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
     const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
@@ -326,7 +325,8 @@ __device__ void tc_issue_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_
                 umma_bf16_tmem_a(d0 + (kk >> 1) * kNPad, a_col + kk * 8,
                                  sw128_kmajor_desc(sX + kk * 32), idesc,
                                  static_cast<uint32_t>(kk & 1));
-            umma_commit(a_empty(g, gi));
+            // No commit for the A slot: the dequantize warps reuse it only after they have
+            // waited for acc_full of the super-step two back, whose MMAs read it.
             umma_commit(raw_empty(r));
             umma_commit(acc_full(b));
         }
@@ -357,7 +357,6 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
     auto raw_full = [&](int r) { return bar0 + 8u * r; };
     auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
     auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
-    auto a_empty = [&](int g, int i) { return bar0 + 8u * (2 * R + 2 * G + g * G + i); };
     auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
     auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
     const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
@@ -391,16 +390,14 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
         tc_fence_after();
         const uint32_t acc =
             tmem + tlane + static_cast<uint32_t>(b * L::kUnitCols + g * kHalfBlocks * kNPad);
+        uint32_t v[kHalfBlocks][16];   // all four blocks' accumulators behind one wait
 #pragma unroll
-        for (int blk = 0; blk < kHalfBlocks; blk += 2) {
-            uint32_t v0[16], v1[16];
-            tmem_ld16_async(acc + blk * kNPad, v0);
-            tmem_ld16_async(acc + (blk + 1) * kNPad, v1);
-            tmem_ld_wait();
+        for (int blk = 0; blk < kHalfBlocks; ++blk) tmem_ld16_async(acc + blk * kNPad, v[blk]);
+        tmem_ld_wait();
 #pragma unroll
-            for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk], __uint_as_float(v0[t]), y[t]);
+        for (int blk = 0; blk < kHalfBlocks; ++blk) {
 #pragma unroll
-            for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk + 1], __uint_as_float(v1[t]), y[t]);
+            for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk], __uint_as_float(v[blk][t]), y[t]);
         }
         tc_fence_before();
         mbar_arrive(acc_empty(b));
@@ -475,11 +472,10 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
 #pragma unroll
         for (int blk = 0; blk < kHalfBlocks; ++blk)
             dcur[blk] = half_bits_to_float(u16_at(raw, blk * kQ4Bytes));
+        // The A slot of super-step n was last read by the MMAs of n - G (G = 2), which this
+        // thread saw complete when it waited for acc_full(n - 2) while scaling it.
+        static_assert(G == 2, "slot reuse follows the accumulator buffers");
         const int gi = raw_n % G;
-        if (!mbar_wait(a_empty(g, gi), ((raw_n / G) & 1) ^ 1)) {
-            ok = false;
-            break;
-        }
         tc_fence_after();
         const uint32_t a_slot = a_lane + (g * G + gi) * kSlotCols;
         {
