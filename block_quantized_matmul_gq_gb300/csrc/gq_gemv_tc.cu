@@ -204,6 +204,18 @@ __device__ void tc_walk_next(const TcParams<kMaxProbs>& P, TcWalk& w) {
 // memory. The half starts 16-byte aligned (kG = 0) or 8 bytes past (kG = 1): one 8-byte
 // load at the unaligned end, 16-byte loads for the rest, which a quarter warp serves
 // without bank conflicts at the 144 / 272-byte row pitch.
+// One word of each shared load of load_half_row<kG>, combined: depending on it makes every
+// load complete before what follows (the proxy fence that lets the stage be refilled).
+template <int kG, int kWords>
+__device__ __forceinline__ uint32_t half_row_dep(const uint32_t (&raw)[kWords]) {
+    constexpr int w8 = kG == 0 ? kWords - 2 : 0;
+    constexpr int w16 = kG == 0 ? 0 : 2;
+    uint32_t d = raw[w8];
+#pragma unroll
+    for (int i = 0; i < (kWords - 2) / 4; ++i) d ^= raw[w16 + 4 * i];
+    return d;
+}
+
 template <int kG, int kWords>
 __device__ __forceinline__ void load_half_row(const uint8_t* src, uint32_t (&raw)[kWords]) {
     constexpr int w8 = kG == 0 ? kWords - 2 : 0;
@@ -295,7 +307,6 @@ __device__ void tc_issue_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_
     auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
     auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
     auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
-    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
     const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -308,8 +319,9 @@ __device__ void tc_issue_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_
         const int b = raw_n & 1;
         const int r = raw_n % R;
         const int gi = raw_n % G;
-        if (!warp_wait(acc_empty(b), ((raw_n >> 1) & 1) ^ 1) ||   // buffer b scaled out
-            !warp_wait(raw_full(r), (raw_n / R) & 1) ||            // the super-step's X landed
+        // Buffer b's columns of blocks 2q, 2q + 1 were last read by group g scaling
+        // super-step n - 2, which it did before storing the codes that a_full(g) announces.
+        if (!warp_wait(raw_full(r), (raw_n / R) & 1) ||            // the super-step's X landed
             !warp_wait(a_full(g, gi), (raw_n / G) & 1)) {          // quarter q's codes stored
             ok = false;
             break;
@@ -358,7 +370,6 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
     auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
     auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
     auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
-    auto acc_empty = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + B + b); };
     const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
     auto y_full = [&](int t) { return mma_done + 8u * (1 + t); };
     auto y_free = [&](int t) { return mma_done + 8u * (3 + t); };
@@ -399,8 +410,6 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
 #pragma unroll
             for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk], __uint_as_float(v[blk][t]), y[t]);
         }
-        tc_fence_before();
-        mbar_arrive(acc_empty(b));
         return true;
     };
     auto finish_tile = [&](int p, int64_t row0, int rows, int slot) -> bool {
@@ -458,13 +467,14 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
         {
             const uint8_t* src =
                 base + L::kOffRaw + r * L::kStage + row * L::kRawRow + g * (L::kRawRow / 2);
-            if (g == 0)
+            uint32_t dep;
+            if (g == 0) {
                 load_half_row<0>(src, raw);
-            else
+                dep = half_row_dep<0>(raw);
+            } else {
                 load_half_row<1>(src, raw);
-            uint32_t dep = 0;
-#pragma unroll
-            for (int i = 0; i < kHalfWords; ++i) dep ^= raw[i];
+                dep = half_row_dep<1>(raw);
+            }
             release_to_async_proxy(dep);
         }
         mbar_arrive(raw_empty(r));
@@ -672,7 +682,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                 float* part = P.part + (static_cast<int64_t>(blockIdx.x) * 2 + max(slot, 0)) *
                                            (kNPad * kBM);
                 const uint32_t acc = tmem + tlane + static_cast<uint32_t>(b * kQuarters * kNPad);
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < kNPad; c += 16) {
                     // y = (acc0 + acc1) + (acc2 + acc3), the same order for every element
                     float y[16];
@@ -680,7 +690,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                         uint32_t v0[16], v1[16];
                         tmem_ld16(acc + 0 * kNPad + c, v0);
                         tmem_ld16(acc + 1 * kNPad + c, v1);
-    #pragma unroll
+#pragma unroll
                         for (int jj = 0; jj < 16; ++jj)
                             y[jj] = __uint_as_float(v0[jj]) + __uint_as_float(v1[jj]);
                     }
@@ -688,12 +698,12 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                         uint32_t v2[16], v3[16];
                         tmem_ld16(acc + 2 * kNPad + c, v2);
                         tmem_ld16(acc + 3 * kNPad + c, v3);
-    #pragma unroll
+#pragma unroll
                         for (int jj = 0; jj < 16; ++jj)
                             y[jj] += __uint_as_float(v2[jj]) + __uint_as_float(v3[jj]);
                     }
                     if (row < rows) {
-    #pragma unroll
+#pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
                             const int n = c + jj;
                             if (n >= P.n_tok) continue;
@@ -737,7 +747,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                     const uint32_t a_col =
                         tmem + L::kAccCols + (g * G + gi) * kSlotCols + (q & 1) * (kBK / 2);
                     const uint32_t d = tmem + static_cast<uint32_t>((b * kQuarters + q) * kNPad);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         umma_bf16_tmem_a(d, a_col + kk * 8, sw128_kmajor_desc(sX + kk * 32), idesc,
                                          (w.j != w.jbeg || kk != 0) ? 1u : 0u);
@@ -805,13 +815,14 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                 {
                     const uint8_t* src = base + L::kOffRaw + r * L::kStage + row * L::kRawRow +
                                          g * (L::kRawRow / 2);
-                    if (g == 0)
+                    uint32_t dep;
+                    if (g == 0) {
                         load_half_row<0>(src, raw);
-                    else
+                        dep = half_row_dep<0>(raw);
+                    } else {
                         load_half_row<1>(src, raw);
-                    uint32_t dep = 0;
-    #pragma unroll
-                    for (int i = 0; i < kHalfWords; ++i) dep ^= raw[i];
+                        dep = half_row_dep<1>(raw);
+                    }
                     release_to_async_proxy(dep);
                 }
                 mbar_arrive(raw_empty(r));
