@@ -58,6 +58,17 @@ __device__ __forceinline__ float2 sub_mul2(float2 a, float2 b, float2 c) {
     return r;
 }
 
+// (y0, y1) = fma(d, (a0, a1), (y0, y1)) on two fp32 lanes at once (Blackwell packed fp32):
+// each lane rounded once, exactly like fmaf.
+__device__ __forceinline__ void fma2_bcast(float& y0, float& y1, float d, float a0, float a1) {
+    asm("{\n\t.reg .b64 y, a, dd;\n\t"
+        "mov.b64 y, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\tmov.b64 dd, {%4, %4};\n\t"
+        "fma.rn.f32x2 y, dd, a, y;\n\t"
+        "mov.b64 {%0, %1}, y;\n\t}"
+        : "+f"(y0), "+f"(y1)
+        : "f"(a0), "f"(a1), "f"(d));
+}
+
 // Dequantizes the block that starts at byte kOff of the raw bytes in r (kOff even) into
 // 32 bf16 values packed in pairs: out[i] = elements 2i (low half) and 2i+1 (high half).
 // Each value is the exact (c - 8) * d (Q4_0) or c * d (Q8_0) (at most 8 + 11 significant

@@ -408,7 +408,9 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
 #pragma unroll
         for (int blk = 0; blk < kHalfBlocks; ++blk) {
 #pragma unroll
-            for (int t = 0; t < kNPad; ++t) y[t] = fmaf(d[blk], __uint_as_float(v[blk][t]), y[t]);
+            for (int t = 0; t < kNPad; t += 2)   // y = fma(d, acc, y) on two tokens at once
+                fma2_bcast(y[t], y[t + 1], d[blk], __uint_as_float(v[blk][t]),
+                           __uint_as_float(v[blk][t + 1]));
         }
         return true;
     };
