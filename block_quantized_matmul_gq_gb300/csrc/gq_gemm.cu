@@ -229,9 +229,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                 raw[4 * i + 3] = v.w;
             }
             {
+                // one word of each 16-byte load: all loads complete before the fence
                 uint32_t dep = 0;
 #pragma unroll
-                for (int i = 0; i < kRawWords; ++i) dep ^= raw[i];
+                for (int i = 0; i < kRawWords / 4; ++i) dep ^= raw[4 * i];
                 release_to_async_proxy(dep);
             }
             mbar_arrive(raw_empty(r));
