@@ -295,6 +295,7 @@ def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None):
 # (key, workload id, type, shapes, N values).
 DECODE_SETS = [
     ("single_q4_0_2048x2048", 1, "q4_0", "single", (1,)),
+    ("tinyllama_decode_q4_0", 2, "q4_0", "tinyllama", (2, 4, 8, 16)),
     ("tinyllama_decode_q8_0", 3, "q8_0", "tinyllama", (1, 2, 4, 8, 16)),
     ("llama7b_decode_q4_0", 5, "q4_0", "llama7b", (1, 16)),
 ]
