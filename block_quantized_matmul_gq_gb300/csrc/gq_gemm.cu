@@ -70,7 +70,7 @@ struct Layout {
     static constexpr int kOffB = kOffA + kStages * kA;
     static constexpr int kOffRaw = kOffB + kStages * kB;
     static constexpr int kOffBar = kOffRaw + kRawStages * kRaw;
-    static constexpr int kNumBars = 3 * kStages + 2 * kRawStages + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * kRawStages + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;   // room to align the base to 1024
@@ -98,13 +98,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     const uint32_t sB = base_addr + L::kOffB;
     const uint32_t sRaw = base_addr + L::kOffRaw;
     const uint32_t bar0 = base_addr + L::kOffBar;
-    // barrier order: a_full[S], b_full[S], empty[S], raw_full[R], raw_empty[R], acc_full
-    auto a_full = [&](int s) { return bar0 + 8u * s; };
-    auto b_full = [&](int s) { return bar0 + 8u * (S + s); };
-    auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto raw_full = [&](int r) { return bar0 + 8u * (3 * S + r); };
-    auto raw_empty = [&](int r) { return bar0 + 8u * (3 * S + L::kRawStages + r); };
-    const uint32_t acc_full = bar0 + 8u * (3 * S + 2 * L::kRawStages);
+    // barrier order: full[S], empty[S], raw_full[R], raw_empty[R], acc_full. Stage s is
+    // "full" when its dequantized A (every dequantize thread arrives) and its X tile (the
+    // producer's arrival with the copy's bytes) are both in place: one wait for the MMAs.
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    auto raw_full = [&](int r) { return bar0 + 8u * (2 * S + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * S + L::kRawStages + r); };
+    const uint32_t acc_full = bar0 + 8u * (2 * S + 2 * L::kRawStages);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
 
     const int m0 = blockIdx.x * kBM;
@@ -120,8 +121,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(a_full(s), 32 * kDequantWarps);
-            mbar_init(b_full(s), 1);
+            mbar_init(full(s), 32 * kDequantWarps + 1);
             mbar_init(empty(s), 1);
         }
         for (int r = 0; r < L::kRawStages; ++r) {
@@ -168,14 +168,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(b_full(s), L::kB);
-                tma_load_2d(sB + s * L::kB, &tmap_x, (j0 * (kSuperK / kBK) + ks) * kBK, n0, b_full(s));
+                mbar_arrive_expect_tx(full(s), L::kB);
+                tma_load_2d(sB + s * L::kB, &tmap_x, (j0 * (kSuperK / kBK) + ks) * kBK, n0, full(s));
                 ++b_issued;
             }
             if (!ok) report_status(status, kStatusTimeout);
             // Every copy this thread issued must land before the CTA's memory is released.
             for (int i = max(0, b_issued - S); i < b_issued; ++i)
-                mbar_wait(b_full(i % S), (i / S) & 1, kDrainNs);
+                mbar_wait(full(i % S), (i / S) & 1, kDrainNs);
             for (int j = max(0, raw_issued - L::kRawStages); j < raw_issued; ++j)
                 mbar_wait(raw_full(j % L::kRawStages), (j / L::kRawStages) & 1, kDrainNs);
         }
@@ -187,7 +187,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             for (int ks = 0; ks < nk; ++ks) {
                 const int s = ks % S;
                 const uint32_t ph = (ks / S) & 1;
-                if (!mbar_wait(a_full(s), ph) || !mbar_wait(b_full(s), ph)) {
+                if (!mbar_wait(full(s), ph)) {
                     ok = false;
                     break;
                 }
@@ -257,7 +257,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     if (q == 3) dequant_store<kType, 3, 1>(raw, arow, row);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(a_full(s));
+                mbar_arrive(full(s));
             }
         }
         if (!ok) report_status(status, kStatusTimeout);
