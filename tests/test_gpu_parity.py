@@ -200,6 +200,37 @@ def test_back_to_back_calls_see_previous_results(gq_lib, cuda_dev, N):
     assert gq_lib.get_last_error() == 0
 
 
+@pytest.mark.parametrize("N", [1, 8])
+def test_decode_after_quantize_into_the_same_blocks(gq_lib, cuda_dev, N):
+    """A decode call may load its weights before the kernel ahead of it on the stream has
+    completed, but only when that kernel lets it start early, which only libgq's decode
+    kernels do. Quantizing a different matrix into the same block buffer right before each
+    call, with no synchronize, must give bitwise the results of the same sequence with a
+    synchronize after every launch."""
+    M = K = 2048
+    Ws = [workloads.weights(M, K, 70 + i, device=cuda_dev) for i in range(3)]
+    X = workloads.activations(N, K, 73, device=cuda_dev)
+    q = torch.empty((M, gq_lib.row_bytes("q4_0", K)), dtype=torch.uint8, device=cuda_dev)
+
+    def run(sync):
+        outs = []
+        for i in range(12):
+            gq_lib.quantize(Ws[i % 3], "q4_0", out=q)
+            if sync:
+                torch.cuda.synchronize(cuda_dev)
+            outs.append(gq_lib.mul_mat(q, "q4_0", M, K, X))
+            if sync:
+                torch.cuda.synchronize(cuda_dev)
+        torch.cuda.synchronize(cuda_dev)
+        return torch.stack(outs)
+
+    ref = run(True)
+    assert not torch.equal(ref[0], ref[1])   # the matrices differ, so stale blocks would show
+    for _ in range(3):
+        assert torch.equal(run(False).view(torch.int32), ref.view(torch.int32))
+    assert gq_lib.get_last_error() == 0
+
+
 def test_mul_mat_misaligned_x(gq_lib, oracle_mod, cuda_dev):
     """X 4-byte but not 16-byte aligned: correct through the generic kernel."""
     M, K = 40, 2048
