@@ -14,6 +14,10 @@ Every function follows the pages as cited in ``gq_oracle.c``:
     and 7.2 (C = A B; Y = X W^T in the cuBLAS call's layout).
   - mul_mat_q8x: "A Complete Guide to llama.cpp ...", section 2.2 (x quantized like the
     weights; y ~= Delta Delta_x sum q q_x with an integer sum per block).
+  - mul_mat_rmsnorm: "Development Guide ...", section 4.1 (RMSNorm(x) = x / sqrt(mean(x^2)
+    + eps) * gamma) ahead of the product.
+  - mul_mat_swiglu: "Development Guide ...", section 4.4 (Swish(x W_gate) * (x W_up),
+    Swish(z) = z / (1 + e^-z)).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` (IEEE fp16
 conversion against numpy, closed-form blocks, exact-rational brute force, one-hot rows).
@@ -74,6 +78,12 @@ def _load():
         lib.oracle_mul_mat.restype = c_int
         lib.oracle_mul_mat_q8x.argtypes = [c_int, vp, c_int64, c_int64, vp, c_int64, vp, vp]
         lib.oracle_mul_mat_q8x.restype = c_int
+        lib.oracle_mul_mat_rmsnorm.argtypes = [c_int, vp, c_int64, c_int64, vp, vp,
+                                               ctypes.c_double, c_int64, vp, vp, vp]
+        lib.oracle_mul_mat_rmsnorm.restype = c_int
+        lib.oracle_mul_mat_swiglu.argtypes = [c_int, vp, vp, c_int64, c_int64, vp, c_int64,
+                                              vp, vp]
+        lib.oracle_mul_mat_swiglu.restype = c_int
         _lib = lib
     return _lib
 
@@ -189,3 +199,62 @@ def mul_mat_rows(t, blocks, M: int, K: int, X, rows) -> np.ndarray:
     rows = np.asarray(rows, dtype=np.int64)
     sub = np.ascontiguousarray(blocks[rows])
     return mul_mat(t, sub, len(rows), K, X)
+
+
+def mul_mat_rmsnorm(t, blocks, M: int, K: int, X, gamma, eps: float) -> np.ndarray:
+    """Y (N x M fp32) = RMSNorm(X) . What^T, RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gamma
+    ("Development Guide for Small AI Models (TinyLLaMA, etc.) Using C++", section 4.1),
+    the normalized row and the sum in fp64, one rounding at the end."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    X = _f32(X)
+    if X.ndim == 1:
+        X = X.reshape(1, -1)
+    gamma = _f32(gamma).reshape(-1)
+    N = X.shape[0]
+    if X.shape[1] != K or gamma.size != K or blocks.size != M * row_bytes(t, K):
+        raise ValueError("shape mismatch")
+    Y = np.empty((N, M), dtype=np.float32)
+    wrow = np.empty(max(K, 1), dtype=np.float32)
+    xhat = np.empty(max(K, 1), dtype=np.float64)
+    rc = _load().oracle_mul_mat_rmsnorm(_type(t), blocks.ctypes.data, M, K, X.ctypes.data,
+                                        gamma.ctypes.data, float(eps), N, Y.ctypes.data,
+                                        wrow.ctypes.data, xhat.ctypes.data)
+    if rc:
+        raise ValueError("oracle_mul_mat_rmsnorm rejected its arguments")
+    return Y
+
+
+def mul_mat_swiglu(t, gate, up, M: int, K: int, X) -> np.ndarray:
+    """H (N x M fp32) = Swish(X . Wgate_hat^T) * (X . Wup_hat^T), Swish(z) = z / (1 + e^-z)
+    ("Development Guide ...", section 4.4), both sums, Swish and the product in fp64."""
+    gate = np.ascontiguousarray(gate, dtype=np.uint8)
+    up = np.ascontiguousarray(up, dtype=np.uint8)
+    X = _f32(X)
+    if X.ndim == 1:
+        X = X.reshape(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K or gate.size != M * row_bytes(t, K) or up.size != gate.size:
+        raise ValueError("shape mismatch")
+    H = np.empty((N, M), dtype=np.float32)
+    wrow = np.empty(max(2 * K, 1), dtype=np.float32)
+    rc = _load().oracle_mul_mat_swiglu(_type(t), gate.ctypes.data, up.ctypes.data, M, K,
+                                       X.ctypes.data, N, H.ctypes.data, wrow.ctypes.data)
+    if rc:
+        raise ValueError("oracle_mul_mat_swiglu rejected its arguments")
+    return H
+
+
+def _rows_of(t, blocks, M: int, K: int, rows) -> np.ndarray:
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(M, row_bytes(t, K))
+    return np.ascontiguousarray(b[np.asarray(rows, dtype=np.int64)])
+
+
+def mul_mat_rmsnorm_rows(t, blocks, M: int, K: int, X, gamma, eps: float, rows) -> np.ndarray:
+    """mul_mat_rmsnorm on the selected rows only (sampled checks of large problems)."""
+    return mul_mat_rmsnorm(t, _rows_of(t, blocks, M, K, rows), len(rows), K, X, gamma, eps)
+
+
+def mul_mat_swiglu_rows(t, gate, up, M: int, K: int, X, rows) -> np.ndarray:
+    """mul_mat_swiglu on the selected rows only."""
+    return mul_mat_swiglu(t, _rows_of(t, gate, M, K, rows), _rows_of(t, up, M, K, rows),
+                          len(rows), K, X)

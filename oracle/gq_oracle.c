@@ -21,6 +21,9 @@
  *   - Dequantize right after the load, then multiply-accumulate with fp32 activations
  *     ("Development Guide ...", section 6.2, the load / unpack / dequantize / FMA flow;
  *     "No Python! ...", section 9).
+ *   - The two adjacent steps of a transformer layer fused with the product: RMSNorm of
+ *     the activations ahead of it ("Development Guide ...", section 4.1) and the SwiGLU
+ *     of the gate and up projections after it (the same guide, section 4.4).
  *   - The product itself: C_ij = sum_k A_ik B_kj ("No Python! ...", section 6), realised
  *     as Y[n][m] = sum_k What[m][k] * X[n][k] -- the layout of the cuBLAS call in
  *     section 7.2 of the same article (W is M x K row-major, X is N x K row-major,
@@ -303,6 +306,73 @@ int oracle_mul_mat_q8x(int type, const uint8_t* blocks, int64_t M, int64_t K,
                 acc += dw * dx * (double)sum;
             }
             Y[n * M + m] = (float)acc;
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* mul_mat of the RMS-normalized activations ("Development Guide for Small AI Models   */
+/* (TinyLLaMA, etc.) Using C++", section 4.1):                                          */
+/*     RMSNorm(x) = x / sqrt((1/d) sum_i x_i^2 + eps) (.) gamma,   d = K,              */
+/*     Y[n][m] = (float) sum_k (double) What[m][k] * xhat[n][k],                        */
+/* with xhat computed in fp64 (sum of squares in increasing k, then the square root    */
+/* and the division) and never rounded; one rounding at the end. `wrow` holds one      */
+/* dequantized row (K floats); `xhat` is caller space for one normalized row (K).      */
+/* ---------------------------------------------------------------------------------- */
+int oracle_mul_mat_rmsnorm(int type, const uint8_t* blocks, int64_t M, int64_t K,
+                           const float* X, const float* gamma, double eps, int64_t N,
+                           float* Y, float* wrow, double* xhat)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K % 32 != 0 || M < 0 || K <= 0 || N < 0) return -1;
+    const int64_t nb = K / 32;
+    for (int64_t n = 0; n < N; ++n) {
+        const float* x = X + n * K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) ss += (double)x[k] * (double)x[k];
+        const double rms = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k) xhat[k] = (double)x[k] / rms * (double)gamma[k];
+        for (int64_t m = 0; m < M; ++m) {
+            for (int64_t b = 0; b < nb; ++b)
+                dequantize_block(type, blocks + (m * nb + b) * bb, wrow + b * 32);
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += (double)wrow[k] * xhat[k];
+            Y[n * M + m] = (float)acc;
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------- */
+/* The gated feed-forward activation ("Development Guide ...", section 4.4):           */
+/*     SwiGLU(x) = Swish(x W_gate) (x) (x W_up),   Swish(z) = z / (1 + e^-z),           */
+/* in this library's layout H[n][m] = Swish(g) * u with g = sum_k Wgate_hat[m][k] x[k]  */
+/* and u = sum_k Wup_hat[m][k] x[k], each an fp64 sum in increasing k; Swish and the    */
+/* product in fp64, one rounding at the end. Both weights: M x K blocks of `type`.     */
+/* `wrow` is caller space for two dequantized rows (2 K floats).                        */
+/* ---------------------------------------------------------------------------------- */
+int oracle_mul_mat_swiglu(int type, const uint8_t* gate, const uint8_t* up, int64_t M,
+                          int64_t K, const float* X, int64_t N, float* H, float* wrow)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0 || N < 0) return -1;
+    const int64_t nb = K / 32;
+    float* wg = wrow;
+    float* wu = wrow + K;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < nb; ++b) {
+            dequantize_block(type, gate + (m * nb + b) * bb, wg + b * 32);
+            dequantize_block(type, up + (m * nb + b) * bb, wu + b * 32);
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            const float* x = X + n * K;
+            double g = 0.0, u = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                g += (double)wg[k] * (double)x[k];
+                u += (double)wu[k] * (double)x[k];
+            }
+            H[n * M + m] = (float)(g / (1.0 + exp(-g)) * u);
         }
     }
     return 0;

@@ -37,6 +37,18 @@ MUTANTS = {
     "q8x_scale": ("acc += dw * dx * (double)sum;", "acc += dw * (double)sum;"),
     "q8x_x_block": ("const uint8_t* xb = xq + (n * nb + b) * 34;",
                     "const uint8_t* xb = xq + (n * nb + (nb - 1 - b)) * 34;"),
+    "rmsnorm_sum_not_mean": ("const double rms = sqrt(ss / (double)K + eps);",
+                             "const double rms = sqrt(ss + eps);"),
+    "rmsnorm_eps_outside": ("const double rms = sqrt(ss / (double)K + eps);",
+                            "const double rms = sqrt(ss / (double)K) + eps;"),
+    "rmsnorm_no_gamma": ("xhat[k] = (double)x[k] / rms * (double)gamma[k];",
+                         "xhat[k] = (double)x[k] / rms;"),
+    "swiglu_exp_sign": ("H[n * M + m] = (float)(g / (1.0 + exp(-g)) * u);",
+                        "H[n * M + m] = (float)(g / (1.0 + exp(g)) * u);"),
+    "swiglu_no_up": ("H[n * M + m] = (float)(g / (1.0 + exp(-g)) * u);",
+                     "H[n * M + m] = (float)(g / (1.0 + exp(-g)));"),
+    "swiglu_roles_swapped": ("H[n * M + m] = (float)(g / (1.0 + exp(-g)) * u);",
+                             "H[n * M + m] = (float)(u / (1.0 + exp(-u)) * g);"),
 }
 
 

@@ -384,6 +384,105 @@ def test_mul_mat_q8x_exact_when_x_is_representable(oracle_mod):
 # ------------------------------------------------------------------------------------
 # Figures the pages print
 # ------------------------------------------------------------------------------------
+# ------------------------------------------------------------------------------------
+# Fused adjacent steps: RMSNorm ahead of the product, SwiGLU after it
+# ("Development Guide for Small AI Models (TinyLLaMA, etc.) Using C++", sections 4.1, 4.4)
+# ------------------------------------------------------------------------------------
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_rmsnorm_one_hot_closed_form(oracle_mod, t):
+    """eps = 0, gamma = 1, x = a e_k: mean(x^2) = a^2 / K, so RMSNorm(x) = sign(a) sqrt(K) e_k
+    and Y[m] = sign(a) sqrt(K) What[m][k], within an fp32 rounding."""
+    M, K = 6, 96
+    W = workloads.weights(M, K, seed=81).numpy()
+    q = oracle_mod.quantize(t, W)
+    wh = oracle_mod.dequantize(t, q, M, K).astype(np.float64)
+    gamma = np.ones(K, np.float32)
+    for k, a in [(0, 1.0), (17, -3.5), (95, 0.002)]:
+        X = np.zeros((1, K), np.float32)
+        X[0, k] = a
+        Y = oracle_mod.mul_mat_rmsnorm(t, q, M, K, X, gamma, 0.0)[0].astype(np.float64)
+        ref = np.sign(a) * np.sqrt(K) * wh[:, k]
+        assert np.all(np.abs(Y - ref) <= np.abs(ref) * 2.0 ** -23), (k, a)
+
+
+def test_rmsnorm_scale_invariant_and_gamma_linear(oracle_mod):
+    """eps = 0: scaling X by a power of two leaves Y unchanged bit for bit; scaling gamma by
+    a power of two scales Y by it exactly."""
+    M, N, K = 9, 3, 256
+    W = workloads.weights(M, K, seed=82).numpy()
+    X = workloads.activations(N, K, seed=83).numpy()
+    q = oracle_mod.quantize("q4_0", W)
+    gamma = (1.0 + 0.1 * np.random.default_rng(84).standard_normal(K)).astype(np.float32)
+    Y = oracle_mod.mul_mat_rmsnorm("q4_0", q, M, K, X, gamma, 0.0)
+    for s in (8.0, 1.0 / 16.0):
+        assert np.array_equal(oracle_mod.mul_mat_rmsnorm("q4_0", q, M, K, X * np.float32(s), gamma, 0.0), Y)
+    assert np.array_equal(oracle_mod.mul_mat_rmsnorm("q4_0", q, M, K, X, gamma * np.float32(2.0), 0.0),
+                          Y * np.float32(2.0))
+
+
+def test_rmsnorm_eps_dominates(oracle_mod):
+    """eps far above mean(x^2): RMSNorm(x) -> x * gamma / sqrt(eps), so Y equals the pinned
+    mul_mat of X * gamma divided by sqrt(eps) to within the neglected mean(x^2) / eps."""
+    M, N, K = 5, 2, 128
+    W = workloads.weights(M, K, seed=85).numpy()
+    X = workloads.activations(N, K, seed=86).numpy()
+    q = oracle_mod.quantize("q8_0", W)
+    gamma = np.linspace(0.5, 1.5, K, dtype=np.float32)
+    eps = 1.0e12
+    Y = oracle_mod.mul_mat_rmsnorm("q8_0", q, M, K, X, gamma, eps).astype(np.float64)
+    ref = oracle_mod.mul_mat("q8_0", q, M, K, X * gamma).astype(np.float64) / np.sqrt(eps)
+    assert np.all(np.abs(Y - ref) <= np.abs(ref) * 1e-6 + 1e-30)
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_swiglu_one_hot_closed_form(oracle_mod, t):
+    """x = a e_k: g = What_gate[m][k] a and u = What_up[m][k] a exactly, so
+    H[m] = g / (1 + e^-g) * u (computed here with Python's math, in fp64)."""
+    import math
+    M, K = 7, 64
+    qg = oracle_mod.quantize(t, workloads.weights(M, K, seed=87).numpy())
+    qu = oracle_mod.quantize(t, workloads.weights(M, K, seed=88).numpy())
+    wg = oracle_mod.dequantize(t, qg, M, K).astype(np.float64)
+    wu = oracle_mod.dequantize(t, qu, M, K).astype(np.float64)
+    for k, a in [(3, 1.0), (40, -250.0), (63, 900.0)]:
+        X = np.zeros((1, K), np.float32)
+        X[0, k] = a
+        H = oracle_mod.mul_mat_swiglu(t, qg, qu, M, K, X)[0].astype(np.float64)
+        for m in range(M):
+            g, u = wg[m, k] * a, wu[m, k] * a
+            ref = g / (1.0 + math.exp(-g)) * u
+            assert abs(H[m] - ref) <= abs(ref) * 2.0 ** -23 + 1e-45, (k, a, m)
+
+
+def test_swiglu_zero_input_and_roles(oracle_mod):
+    """X = 0 gives H = 0; with the same matrix as gate and up, H = Swish(g) g against the
+    pinned mul_mat, and exchanging gate and up changes the result."""
+    M, N, K = 6, 2, 96
+    qg = oracle_mod.quantize("q4_0", workloads.weights(M, K, seed=89).numpy())
+    qu = oracle_mod.quantize("q4_0", workloads.weights(M, K, seed=90).numpy())
+    assert not oracle_mod.mul_mat_swiglu("q4_0", qg, qu, M, K, np.zeros((N, K), np.float32)).any()
+    X = workloads.activations(N, K, seed=91).numpy() * np.float32(10.0)
+    g = oracle_mod.mul_mat("q4_0", qg, M, K, X).astype(np.float64)
+    H = oracle_mod.mul_mat_swiglu("q4_0", qg, qg, M, K, X).astype(np.float64)
+    ref = g / (1.0 + np.exp(-g)) * g
+    assert np.all(np.abs(H - ref) <= np.abs(ref) * 1e-6 + 1e-30)
+    assert not np.array_equal(oracle_mod.mul_mat_swiglu("q4_0", qg, qu, M, K, X),
+                              oracle_mod.mul_mat_swiglu("q4_0", qu, qg, M, K, X))
+
+
+def test_fused_rows_subsets(oracle_mod):
+    M, N, K = 20, 2, 128
+    qg = oracle_mod.quantize("q4_0", workloads.weights(M, K, seed=92).numpy())
+    qu = oracle_mod.quantize("q4_0", workloads.weights(M, K, seed=93).numpy())
+    X = workloads.activations(N, K, seed=94).numpy()
+    gamma = np.ones(K, np.float32)
+    rows = [0, 19, 7]
+    assert np.array_equal(oracle_mod.mul_mat_rmsnorm_rows("q4_0", qg, M, K, X, gamma, 1e-5, rows),
+                          oracle_mod.mul_mat_rmsnorm("q4_0", qg, M, K, X, gamma, 1e-5)[:, rows])
+    assert np.array_equal(oracle_mod.mul_mat_swiglu_rows("q4_0", qg, qu, M, K, X, rows),
+                          oracle_mod.mul_mat_swiglu("q4_0", qg, qu, M, K, X)[:, rows])
+
+
 def test_page_facts():
     import oracle
     facts = json.load(open(GOLDEN))
