@@ -35,7 +35,8 @@ EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0
            "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
            "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched",
            "gq_mul_mat_batched_workspace_size", "gq_mul_mat_batched_ws", "gq_mul_mat_q8x",
-           "gq_mul_mat_q8x_batched", "gq_get_last_error",
+           "gq_mul_mat_q8x_batched", "gq_mul_mat_rmsnorm", "gq_mul_mat_swiglu",
+           "gq_get_last_error",
            "gq_selftest_wait_timeout", "gq_status_string")
 
 
@@ -75,6 +76,11 @@ def load(path: str = LIB_PATH):
     L.gq_mul_mat_batched_ws.restype = ctypes.c_int
     L.gq_mul_mat_q8x.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp, vp]
     L.gq_mul_mat_q8x.restype = ctypes.c_int
+    L.gq_mul_mat_rmsnorm.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, ctypes.c_float, i64,
+                                     vp, vp]
+    L.gq_mul_mat_rmsnorm.restype = ctypes.c_int
+    L.gq_mul_mat_swiglu.argtypes = [vp, vp, ctypes.c_int, i64, i64, vp, i64, vp, vp]
+    L.gq_mul_mat_swiglu.restype = ctypes.c_int
     L.gq_mul_mat_q8x_batched.argtypes = [ctypes.POINTER(Problem), i32, ctypes.c_int, i64, vp]
     L.gq_mul_mat_q8x_batched.restype = ctypes.c_int
     L.gq_get_last_error.argtypes, L.gq_get_last_error.restype = [vp], ctypes.c_int
@@ -262,6 +268,41 @@ def mul_mat_q8x(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
     _check(lib.gq_mul_mat_q8x(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
                               _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
                               _stream(stream)), "gq_mul_mat_q8x")
+    return out
+
+
+def mul_mat_rmsnorm(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
+                    gamma: torch.Tensor, eps: float, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Y (N, M) = RMSNorm(X) . What^T, RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gamma."""
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K or gamma.numel() != K:
+        raise ValueError("X must be (N, K) and gamma (K,)")
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    _check(lib.gq_mul_mat_rmsnorm(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
+                                  _dev(X, torch.float32, "X"), _dev(gamma, torch.float32, "gamma"),
+                                  float(eps), N, _dev(out, torch.float32, "Y"), _stream(stream)),
+           "gq_mul_mat_rmsnorm")
+    return out
+
+
+def mul_mat_swiglu(gate: torch.Tensor, up: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """H (N, M) = Swish(X . Wgate_hat^T) * (X . Wup_hat^T), Swish(z) = z / (1 + e^-z)."""
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    N = X.shape[0]
+    if X.shape[1] != K:
+        raise ValueError("X must be (N, K)")
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    _check(lib.gq_mul_mat_swiglu(_dev(gate, torch.uint8, "W_gate"), _dev(up, torch.uint8, "W_up"),
+                                 _type(t), M, K, _dev(X, torch.float32, "X"), N,
+                                 _dev(out, torch.float32, "H"), _stream(stream)),
+           "gq_mul_mat_swiglu")
     return out
 
 

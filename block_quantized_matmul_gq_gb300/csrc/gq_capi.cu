@@ -3,6 +3,7 @@
 // bounded wait runs out.
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -322,6 +323,64 @@ gq_status check_q8x(const void* W, gq_type t, int64_t M, int64_t K, const float*
 }  // namespace
 
 extern "C" {
+
+gq_status gq_mul_mat_rmsnorm(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                             const float* X, const float* gamma, float eps, int64_t N,
+                             float* Y, void* stream) {
+    bool empty = false;
+    gq_status st = check_problem(W_blocks, t, M, K, X, N, Y, &empty);
+    if (st != GQ_OK) return st;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return GQ_ERR_SHAPE;
+    if (empty) return GQ_OK;
+    if (K == 0) return GQ_ERR_SHAPE;   // the mean over no elements is undefined
+    if (!gamma) return GQ_ERR_NULL;
+    if (!aligned(gamma, 4)) return GQ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
+    p.gamma = gamma;
+    p.eps = eps;
+    if (N <= 2 && gq::fused_decode_eligible(t, p))   // normalized inside the decode kernel
+        return from_cuda(gq::launch_mul_mat_fused(t, p, N, s));
+    // Otherwise: Xhat = RMSNorm(X) into library workspace, then the plain product on it.
+    const size_t xb = (static_cast<size_t>(N * K) * 4 + 255) / 256 * 256;
+    const size_t down = gq_mul_mat_workspace_size(t, M, K, N);
+    void* w = nullptr;
+    if (internal_workspace(s, xb + down, &w) != cudaSuccess) return GQ_ERR_CUDA;
+    float* xhat = static_cast<float*>(w);
+    cudaError_t e = gq::launch_rmsnorm_x(X, gamma, eps, N, K, xhat, s);
+    if (e != cudaSuccess) return GQ_ERR_CUDA;
+    const gq::MatProblem q{static_cast<const uint8_t*>(W_blocks), xhat, Y, M, K};
+    return run_one(t, q, N, static_cast<uint8_t*>(w) + xb, down, s);
+}
+
+gq_status gq_mul_mat_swiglu(const void* W_gate, const void* W_up, gq_type t, int64_t M,
+                            int64_t K, const float* X, int64_t N, float* H, void* stream) {
+    bool empty = false;
+    gq_status st = check_problem(W_gate, t, M, K, X, N, H, &empty);
+    if (st != GQ_OK || empty) return st;
+    if (K > 0 && !W_up) return GQ_ERR_NULL;
+    if (K > 0 && !aligned(W_up, 16)) return GQ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(H, 0, sizeof(float) * N * M, s));   // Swish(0) * 0
+    gq::MatProblem p{static_cast<const uint8_t*>(W_gate), X, H, M, K};
+    p.W2 = static_cast<const uint8_t*>(W_up);
+    if (N <= 2 && gq::fused_decode_eligible(t, p))   // gate/up row pairs in the decode kernel
+        return from_cuda(gq::launch_mul_mat_fused(t, p, N, s));
+    // Otherwise: G and U into library workspace by two plain products, then Swish(G) * U.
+    const size_t yb = (static_cast<size_t>(N * M) * 4 + 255) / 256 * 256;
+    const size_t down = gq_mul_mat_workspace_size(t, M, K, N);
+    void* w = nullptr;
+    if (internal_workspace(s, 2 * yb + down, &w) != cudaSuccess) return GQ_ERR_CUDA;
+    float* G = static_cast<float*>(w);
+    float* U = reinterpret_cast<float*>(static_cast<uint8_t*>(w) + yb);
+    void* dws = static_cast<uint8_t*>(w) + 2 * yb;
+    const gq::MatProblem pg{static_cast<const uint8_t*>(W_gate), X, G, M, K};
+    const gq::MatProblem pu{static_cast<const uint8_t*>(W_up), X, U, M, K};
+    st = run_one(t, pg, N, dws, down, s);
+    if (st == GQ_OK) st = run_one(t, pu, N, dws, down, s);
+    if (st != GQ_OK) return st;
+    return from_cuda(gq::launch_swiglu(G, U, H, N * M, s));
+}
 
 gq_status gq_mul_mat_q8x(const void* W_blocks, gq_type t, int64_t M, int64_t K, const float* X,
                          int64_t N, float* Y, void* stream) {

@@ -120,6 +120,14 @@ struct GemvProb {
     int64_t cost_begin;   // weight of all earlier problems
     int32_t C;            // chunks per row
     int32_t K;
+    // Fused forms. gamma != NULL: X is RMS-normalized per token (x / sqrt(mean x^2 + eps)
+    // * gamma) as it is prepared. W2 != NULL: gate/up pairs -- the row sequence has M =
+    // 2 M_h rows, row 2m from W (gate m) and row 2m + 1 from W2 (up m), and Y (rows of
+    // M_h) receives Swish(gate) * up.
+    const uint8_t* W2;
+    const float* gamma;
+    float eps;
+    int32_t pad_;
 };
 
 template <int kMaxProbs>
@@ -148,6 +156,7 @@ __device__ void row_at_cost(const GemvParams<kMaxProbs>& P, int64_t cost, int& p
     while (p + 1 < P.count && P.p[p + 1].cost_begin <= cost) ++p;
     const int64_t off = cost - P.p[p].cost_begin;
     r = off <= 0 ? 0 : (off + P.p[p].row_cost - 1) / P.p[p].row_cost;
+    if (P.p[p].W2 != nullptr) r = (r + 1) & ~int64_t(1);   // gate/up pairs stay together
     if (r >= P.p[p].M) {
         ++p;
         r = 0;
@@ -262,20 +271,58 @@ __device__ __forceinline__ uint32_t u16_at(const uint32_t* r, int byte_off) {
     return (byte_off & 3) ? (r[w] >> 16) : (r[w] & 0xFFFFu);
 }
 
+// Swish(z) = z / (1 + e^-z) ("Development Guide for Small AI Models (TinyLLaMA, etc.)
+// Using C++", section 4.4).
+__device__ __forceinline__ float swish(float z) { return z / (1.0f + expf(-z)); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
 
+// RMSNorm scale of each token of the problem ("Development Guide for Small AI Models
+// (TinyLLaMA, etc.) Using C++", section 4.1): inv[t] = 1 / sqrt(mean_k x^2 + eps). The sum
+// of squares runs in a fixed order (thread strides, a fixed shuffle tree, then the warps
+// in order through `scratch`, kWarps * kNT floats), so it does not depend on timing. All
+// threads of the CTA call it.
+template <int kNT>
+__device__ void rms_scales(const GemvProb& pr, int n_tok, float* scratch, float (&inv)[kNT]) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        float ss = 0.0f;
+        if (t < n_tok) {
+            const float* x = pr.X + static_cast<int64_t>(t) * pr.K;
+            for (int k = threadIdx.x; k < pr.K; k += kThreads) ss = fmaf(x[k], x[k], ss);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        if (lane == 0) scratch[warp * kNT + t] = ss;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        float ss = 0.0f;
+        for (int w = 0; w < kWarps; ++w) ss += scratch[w * kNT + t];
+        inv[t] = 1.0f / sqrtf(ss / static_cast<float>(pr.K) + pr.eps);
+    }
+    __syncthreads();   // scratch is the k-split buffer of the segment that follows
+}
+
 // X (n_tok x K fp32) -> x16 records, one per (token, chunk column). Warp per record.
-template <int kType, int kNT>
-__device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbuf) {
+// With kNorm (pr.gamma set), each x is first RMS-normalized: x * inv_rms[t] * gamma[k].
+template <int kType, int kNT, bool kNorm>
+__device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbuf,
+                          float* scratch) {
     using G = Geo<kType>;
     constexpr int kPerLane = G::kWPC / 32;   // 8 (Q4_0) or 4 (Q8_0) elements
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int C = pr.C;
+    float inv[kNT];
+    if constexpr (kNorm) rms_scales<kNT>(pr, n_tok, scratch, inv);
     for (int idx = warp; idx < kNT * C; idx += kWarps) {
         const int t = idx / C;
         const int col = idx - t * C;
@@ -291,6 +338,22 @@ __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbu
                 v[4 * i + 1] = f.y;
                 v[4 * i + 2] = f.z;
                 v[4 * i + 3] = f.w;
+            }
+            if constexpr (kNorm) {
+                float inv_t = inv[0];   // inv[t], kept in registers
+#pragma unroll
+                for (int tt = 1; tt < kNT; ++tt)
+                    if (tt == t) inv_t = inv[tt];
+                const float4* gsrc =
+                    reinterpret_cast<const float4*>(pr.gamma + col * G::kWPC + lane * kPerLane);
+#pragma unroll
+                for (int i = 0; i < kPerLane / 4; ++i) {
+                    const float4 gm = __ldg(gsrc + i);
+                    v[4 * i] = v[4 * i] * inv_t * gm.x;
+                    v[4 * i + 1] = v[4 * i + 1] * inv_t * gm.y;
+                    v[4 * i + 2] = v[4 * i + 2] * inv_t * gm.z;
+                    v[4 * i + 3] = v[4 * i + 3] * inv_t * gm.w;
+                }
             }
         } else {
 #pragma unroll
@@ -609,9 +672,12 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xre
 
 // kXM selects the activation form: 0 = 16-bit block fixed point (exact mul_mat within a
 // proven bound), 1 = Q8_0-quantized activations (the quantized-activation product).
-template <int kType, int kNT, int kMaxProbs, int kXM>
+template <int kType, int kNT, int kMaxProbs, int kXM, int kFuse>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
+    // kFuse: 0 plain, 1 RMSNorm of X in the preparation, 2 gate/up row pairs (Swish * up)
+    constexpr bool kPair = kFuse == 2;
+    constexpr bool kNorm = kFuse == 1;
     using G = Geo<kType>;
     constexpr int kRec = xrec_bytes<kType, kXM>();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -659,7 +725,17 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
         const uint8_t* src = pr.W + row0 * pr.row_bytes + static_cast<int64_t>(c0) * G::kChunkBytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, row_copy * rows);
-            if (pr.C <= kLanesPerRow) {
+            if constexpr (kPair) {
+                // row 2m + h of the sequence is row m of the gate (h = 0) or up (h = 1) matrix
+                for (int r = 0; r < rows; ++r) {
+                    const int64_t q = row0 + r;
+                    const uint8_t* base_w = (q & 1) ? pr.W2 : pr.W;
+                    bulk_g2s_evict_first(dst + r * G::kRowStride,
+                                         base_w + (q >> 1) * pr.row_bytes +
+                                             static_cast<int64_t>(c0) * G::kChunkBytes,
+                                         row_copy, bar);
+                }
+            } else if (pr.C <= kLanesPerRow) {
                 bulk_g2s_evict_first(dst, src, row_copy * rows, bar);
             } else {
                 for (int r = 0; r < rows; ++r)
@@ -685,7 +761,7 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
         if (__syncthreads_or(timed_out)) break;   // previous segment done everywhere
         const GemvProb& pr = P.p[seg.p];
         if constexpr (kXM == 0)
-            prepare_x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
+            prepare_x<kType, kNT, kNorm>(pr, P.n_tok, P.max_c, xbuf, red);
         else
             prepare_x_q8x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
         __syncthreads();
@@ -706,7 +782,8 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
                 }
                 const int col = kLanesPerRow * cs + lc;
                 // Whole-row stages hold rows at their global stride; others at kRowStride.
-                const int rs = pr.C <= kLanesPerRow ? static_cast<int>(pr.row_bytes) : G::kRowStride;
+                const int rs = (!kPair && pr.C <= kLanesPerRow) ? static_cast<int>(pr.row_bytes)
+                                                                 : G::kRowStride;
                 if (rrow < rows && col < pr.C) {
                     const uint8_t* raw = ring + s * G::kStageBytes + rrow * rs + lc * G::kChunkBytes;
                     if constexpr (kXM == 0)
@@ -725,11 +802,26 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
                 for (int o = 1; o < kLanesPerRow; o <<= 1)
                     acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
             }
-            if (lc == 0 && rrow < rows) {
-                if (sp.ksplit == 1) {
+            if constexpr (kPair) {
+                // The up row's sums sit kLanesPerRow lanes above the gate row's.
+                float up[kNT];
+#pragma unroll
+                for (int t = 0; t < kNT; ++t)
+                    up[t] = __shfl_down_sync(0xFFFFFFFFu, acc[t], kLanesPerRow);
+                if (sp.ksplit == 1 && lc == 0 && (rrow & 1) == 0 && rrow < rows) {
+                    const int64_t mh = pr.M >> 1;
 #pragma unroll
                     for (int t = 0; t < kNT; ++t)
-                        if (t < P.n_tok) pr.Y[t * pr.M + row0 + rrow] = acc[t];
+                        if (t < P.n_tok) pr.Y[t * mh + ((row0 + rrow) >> 1)] = swish(acc[t]) * up[t];
+                }
+            }
+            if (lc == 0 && rrow < rows) {
+                if (sp.ksplit == 1) {
+                    if constexpr (!kPair) {
+#pragma unroll
+                        for (int t = 0; t < kNT; ++t)
+                            if (t < P.n_tok) pr.Y[t * pr.M + row0 + rrow] = acc[t];
+                    }
                 } else {
 #pragma unroll
                     for (int t = 0; t < kNT; ++t) red[(item * kTileRows + rrow) * kNT + t] = acc[t];
@@ -739,17 +831,35 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
         if (sp.ksplit > 1) {
             // Sum the k-groups of each row in group order (deterministic).
             if (__syncthreads_or(timed_out)) break;
-            const int n_out = sp.ntiles * kTileRows * kNT;
-            for (int idx = threadIdx.x; idx < n_out; idx += kThreads) {
-                const int t = idx % kNT;
-                const int rr = (idx / kNT) % kTileRows;
-                const int tile = idx / (kNT * kTileRows);
-                const int64_t row = seg.rb + static_cast<int64_t>(tile) * kTileRows + rr;
-                if (row >= seg.re || t >= P.n_tok) continue;
-                float v = 0.0f;
-                for (int kg = 0; kg < sp.ksplit; ++kg)
-                    v += red[((tile * sp.ksplit + kg) * kTileRows + rr) * kNT + t];
-                pr.Y[t * pr.M + row] = v;
+            if constexpr (kPair) {
+                // one output per (gate, up) row pair: Swish(gate) * up
+                const int n_out = sp.ntiles * (kTileRows / 2) * kNT;
+                for (int idx = threadIdx.x; idx < n_out; idx += kThreads) {
+                    const int t = idx % kNT;
+                    const int rr = 2 * ((idx / kNT) % (kTileRows / 2));
+                    const int tile = idx / (kNT * (kTileRows / 2));
+                    const int64_t row = seg.rb + static_cast<int64_t>(tile) * kTileRows + rr;
+                    if (row >= seg.re || t >= P.n_tok) continue;
+                    float g = 0.0f, u = 0.0f;
+                    for (int kg = 0; kg < sp.ksplit; ++kg) {
+                        g += red[((tile * sp.ksplit + kg) * kTileRows + rr) * kNT + t];
+                        u += red[((tile * sp.ksplit + kg) * kTileRows + rr + 1) * kNT + t];
+                    }
+                    pr.Y[t * (pr.M >> 1) + (row >> 1)] = swish(g) * u;
+                }
+            } else {
+                const int n_out = sp.ntiles * kTileRows * kNT;
+                for (int idx = threadIdx.x; idx < n_out; idx += kThreads) {
+                    const int t = idx % kNT;
+                    const int rr = (idx / kNT) % kTileRows;
+                    const int tile = idx / (kNT * kTileRows);
+                    const int64_t row = seg.rb + static_cast<int64_t>(tile) * kTileRows + rr;
+                    if (row >= seg.re || t >= P.n_tok) continue;
+                    float v = 0.0f;
+                    for (int kg = 0; kg < sp.ksplit; ++kg)
+                        v += red[((tile * sp.ksplit + kg) * kTileRows + rr) * kNT + t];
+                    pr.Y[t * pr.M + row] = v;
+                }
             }
         }
     }
@@ -840,9 +950,9 @@ cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
     return e;
 }
 
-template <int kType, int kNT, int kMaxProbs, int kXM>
+template <int kType, int kNT, int kMaxProbs, int kXM, int kFuse>
 cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
-    auto kernel = gemv_stream_kernel<kType, kNT, kMaxProbs, kXM>;
+    auto kernel = gemv_stream_kernel<kType, kNT, kMaxProbs, kXM, kFuse>;
     const int64_t smem = stream_smem_bytes<kType, kXM>(kNT, P.max_c);
     if (smem > info->max_smem_optin) return cudaErrorInvalidValue;   // see stream_eligible
     cudaError_t e = ensure_smem(kernel, info->device, smem);
@@ -867,17 +977,17 @@ cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cu
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
 }
 
-template <int kType, int kMaxProbs, int kXM>
+template <int kType, int kMaxProbs, int kXM, int kFuse>
 cudaError_t launch_stream_nt(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
     switch (P.n_tok) {
-        case 1: return launch_stream_t<kType, 1, kMaxProbs, kXM>(P, info, s);
-        case 2: return launch_stream_t<kType, 2, kMaxProbs, kXM>(P, info, s);
-        case 3: return launch_stream_t<kType, 3, kMaxProbs, kXM>(P, info, s);
-        default: return launch_stream_t<kType, 4, kMaxProbs, kXM>(P, info, s);
+        case 1: return launch_stream_t<kType, 1, kMaxProbs, kXM, kFuse>(P, info, s);
+        case 2: return launch_stream_t<kType, 2, kMaxProbs, kXM, kFuse>(P, info, s);
+        case 3: return launch_stream_t<kType, 3, kMaxProbs, kXM, kFuse>(P, info, s);
+        default: return launch_stream_t<kType, 4, kMaxProbs, kXM, kFuse>(P, info, s);
     }
 }
 
-template <int kMaxProbs, int kXM = 0>
+template <int kMaxProbs, int kXM = 0, int kFuse = 0>
 cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t tok0,
                           int n_tok, const DeviceInfo* info, cudaStream_t s) {
     GemvParams<kMaxProbs> P{};
@@ -894,7 +1004,10 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
         g.W = probs[i].W;
         g.X = probs[i].X + tok0 * probs[i].K;
         g.Y = probs[i].Y + tok0 * probs[i].M;
-        g.M = probs[i].M;
+        g.W2 = probs[i].W2;
+        g.gamma = probs[i].gamma;
+        g.eps = probs[i].eps;
+        g.M = kFuse == 2 ? 2 * probs[i].M : probs[i].M;   // gate/up pairs: two rows per output
         g.K = static_cast<int32_t>(probs[i].K);
         g.C = static_cast<int32_t>(probs[i].K / wpc);
         g.row_bytes = static_cast<int64_t>(g.C) * cb;
@@ -907,8 +1020,8 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
     P.total_bytes = bytes;
     P.total_cost = cost;
     P.max_c = max_c;
-    if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs, kXM>(P, info, s);
-    return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs, kXM>(P, info, s);
+    if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs, kXM, kFuse>(P, info, s);
+    return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs, kXM, kFuse>(P, info, s);
 }
 
 cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_tok,
@@ -1008,6 +1121,37 @@ cudaError_t launch_mul_mat_q8x(gq_type t, const MatProblem* probs, int count, in
             e = launch_stream<1, 1>(t, probs, count, tok0, n_tok, info, s);
         else
             e = launch_stream<GQ_MAX_BATCH, 1>(t, probs, count, tok0, n_tok, info, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gq
+
+namespace gq {
+
+// Fused forms on the CUDA-core decode kernel: RMSNorm of X in the activation preparation
+// (p.gamma) and the gate/up pair with Swish(gate) * up written directly (p.W2). Shapes the
+// streaming kernel takes only; the caller composes the other shapes from plain kernels.
+bool fused_decode_eligible(gq_type t, const MatProblem& p) {
+    DeviceInfo* info = nullptr;
+    if (current_device_info(&info) != cudaSuccess) return false;
+    if (p.gamma && reinterpret_cast<uintptr_t>(p.gamma) % 16 != 0) return false;   // float4
+    if (p.W2 && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0) return false;         // bulk copies
+    return stream_shape_ok(p) && stream_fits(t, p, 1, info);
+}
+
+cudaError_t launch_mul_mat_fused(gq_type t, const MatProblem& p, int64_t N, cudaStream_t s) {
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    int64_t step = 0;
+    for (int64_t tok0 = 0; tok0 < N; tok0 += step) {
+        int n_tok = static_cast<int>(std::min<int64_t>(kMaxTok, N - tok0));
+        while (n_tok > 1 && !stream_fits(t, p, n_tok, info)) --n_tok;
+        step = n_tok;
+        e = p.W2 ? launch_stream<1, 0, 2>(t, &p, 1, tok0, n_tok, info, s)
+                 : launch_stream<1, 0, 1>(t, &p, 1, tok0, n_tok, info, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -23,6 +23,11 @@ struct MatProblem {
     float* Y;
     int64_t M;
     int64_t K;
+    // Fused forms (CUDA-core decode only): RMSNorm of X ahead of the product when gamma is
+    // set; Swish(X W^T) * (X W2^T) into Y when W2 (the up matrix) is set.
+    const uint8_t* W2 = nullptr;
+    const float* gamma = nullptr;
+    float eps = 0.0f;
 };
 
 // Per-device facts, looked up once per device.
@@ -43,6 +48,17 @@ cudaError_t launch_dequantize(gq_type t, const uint8_t* blocks, int64_t n_elems,
 // share type t and N tokens.
 cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_t N,
                            cudaStream_t s);
+
+// Fused decode forms on the CUDA-core decode kernel (see MatProblem::gamma, ::W2): whether
+// the streaming kernel takes this shape, and the launch (any N, in passes of up to 4).
+bool fused_decode_eligible(gq_type t, const MatProblem& p);
+cudaError_t launch_mul_mat_fused(gq_type t, const MatProblem& p, int64_t N, cudaStream_t s);
+
+// Composite pieces of the fused entry points (gq_fused.cu): Xhat = RMSNorm(X) per token
+// (N x K), and H = Swish(G) * U elementwise (n floats).
+cudaError_t launch_rmsnorm_x(const float* X, const float* gamma, float eps, int64_t N,
+                             int64_t K, float* Xhat, cudaStream_t s);
+cudaError_t launch_swiglu(const float* G, const float* U, float* H, int64_t n, cudaStream_t s);
 
 // Quantized-activation mul_mat (X quantized per 32-block like Q8_0, integer block sums):
 // the streaming decode kernel with Q8_0 activation records, up to 4 tokens per pass over

@@ -240,6 +240,39 @@ gq_status gq_mul_mat_q8x_batched(const gq_mul_mat_problem* problems, int32_t cou
                                  gq_type t, int64_t N, void* stream);
 
 /*
+ * The two steps next to the product in a transformer layer, fused with it.
+ *
+ * gq_mul_mat_rmsnorm: Y = RMSNorm(X) . What^T, where per token n
+ *     RMSNorm(x) = x / sqrt((1/K) sum_k x_k^2 + eps) (.) gamma
+ * ("Development Guide for Small AI Models (TinyLLaMA, etc.) Using C++", section 4.1:
+ * the norm ahead of the projections and of the LM head).
+ *   - gamma: K floats (device), 4-byte aligned; eps: finite and >= 0 (else GQ_ERR_SHAPE).
+ *   - K == 0 is GQ_ERR_SHAPE (the mean of nothing); other arguments as gq_mul_mat.
+ *   - Decode (N <= 2, K % 256 == 0, X and gamma 16-byte aligned): one launch; the decode
+ *     kernel normalizes X while it prepares it. Otherwise a per-token norm kernel writes the
+ *     normalized X into library workspace and the plain product follows.
+ *   - Accuracy: as gq_mul_mat, with ||RMSNorm(X)[n]||_2 in place of ||X[n]||_2.
+ *
+ * gq_mul_mat_swiglu: H[n][m] = Swish(G[n][m]) * U[n][m], G = X . What_gate^T,
+ * U = X . What_up^T, Swish(z) = z / (1 + e^-z) (the same guide, section 4.4: the gated
+ * feed-forward activation).
+ *   - W_gate and W_up: M x K blocks of the same type, both 16-byte aligned; H: N x M.
+ *   - K == 0 writes H = 0; other arguments as gq_mul_mat.
+ *   - Decode (N <= 2, K % 256 == 0): one launch; each warp streams gate row m and up row m
+ *     side by side and writes H directly. Otherwise G and U go to library workspace by two
+ *     plain products and an elementwise kernel writes H.
+ *   - Accuracy: |H - H_exact| <= 1.1 |U| e_G + |Swish(G)| e_U to first order, where e_G and
+ *     e_U are the gq_mul_mat bounds of the two products (|Swish'| <= 1.1).
+ * Both need library workspace off the decode path (like gq_mul_mat; refused while the
+ * stream is being captured if it must grow). Y / H must not overlap the other arrays.
+ */
+gq_status gq_mul_mat_rmsnorm(const void* W_blocks, gq_type t, int64_t M, int64_t K,
+                             const float* X, const float* gamma, float eps, int64_t N,
+                             float* Y, void* stream);
+gq_status gq_mul_mat_swiglu(const void* W_gate, const void* W_up, gq_type t, int64_t M,
+                            int64_t K, const float* X, int64_t N, float* H, void* stream);
+
+/*
  * Device-side status of the current device: synchronizes `stream`, then returns and
  * clears the status word (GQ_OK, or GQ_ERR_TIMEOUT if a kernel gave up waiting), or
  * GQ_ERR_CUDA if the stream itself reports an error.

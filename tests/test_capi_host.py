@@ -125,3 +125,24 @@ def test_mul_mat_q8x_argument_checks(gq_lib):
     assert fb(None, 300, 2, 1, None) == -2
     arr = gq_lib.make_problems([])
     assert fb(arr, 1, 7, 1, None) == -3
+
+
+def test_fused_entry_points_argument_checks(gq_lib):
+    rn = gq_lib.lib.gq_mul_mat_rmsnorm
+    assert rn(A16, 7, 4, 64, A16, A16, 1e-5, 1, A16, None) == -3     # unknown type
+    assert rn(A16, 2, 4, 48, A16, A16, 1e-5, 1, A16, None) == -2     # K % 32
+    assert rn(A16, 2, 4, 64, A16, A16, -1.0, 1, A16, None) == -2     # eps < 0
+    assert rn(A16, 2, 4, 64, A16, A16, float("nan"), 1, A16, None) == -2
+    assert rn(A16, 2, 4, 64, A16, A16, float("inf"), 1, A16, None) == -2
+    assert rn(A16, 2, 4, 0, A16, A16, 1e-5, 1, A16, None) == -2      # mean of nothing
+    assert rn(A16, 2, 4, 64, A16, None, 1e-5, 1, A16, None) == -1    # gamma missing
+    assert rn(A16, 2, 4, 64, A16, A2, 1e-5, 1, A16, None) == -4      # gamma misaligned
+    assert rn(A4, 2, 4, 64, A16, A16, 1e-5, 1, A16, None) == -4      # W misaligned
+    assert rn(A16, 2, 0, 64, A16, A16, 1e-5, 1, A16, None) == 0      # M == 0: nothing to do
+    sw = gq_lib.lib.gq_mul_mat_swiglu
+    assert sw(A16, A16, 7, 4, 64, A16, 1, A16, None) == -3
+    assert sw(A16, A16, 2, 4, 48, A16, 1, A16, None) == -2
+    assert sw(A16, None, 2, 4, 64, A16, 1, A16, None) == -1          # up missing
+    assert sw(A16, A4, 2, 4, 64, A16, 1, A16, None) == -4            # up misaligned
+    assert sw(None, A16, 2, 4, 64, A16, 1, A16, None) == -1          # gate missing
+    assert sw(A16, A16, 2, 4, 64, A16, 0, A16, None) == 0            # N == 0

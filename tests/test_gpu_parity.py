@@ -585,3 +585,91 @@ def test_q8x_rejects_unsupported_shapes(gq_lib, cuda_dev):
     with pytest.raises(gq_lib.GQError) as e:
         gq_lib.mul_mat_q8x(q, "q4_0", 4, 256, Xb[1:257].view(1, 256))
     assert e.value.status == -4
+
+
+# ------------------------------------------------------------------------------------
+# Fused adjacent steps ("Development Guide for Small AI Models (TinyLLaMA, etc.) Using
+# C++", sections 4.1 and 4.4): RMSNorm ahead of the product, SwiGLU of gate/up after it
+# ------------------------------------------------------------------------------------
+# (M, K, N): N <= 2 with K % 256 == 0 runs fused in the decode kernel (K = 1024: whole-row
+# stages; M = 20: few rows, so tiles split K between warps); the rest composes plain kernels
+# (N = 8 tensor-core decode, N = 100 GEMM, K = 96 the generic kernel).
+FUSED = [(300, 2048, 1), (129, 5632, 2), (129, 1024, 1), (20, 2048, 1), (7, 256, 2),
+         (200, 2048, 8), (300, 512, 100), (40, 96, 2)]
+
+
+def _gamma(K, seed):
+    return (1.0 + 0.1 * np.random.default_rng(seed).standard_normal(K)).astype(np.float32)
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", FUSED)
+def test_mul_mat_rmsnorm_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    """Y = RMSNorm(X) . What^T within 1e-3 ||RMSNorm(X)[n]|| ||What[m]||: the gq_mul_mat bound
+    on the normalized activations (their norm from the page formula in fp64)."""
+    W = _np_weights(M, K, seed=M + K)
+    q = oracle_mod.quantize(t, W)
+    X = workloads.activations(N, K, seed=N + 7).numpy() * np.float32(3.0)
+    gamma, eps = _gamma(K, K), 1e-5
+    Y = gq_lib.mul_mat_rmsnorm(torch.from_numpy(q).to(cuda_dev), t, M, K,
+                               torch.from_numpy(X).to(cuda_dev),
+                               torch.from_numpy(gamma).to(cuda_dev), eps).cpu().numpy()
+    assert gq_lib.get_last_error() == 0
+    Y_ref = oracle_mod.mul_mat_rmsnorm(t, q, M, K, X, gamma, eps)
+    x64 = X.astype(np.float64)
+    xhat = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + eps) * gamma
+    check_tolerance(Y, Y_ref, oracle_mod.dequantize(t, q, M, K), xhat, f"rmsnorm {t} {M} {K} {N}")
+
+
+def _check_swiglu(oracle_mod, t, qg, qu, M, K, X, H, where):
+    """|H - H_ref| <= 1.1 |U| e_G + |Swish(G)| e_U + 1e-6 |H_ref|: first-order propagation of
+    the mul_mat bounds e = 1e-3 ||x|| ||w_m|| of both products (|Swish'| <= 1.1)."""
+    H_ref = oracle_mod.mul_mat_swiglu(t, qg, qu, M, K, X).astype(np.float64)
+    G = oracle_mod.mul_mat(t, qg, M, K, X).astype(np.float64)
+    U = oracle_mod.mul_mat(t, qu, M, K, X).astype(np.float64)
+    xn = np.linalg.norm(X.astype(np.float64), axis=1)[:, None]
+    eg = TOL * xn * np.linalg.norm(oracle_mod.dequantize(t, qg, M, K).astype(np.float64), axis=1)[None, :]
+    eu = TOL * xn * np.linalg.norm(oracle_mod.dequantize(t, qu, M, K).astype(np.float64), axis=1)[None, :]
+    tol = 1.1 * np.abs(U) * eg + np.abs(G / (1.0 + np.exp(-G))) * eu + 1e-6 * np.abs(H_ref)
+    err = np.abs(np.asarray(H, np.float64) - H_ref)
+    bad = err > tol
+    assert not bad.any(), f"{where}: {bad.sum()} out of tolerance, first {np.argwhere(bad)[0]}"
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", FUSED)
+def test_mul_mat_swiglu_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    qg = oracle_mod.quantize(t, _np_weights(M, K, seed=M + 2 * K))
+    qu = oracle_mod.quantize(t, _np_weights(M, K, seed=M + 3 * K))
+    X = workloads.activations(N, K, seed=N + 11).numpy() * np.float32(4.0)
+    H = gq_lib.mul_mat_swiglu(torch.from_numpy(qg).to(cuda_dev), torch.from_numpy(qu).to(cuda_dev),
+                              t, M, K, torch.from_numpy(X).to(cuda_dev)).cpu().numpy()
+    assert gq_lib.get_last_error() == 0
+    _check_swiglu(oracle_mod, t, qg, qu, M, K, X, H, f"swiglu {t} {M} {K} {N}")
+
+
+def test_fused_decode_full_size_and_deterministic(gq_lib, oracle_mod, cuda_dev):
+    """TinyLLaMA at N = 1: the FFN gate/up pair (5632 x 2048) through the fused SwiGLU, and
+    the final RMSNorm into the LM head (32000 x 2048); all outputs against the oracle, and
+    bitwise-equal reruns."""
+    M, K = 5632, 2048
+    qg = gq_lib.quantize(workloads.weights(M, K, 95, device=cuda_dev), "q4_0")
+    qu = gq_lib.quantize(workloads.weights(M, K, 96, device=cuda_dev), "q4_0")
+    X = workloads.activations(1, K, 97)
+    Xd = X.to(cuda_dev)
+    H = gq_lib.mul_mat_swiglu(qg, qu, "q4_0", M, K, Xd)
+    assert torch.equal(H.view(torch.int32), gq_lib.mul_mat_swiglu(qg, qu, "q4_0", M, K, Xd).view(torch.int32))
+    _check_swiglu(oracle_mod, "q4_0", qg.cpu().numpy(), qu.cpu().numpy(), M, K, X.numpy(),
+                  H.cpu().numpy(), "tinyllama ffn")
+    Ml = 32000
+    ql = gq_lib.quantize(workloads.weights(Ml, K, 98, device=cuda_dev), "q4_0")
+    gamma = torch.from_numpy(_gamma(K, 99))
+    Y = gq_lib.mul_mat_rmsnorm(ql, "q4_0", Ml, K, Xd, gamma.to(cuda_dev), 1e-5)
+    assert torch.equal(Y.view(torch.int32),
+                       gq_lib.mul_mat_rmsnorm(ql, "q4_0", Ml, K, Xd, gamma.to(cuda_dev), 1e-5).view(torch.int32))
+    q_np = ql.cpu().numpy()
+    Y_ref = oracle_mod.mul_mat_rmsnorm("q4_0", q_np, Ml, K, X.numpy(), gamma.numpy(), 1e-5)
+    x64 = X.numpy().astype(np.float64)
+    xhat = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + 1e-5) * gamma.numpy()
+    check_tolerance(Y.cpu().numpy(), Y_ref, oracle_mod.dequantize("q4_0", q_np, Ml, K), xhat, "lm_head")
+    assert gq_lib.get_last_error() == 0
