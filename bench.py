@@ -399,6 +399,74 @@ def q8x_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2, 4, 8, 16)) -> dic
             "unit": "GB/s", "per_N": rows}
 
 
+def fused_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2)) -> dict:
+    """The fused adjacent steps at decode, each timed from a CUDA graph against the plain
+    products it replaces: TinyLLaMA's FFN gate/up pair (2 x 5632 x 2048) through
+    gq_mul_mat_swiglu vs two gq_mul_mat calls, and the final RMSNorm into the LM head
+    (32000 x 2048) through gq_mul_mat_rmsnorm vs gq_mul_mat alone. Weight copies are
+    rotated so every call reads its weights from HBM; GB/s counts weights + X + output once."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    peak, _ = measured_peaks()
+    K, Mf, Ml = 2048, 5632, 32000
+    rb = binding.row_bytes("q4_0", K)
+
+    def copies(nbytes):
+        return min(48, max(1, -(-4 * L2_BYTES // nbytes)))
+
+    def timed(calls):
+        for c in calls[:2]:
+            c()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for r in range(reps):
+                calls[r % len(calls)]()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (reps * iters) / 1e3
+
+    out = {"unit": "GB/s", "peak": peak}
+    nf = copies(2 * Mf * rb)
+    gates = [binding.quantize(workloads.weights(Mf, K, 7000 + c, device=dev), "q4_0") for c in range(nf)]
+    ups = [binding.quantize(workloads.weights(Mf, K, 7100 + c, device=dev), "q4_0") for c in range(nf)]
+    nl = copies(Ml * rb)
+    heads = [binding.quantize(workloads.weights(Ml, K, 7200 + c, device=dev), "q4_0") for c in range(nl)]
+    gamma = (1.0 + 0.1 * torch.randn(K, generator=torch.Generator().manual_seed(7300))).to(dev)
+    rows_s, rows_r = [], []
+    for N in Ns:
+        X = workloads.activations(N, K, 7400 + N, device=dev)
+        H, G, U = (torch.empty((N, Mf), device=dev) for _ in range(3))
+        b = 2 * Mf * rb + N * K * 4 + N * Mf * 4
+        fused = timed([lambda c=c: binding.mul_mat_swiglu(gates[c], ups[c], "q4_0", Mf, K, X, out=H)
+                       for c in range(nf)])
+        plain = timed([lambda c=c: (binding.mul_mat(gates[c], "q4_0", Mf, K, X, out=G),
+                                    binding.mul_mat(ups[c], "q4_0", Mf, K, X, out=U))
+                       for c in range(nf)])
+        rows_s.append({"N": N, "fused_us": round(fused * 1e6, 2), "GBps": round(b / fused / 1e9, 1),
+                       "frac": round(b / fused / 1e9 / peak, 4),
+                       "two_mul_mat_us (no activation)": round(plain * 1e6, 2)})
+        Y = torch.empty((N, Ml), device=dev)
+        b = Ml * rb + N * K * 4 + N * Ml * 4
+        fused = timed([lambda c=c: binding.mul_mat_rmsnorm(heads[c], "q4_0", Ml, K, X, gamma, 1e-5, out=Y)
+                       for c in range(nl)])
+        plain = timed([lambda c=c: binding.mul_mat(heads[c], "q4_0", Ml, K, X, out=Y) for c in range(nl)])
+        rows_r.append({"N": N, "fused_us": round(fused * 1e6, 2), "GBps": round(b / fused / 1e9, 1),
+                       "frac": round(b / fused / 1e9 / peak, 4),
+                       "mul_mat_alone_us (no norm)": round(plain * 1e6, 2)})
+    if binding.get_last_error() != 0:
+        raise RuntimeError("device status word set during the fused steps")
+    out["swiglu_tinyllama_ffn_gate_up"] = rows_s
+    out["rmsnorm_tinyllama_lm_head"] = rows_r
+    return out
+
+
 def profile_decode(spec: str, steps: int) -> dict:
     """For ncu: the TinyLLaMA decode step with N tokens (spec "q8_0/16"), one batched call
     per step with a caller-owned workspace, 3 warm-up steps then `steps` timed ones."""
@@ -601,6 +669,7 @@ def run_gb300(args, shapes):
         line["decode"] = {"unit": "GB/s", "peak": peak, "peak_source": line["roofline"]["peak_source"],
                           **decode_measure(dev)}
         line["decode_q8x"] = q8x_measure(dev)
+        line["fused"] = fused_measure(dev)
         pf = prefill_measure(dev)
         line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16 operands, fp32 accumulate",
                            "peak": measured_bf16_peak(),
