@@ -86,18 +86,19 @@ struct TcLayout {
     static constexpr int kRaw = kBM * kRawRow;              // 18 / 34 KB of raw blocks
     static constexpr int kStage = kRaw + 4 * kB;            // raw blocks + the super-step's X
     static constexpr int kOffRaw = 0;
-    // Scaled: the two dequantize groups' halves of a tile's y meet in shared memory, two
-    // buffers by tile parity, 128 rows x kNPad (+1 against bank conflicts) fp32.
+    // Scaled: the two dequantize groups' halves of a tile's y meet in shared memory, one
+    // buffer (tiles are at least 8 super-steps apart), 128 rows x kNPad (+1 against bank
+    // conflicts) fp32.
     static constexpr int kYStride = kNPad + 1;
-    static constexpr int kYBytes = kScaled ? 2 * kBM * kYStride * 4 : 0;
+    static constexpr int kYBytes = kScaled ? kBM * kYStride * 4 : 0;
     static constexpr int kFixed = 1024 + 512 + kYBytes;     // alignment slack, barriers, slot
     static constexpr int kRawFit = (kSmemLimit - kFixed) / kStage;
     static constexpr int kRawStages = kRawFit > 8 ? 8 : kRawFit;
     static constexpr int kOffBar = kOffRaw + kRawStages * kStage;
     // raw_full[R], raw_empty[R], a_full[2][G], a_empty[2][G], acc_full[B], acc_empty[B],
-    // mma_done, and in the scaled form y_full[2], y_free[2]
+    // mma_done, and in the scaled form y_full, y_free
     static constexpr int kNumBars =
-        2 * kRawStages + 4 * kGroupSlots + 2 * kAccBufs + 1 + (kScaled ? 4 : 0);
+        2 * kRawStages + 4 * kGroupSlots + 2 * kAccBufs + 1 + (kScaled ? 2 : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kOffY = kOffMisc + 16;
     static constexpr int kBytes = kOffY + kYBytes;
@@ -372,8 +373,8 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
     auto a_full = [&](int g, int i) { return bar0 + 8u * (2 * R + g * G + i); };
     auto acc_full = [&](int b) { return bar0 + 8u * (2 * R + 4 * G + b); };
     const uint32_t mma_done = bar0 + 8u * (2 * R + 4 * G + 2 * B);
-    auto y_full = [&](int t) { return mma_done + 8u * (1 + t); };
-    auto y_free = [&](int t) { return mma_done + 8u * (3 + t); };
+    const uint32_t y_full = mma_done + 8u;
+    const uint32_t y_free = mma_done + 16u;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -416,23 +417,22 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
         return true;
     };
     auto finish_tile = [&](int p, int64_t row0, int rows, int slot) -> bool {
-        const int tb = tile_n & 1;
-        const uint32_t ph = (tile_n >> 1) & 1;
-        float* yb = ybuf + (tb * kBM + row) * L::kYStride;
+        const uint32_t ph = tile_n & 1;
+        float* yb = ybuf + row * L::kYStride;
         ++tile_n;
         if (g == 1) {
-            if (!mbar_wait(y_free(tb), ph ^ 1)) return false;
+            if (!mbar_wait(y_free, ph ^ 1)) return false;   // group 0 read the last tile's
 #pragma unroll
             for (int t = 0; t < kNPad; ++t) yb[t] = y[t];
-            mbar_arrive(y_full(tb));   // release: the stores above before group 0's reads
+            mbar_arrive(y_full);   // release: the stores above before group 0's reads
 #pragma unroll
             for (int t = 0; t < kNPad; ++t) y[t] = 0.0f;
             return true;
         }
-        if (!mbar_wait(y_full(tb), ph)) return false;
+        if (!mbar_wait(y_full, ph)) return false;
 #pragma unroll
         for (int t = 0; t < kNPad; ++t) y[t] += yb[t];
-        mbar_arrive(y_free(tb));
+        mbar_arrive(y_free);
         const TcProb& pr = P.p[p];
         float* part = P.part + (static_cast<int64_t>(blockIdx.x) * 2 + max(slot, 0)) *
                                    (kNPad * kBM);
@@ -588,7 +588,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
         }
         mbar_init(mma_done, kMmaWarps);
         if constexpr (L::kScaled) {
-            for (int i = 0; i < 4; ++i) mbar_init(mma_done + 8u * (1 + i), 32 * kDequantWarps / 2);
+            for (int i = 0; i < 2; ++i) mbar_init(mma_done + 8u * (1 + i), 32 * kDequantWarps / 2);
         }
         fence_mbar_init();
     }
