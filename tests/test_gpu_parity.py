@@ -673,3 +673,28 @@ def test_fused_decode_full_size_and_deterministic(gq_lib, oracle_mod, cuda_dev):
     xhat = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + 1e-5) * gamma.numpy()
     check_tolerance(Y.cpu().numpy(), Y_ref, oracle_mod.dequantize("q4_0", q_np, Ml, K), xhat, "lm_head")
     assert gq_lib.get_last_error() == 0
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_fused_misaligned_inputs_take_the_composite_path(gq_lib, oracle_mod, cuda_dev, t):
+    """gamma and X only 4-byte aligned: the decode kernel's 16-byte loads cannot take them,
+    so both entry points compose plain kernels at N = 1 and must still match the oracle."""
+    M, K, N = 96, 512, 1
+    q = oracle_mod.quantize(t, _np_weights(M, K, seed=101))
+    qu = oracle_mod.quantize(t, _np_weights(M, K, seed=102))
+    X = workloads.activations(N, K, seed=103).numpy()
+    gamma = _gamma(K, 104)
+    xbuf = torch.zeros(N * K + 1, dtype=torch.float32, device=cuda_dev)
+    xbuf[1:] = torch.from_numpy(X.reshape(-1)).to(cuda_dev)
+    Xm = xbuf[1:].view(N, K)                      # 4-byte aligned, not 16
+    gbuf = torch.zeros(K + 1, dtype=torch.float32, device=cuda_dev)
+    gbuf[1:] = torch.from_numpy(gamma).to(cuda_dev)
+    qd = torch.from_numpy(q).to(cuda_dev)
+    Y = gq_lib.mul_mat_rmsnorm(qd, t, M, K, torch.from_numpy(X).to(cuda_dev), gbuf[1:], 1e-5)
+    x64 = X.astype(np.float64)
+    xhat = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + 1e-5) * gamma
+    check_tolerance(Y.cpu().numpy(), oracle_mod.mul_mat_rmsnorm(t, q, M, K, X, gamma, 1e-5),
+                    oracle_mod.dequantize(t, q, M, K), xhat, "rmsnorm, gamma misaligned")
+    H = gq_lib.mul_mat_swiglu(qd, torch.from_numpy(qu).to(cuda_dev), t, M, K, Xm)
+    _check_swiglu(oracle_mod, t, q, qu, M, K, X, H.cpu().numpy(), "swiglu, X misaligned")
+    assert gq_lib.get_last_error() == 0
