@@ -79,11 +79,19 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """The source without comments, blank lines or indentation: what the compiler sees
+    (a comment-only edit leaves the kernel, and so its counters, unchanged)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.strip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -37,6 +37,12 @@
 //    atomics.
 //  * Waits are bounded: a stage that never arrives sets the device status word; the CTA
 //    leaves at the next problem boundary after draining its own copies.
+//  * Fused forms of the same kernel: RMSNorm of X folded into the activation preparation
+//    (per-token 1 / rms in a fixed-order reduction, times gamma, before the fixed-point
+//    conversion), and gate/up row pairs (row 2m from the gate matrix, 2m + 1 from the up
+//    matrix, adjacent lanes' sums combined into Swish(g) * u), so the SwiGLU output is
+//    written once and the intermediate products never reach HBM ("Development Guide for
+//    Small AI Models (TinyLLaMA, etc.) Using C++", sections 4.1 and 4.4).
 // Shapes the streaming kernel does not take (K % 256 != 0, unaligned X, very large K)
 // run on gemv_generic_kernel: one warp per row, plain loads, fp32 FMA.
 #include <algorithm>

@@ -57,6 +57,14 @@ def test_profile_summary_requires_current_kernel(tmp_path, monkeypatch):
     assert bench.profiled_traffic() is None
 
 
+def test_kernel_hash_ignores_comments_only():
+    src = "// header\nint f(int a) {\n    /* block\n comment */ return a + 1;  // tail\n}\n"
+    same = "int f(int a) {\n\n  return a + 1;\n}\n// a new note\n"
+    changed = "int f(int a) {\n    return a + 2;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(changed)
+
+
 def test_reference_arm_sample_sizes():
     shapes = workloads.tinyllama_decode_set()[:3]
     sample = bench.oracle_sample(shapes, 2, 2)
