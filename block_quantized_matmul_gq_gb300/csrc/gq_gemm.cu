@@ -168,6 +168,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                     ok = false;
                     break;
                 }
+                if (ks == 0) griddep_wait();   // the bf16 X of this call is complete
                 mbar_arrive_expect_tx(full(s), L::kB);
                 tma_load_2d(sB + s * L::kB, &tmap_x, (j0 * (kSuperK / kBK) + ks) * kBK, n0, full(s));
                 ++b_issued;
@@ -351,6 +352,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 // X (fp32, n4 * 4 elements) -> bf16, round to nearest even.
 __global__ void __launch_bounds__(256)
 x_to_bf16_kernel(const float* __restrict__ X, int64_t n, __nv_bfloat16* __restrict__ out) {
+    // The GEMM launched after this kernel may start its prologue and weight copies now; it
+    // waits for this grid's completion before it reads the bf16 X.
+    griddep_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if ((reinterpret_cast<uintptr_t>(X) & 15) == 0) {
@@ -485,29 +489,31 @@ cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* x
     if (e != cudaSuccess) return e;
     const int64_t mt = (p.M + kBM - 1) / kBM, nt = (N + kBN - 1) / kBN;
     const int Z = split_k_ways(split_kernel, L::kAlloc, info, mt * nt, p.K / kSuperK);
-    if (Z == 1) {
-        kernel<<<dim3(static_cast<unsigned>(mt), static_cast<unsigned>(nt)), kThreads, L::kAlloc, s>>>(
-            tw, tx, static_cast<int>(p.M), static_cast<int>(N), static_cast<int>(p.K), p.Y,
-            info->status);
-        return cudaGetLastError();
-    }
+    // A programmatic dependent of x_to_bf16_kernel: barrier setup, TMEM allocation, the
+    // first weight copies and their dequantization overlap the conversion of X; the
+    // producer waits for it (griddepcontrol.wait) before its first X tile copy. Nothing
+    // else this kernel touches is written by x_to_bf16_kernel, and that kernel itself is
+    // an ordinary launch, so everything earlier in the stream has completed.
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(mt), static_cast<unsigned>(nt), static_cast<unsigned>(Z));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kAlloc;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = static_cast<unsigned>(Z);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(Z);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = Z == 1 ? 1 : 2;
     int M = static_cast<int>(p.M), n = static_cast<int>(N), K = static_cast<int>(p.K);
     float* Y = p.Y;
     unsigned* status = info->status;
     void* args[] = {&tw, &tx, &M, &n, &K, &Y, &status};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(split_kernel), args);
+    return cudaLaunchKernelExC(
+        &cfg, reinterpret_cast<const void*>(Z == 1 ? kernel : split_kernel), args);
 }
 
 }  // namespace
