@@ -80,6 +80,24 @@ struct Layout {
     static_assert(kBM * kBN * 4 <= kOffRaw, "partial tile fits the operand stages");
 };
 
+// Stage q (0..3) of a super-step for dequantize half h: block 2q + h of the thread's row,
+// from the raw super-step in registers, into the row's 128-byte swizzled A line.
+template <int kType>
+__device__ __forceinline__ void dequant_stage(int q, int h, const uint32_t* raw, uint8_t* arow,
+                                              int row) {
+    if (h == 0) {
+        if (q == 0) dequant_store<kType, 0, 0>(raw, arow, row);
+        if (q == 1) dequant_store<kType, 1, 0>(raw, arow, row);
+        if (q == 2) dequant_store<kType, 2, 0>(raw, arow, row);
+        if (q == 3) dequant_store<kType, 3, 0>(raw, arow, row);
+    } else {
+        if (q == 0) dequant_store<kType, 0, 1>(raw, arow, row);
+        if (q == 1) dequant_store<kType, 1, 1>(raw, arow, row);
+        if (q == 2) dequant_store<kType, 2, 1>(raw, arow, row);
+        if (q == 3) dequant_store<kType, 3, 1>(raw, arow, row);
+    }
+}
+
 template <int kType, int kBN, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
@@ -237,28 +255,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
                 release_to_async_proxy(dep);
             }
             mbar_arrive(raw_empty(r));
+            // kRound 64-k stages per round: the waits, the proxy fence and the arrivals of
+            // a round are paid once. Two per round pays for Q8_0, whose dequantization is
+            // longer (measured: 7B lm_head at N = 2048 568 -> 533 us); Q4_0 lost with it
+            // (398 -> 426 us), its four stages then refilling only in pairs.
+            constexpr int kRound = kType == GQ_TYPE_Q8_0 ? 2 : 1;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 4; q += kRound) {
                 const int ks = 4 * j + q;
-                const int s = ks % S;
-                if (!mbar_wait(empty(s), ((ks / S) & 1) ^ 1)) {
+                bool free = true;
+#pragma unroll
+                for (int i = 0; i < kRound; ++i)
+                    free = free && mbar_wait(empty((ks + i) % S), (((ks + i) / S) & 1) ^ 1);
+                if (!free) {
                     ok = false;
                     break;
                 }
-                uint8_t* arow = base + L::kOffA + s * L::kA + row * 128;
-                if (half == 0) {
-                    if (q == 0) dequant_store<kType, 0, 0>(raw, arow, row);
-                    if (q == 1) dequant_store<kType, 1, 0>(raw, arow, row);
-                    if (q == 2) dequant_store<kType, 2, 0>(raw, arow, row);
-                    if (q == 3) dequant_store<kType, 3, 0>(raw, arow, row);
-                } else {
-                    if (q == 0) dequant_store<kType, 0, 1>(raw, arow, row);
-                    if (q == 1) dequant_store<kType, 1, 1>(raw, arow, row);
-                    if (q == 2) dequant_store<kType, 2, 1>(raw, arow, row);
-                    if (q == 3) dequant_store<kType, 3, 1>(raw, arow, row);
-                }
+#pragma unroll
+                for (int i = 0; i < kRound; ++i)
+                    dequant_stage<kType>(q + i, half, raw,
+                                         base + L::kOffA + ((ks + i) % S) * L::kA + row * 128, row);
                 fence_proxy_async_smem();
-                mbar_arrive(full(s));
+#pragma unroll
+                for (int i = 0; i < kRound; ++i) mbar_arrive(full((ks + i) % S));
             }
         }
         if (!ok) report_status(status, kStatusTimeout);
