@@ -28,13 +28,15 @@
  *   - Streams. `stream` is a cudaStream_t (NULL = the legacy default stream) passed as
  *     void* so that this header needs no CUDA include. Calls only enqueue work: they do
  *     not synchronize, and results are ready when the stream reaches them.
- *   - Overlap of consecutive calls. A decode call (N <= 2, and gq_mul_mat_q8x) is launched
- *     as a programmatic dependent of the kernel before it on the stream: its CTAs may
- *     begin loading W_blocks on SMs that the previous libgq decode call has left, before
- *     that call has completed. X and Y are touched only after it has completed, so one
- *     call's Y may be the next call's X, or the other way round. W_blocks must therefore
- *     not be memory that the immediately preceding libgq decode call on the stream writes
- *     (its Y); any other kernel in between orders the two calls as usual.
+ *   - Overlap of consecutive calls. A decode call (N <= 64, and gq_mul_mat_q8x) is
+ *     launched as a programmatic dependent of the kernel before it on the stream: its CTAs
+ *     may begin loading W_blocks on SMs that the previous libgq decode call has left,
+ *     before that call has completed. X and Y are touched only after it has completed, so
+ *     one call's Y may be the next call's X, or the other way round. W_blocks must
+ *     therefore not be memory that the immediately preceding libgq decode call on the
+ *     stream writes (its Y); any other kernel in between orders the two calls as usual.
+ *     A prefill call (N >= 65) begins with an ordinary launch, so it starts only after
+ *     everything before it on the stream has completed.
  *   - Errors. Argument checks run on the host before anything is launched and return a
  *     negative gq_status; nothing is enqueued then. A failed CUDA launch returns
  *     GQ_ERR_CUDA. Kernels never trap: a device-side wait that runs past its limit sets a

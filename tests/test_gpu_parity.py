@@ -164,15 +164,16 @@ def test_mul_mat_deterministic(gq_lib, cuda_dev):
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
 
 
-@pytest.mark.parametrize("N", [1, 2, 8, 40])
+@pytest.mark.parametrize("N", [1, 2, 8, 40, 96])
 def test_back_to_back_calls_see_previous_results(gq_lib, cuda_dev, N):
-    """Decode calls launched back to back on one stream, each call's X being the previous
-    call's Y (read after write) and each call's Y overwriting the X of the call before
-    (write after read), give bitwise the results of the same chain with a synchronize after
-    every call. A call may start streaming its weights while the previous one finishes;
-    this pins that it touches X, Y and its workspace (N = 8, 40: the tensor-core path's X
-    tiles, partial sums and counters, reused by every call) only after that call is
-    complete."""
+    """Calls launched back to back on one stream, each call's X being the previous call's Y
+    (read after write) and each call's Y overwriting the X of the call before (write after
+    read), give bitwise the results of the same chain with a synchronize after every call.
+    A decode call may start streaming its weights while the previous one finishes; this
+    pins that it touches X, Y and its workspace (N = 8, 40: the tensor-core path's X tiles,
+    partial sums and counters, reused by every call) only after that call is complete.
+    N = 96 runs the prefill GEMM, which starts while its own X conversion runs and must
+    read the converted X only after it is complete."""
     D = 2048
     qs = [gq_lib.quantize(workloads.weights(D, D, 40 + i, device=cuda_dev), "q4_0")
           for i in range(4)]
@@ -200,13 +201,14 @@ def test_back_to_back_calls_see_previous_results(gq_lib, cuda_dev, N):
     assert gq_lib.get_last_error() == 0
 
 
-@pytest.mark.parametrize("N", [1, 8])
+@pytest.mark.parametrize("N", [1, 8, 96])
 def test_decode_after_quantize_into_the_same_blocks(gq_lib, cuda_dev, N):
     """A decode call may load its weights before the kernel ahead of it on the stream has
     completed, but only when that kernel lets it start early, which only libgq's decode
-    kernels do. Quantizing a different matrix into the same block buffer right before each
-    call, with no synchronize, must give bitwise the results of the same sequence with a
-    synchronize after every launch."""
+    kernels do; the prefill GEMM (N = 96) loads its weights early only behind its own X
+    conversion, an ordinary launch. Quantizing a different matrix into the same block
+    buffer right before each call, with no synchronize, must give bitwise the results of
+    the same sequence with a synchronize after every launch."""
     M = K = 2048
     Ws = [workloads.weights(M, K, 70 + i, device=cuda_dev) for i in range(3)]
     X = workloads.activations(N, K, 73, device=cuda_dev)
