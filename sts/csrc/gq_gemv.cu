@@ -1,0 +1,1166 @@
+// gq_gemv.cu -- decode-side mul_mat (few tokens): Y[n][m] = sum_k What[m][k] * X[n][k].
+//
+// At decode the product is a matrix-vector product that streams every weight once
+// ("A Complete Guide to llama.cpp and Customization with C++", section 2.1) and is
+// bound by memory bandwidth; the weights are dequantized right after they are loaded
+// ("No Python! Building an AI Inference Engine Exclusively in C++", section 9;
+// "Development Guide for Small AI Models (TinyLLaMA, etc.) Using C++", section 6.2:
+// load, unpack with masks and shifts, scale, multiply-accumulate).
+//
+// GB300 design (not the pages' CPU/SIMD one):
+//  * One persistent CTA per SM. All problems of a launch form one sequence of rows; each
+//    CTA takes a contiguous, row-aligned share of equal estimated time (bytes plus a fixed
+//    cost per ring stage), so small matrices (GQA k/v projections) ride along with large
+//    ones and no CTA idles on a tail.
+//  * Inside a CTA, each warp owns tiles of 4 rows; eight lanes share a row and walk its K
+//    columns eight "chunks" at a time (a chunk is 8 Q4_0 blocks = 144 B = 256 weights, or
+//    4 Q8_0 blocks = 136 B = 128 weights), one chunk per lane. Every warp streams its own
+//    tiles through a private ring of shared-memory stages filled by 1-D bulk copies (TMA
+//    cp.async.bulk, L2 evict-first) issued by one lane -- a single copy when the stage
+//    holds whole rows (K <= 2048 for Q4_0), else one per row -- completing on a per-warp
+//    mbarrier; warps never wait for each other inside a problem. Rows are whole chunks
+//    (K % 256 == 0), so copies are 16-byte aligned.
+//  * Activations: at each problem boundary the CTA converts X into 16-bit block fixed
+//    point in shared memory (one power-of-two scale 2^e per chunk), so the inner product
+//    of a 32-weight block is EXACT integer arithmetic with dp2a (two 16x8-bit products
+//    per instruction):
+//        S = sum_i (16 (c_i - 8)) * x16_i       (Q4_0; codes become signed bytes 16(c-8))
+//        S = sum_i c_i * x16_i                  (Q8_0)
+//    then acc += d * float(S) and, per chunk, partial = acc * 2^e. The only approximation
+//    is x16 = rint(x / 2^e) with |x16| <= 32767, i.e. |error| <= sqrt(256) / 65534 *
+//    ||x|| ||What|| = 0.24 of the bound 1e-3 ||x|| ||What|| (Cauchy-Schwarz per chunk),
+//    whatever the inputs. All lanes of a warp read the same x16 columns (broadcast).
+//  * A lane keeps its row's running sum in registers across all columns; the eight lanes
+//    of a row add their sums with three shuffles at the end. When a CTA's part of a problem
+//    has fewer 4-row tiles than warps, each tile's columns are split between warps and
+//    the per-warp sums are added in a fixed order in shared memory: deterministic, no
+//    atomics.
+//  * Waits are bounded: a stage that never arrives sets the device status word; the CTA
+//    leaves at the next problem boundary after draining its own copies.
+//  * Fused forms of the same kernel: RMSNorm of X folded into the activation preparation
+//    (per-token 1 / rms in a fixed-order reduction, times gamma, before the fixed-point
+//    conversion), and gate/up row pairs (row 2m from the gate matrix, 2m + 1 from the up
+//    matrix, adjacent lanes' sums combined into Swish(g) * u), so the SwiGLU output is
+//    written once and the intermediate products never reach HBM ("Development Guide for
+//    Small AI Models (TinyLLaMA, etc.) Using C++", sections 4.1 and 4.4).
+// Shapes the streaming kernel does not take (K % 256 != 0, unaligned X, very large K)
+// run on gemv_generic_kernel: one warp per row, plain loads, fp32 FMA.
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gq_device.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+// Build-time tuning: warps per CTA and ring depth per warp (for <= 3 tokens / 4 tokens).
+#ifndef GQ_GEMV_WARPS
+#define GQ_GEMV_WARPS 16
+#endif
+#ifndef GQ_GEMV_STAGES
+#define GQ_GEMV_STAGES 2
+#endif
+#ifndef GQ_GEMV_STAGES_N4
+#define GQ_GEMV_STAGES_N4 2
+#endif
+constexpr int kWarps = GQ_GEMV_WARPS;
+constexpr int kThreads = kWarps * 32;
+constexpr int kLanesPerRow = 8;               // one chunk per lane, 8 chunks per row per stage
+constexpr int kTileRows = 32 / kLanesPerRow;   // 4 rows per warp tile
+constexpr int kMaxTok = 4;                     // tokens per pass of the weight stream
+// The same with Q8_0-quantized activations: their records are smaller, but more tokens per
+// pass measured no faster (the per-token block sums bind from 4 tokens on: 212 us for 4,
+// 431 us for 8 on the TinyLLaMA step).
+constexpr int kMaxTokQ8x = 4;
+// Ring depth per warp: deeper while the x16 buffer is small (<= 3 tokens).
+template <int kNT>
+__host__ __device__ constexpr int ring_stages() {
+    return kNT <= 3 ? GQ_GEMV_STAGES : GQ_GEMV_STAGES_N4;
+}
+
+template <int kType>
+struct Fmt;
+template <>
+struct Fmt<GQ_TYPE_Q4_0> {
+    static constexpr int kBB = kQ4Bytes;
+    static constexpr int kBlocksPerChunk = 8;
+    static constexpr int kCodeShift = 4;   // dp2a sums come out as 16 * sum (c - 8) x16
+};
+template <>
+struct Fmt<GQ_TYPE_Q8_0> {
+    static constexpr int kBB = kQ8Bytes;
+    static constexpr int kBlocksPerChunk = 4;
+    static constexpr int kCodeShift = 0;
+};
+
+template <int kType>
+struct Geo {
+    static constexpr int kBB = Fmt<kType>::kBB;
+    static constexpr int kBPC = Fmt<kType>::kBlocksPerChunk;
+    static constexpr int kChunkBytes = kBB * kBPC;                 // 144 or 136
+    static constexpr int kChunkWords = kChunkBytes / 4;            // 36 or 34
+    static constexpr int kWPC = 32 * kBPC;                         // weights per chunk
+    static constexpr int kRowStride = kLanesPerRow * kChunkBytes;  // 1152 or 1088 in a stage
+    // One stage of one warp: 4 rows x 8 chunks, padded to 128-byte multiples.
+    static constexpr int kStageBytes = (kTileRows * kRowStride + 127) / 128 * 128;
+    // x16 record of one chunk for one token: kWPC int16; for Q4_0 one int bias per block
+    // (-128 * sum of the block's x16, the code offset 8 folded in); then two float
+    // factors whose product is the chunk's power-of-two scale. Record strides are
+    // 140 / 68 words (12 / 4 mod 32), so the 8 columns a warp reads sit in 8 different
+    // groups of 4 banks: one wavefront per 16-byte load.
+    static constexpr int kBiasOff = kWPC * 2;
+    static constexpr int kScaleOff = kBiasOff + (kType == GQ_TYPE_Q4_0 ? 4 * kBPC : 0);
+    static constexpr int kXRec = kScaleOff + 16;                   // 560 or 272
+};
+
+struct GemvProb {
+    const uint8_t* W;
+    const float* X;
+    float* Y;
+    int64_t M;
+    int64_t row_bytes;
+    int64_t row_cost;     // balancing weight of one row (see kGroupCost)
+    int64_t cost_begin;   // weight of all earlier problems
+    int32_t C;            // chunks per row
+    int32_t K;
+    // Fused forms. gamma != NULL: X is RMS-normalized per token (x / sqrt(mean x^2 + eps)
+    // * gamma) as it is prepared. W2 != NULL: gate/up pairs -- the row sequence has M =
+    // 2 M_h rows, row 2m from W (gate m) and row 2m + 1 from W2 (up m), and Y (rows of
+    // M_h) receives Swish(gate) * up.
+    const uint8_t* W2;
+    const float* gamma;
+    float eps;
+    int32_t pad_;
+};
+
+template <int kMaxProbs>
+struct GemvParams {
+    int32_t count;
+    int32_t n_tok;        // valid tokens of this pass, 1..kMaxTok
+    int32_t max_c;        // largest C: the x buffer holds kNT * max_c records
+    int32_t pad_;
+    int64_t total_bytes;
+    int64_t total_cost;
+    unsigned* status;
+    GemvProb p[kMaxProbs];
+};
+
+// CTA shares balance an estimate of time rather than bytes: a row weighs its bytes plus
+// kGroupCost for each column group (one ring stage per 4-row tile), the part of a stage's
+// cost that does not scale with its bytes (waits, refill, shuffles; a partly filled last
+// group costs the same as a full one). 576 was the best of 0 / 576 / 1152 / 2304 / 4608
+// measured on the TinyLLaMA and LLaMA-7B sets (Q4_0 and Q8_0, N = 1 and 2).
+constexpr int64_t kGroupCost = 576;
+
+// First row (problem p, row r) whose weight begins at or after `cost`; (count, 0) = end.
+template <int kMaxProbs>
+__device__ void row_at_cost(const GemvParams<kMaxProbs>& P, int64_t cost, int& p, int64_t& r) {
+    p = 0;
+    while (p + 1 < P.count && P.p[p + 1].cost_begin <= cost) ++p;
+    const int64_t off = cost - P.p[p].cost_begin;
+    r = off <= 0 ? 0 : (off + P.p[p].row_cost - 1) / P.p[p].row_cost;
+    if (P.p[p].W2 != nullptr) r = (r + 1) & ~int64_t(1);   // gate/up pairs stay together
+    if (r >= P.p[p].M) {
+        ++p;
+        r = 0;
+    }
+}
+
+// A CTA's share is a list of segments: one problem each, a row range [rb, re).
+struct Segment {
+    int p;
+    int64_t rb, re;
+    bool valid;
+};
+
+template <int kMaxProbs>
+__device__ Segment find_segment(const GemvParams<kMaxProbs>& P, int p, int64_t rb, int p_end,
+                                int64_t r_end) {
+    for (; p < P.count && p <= p_end; ++p, rb = 0) {
+        const int64_t re = (p == p_end) ? r_end : P.p[p].M;
+        if (re > rb) return Segment{p, rb, re, true};
+    }
+    return Segment{0, 0, 0, false};
+}
+
+// How a segment is cut into work items: 4-row tiles whose K runs in column groups of 8
+// chunks (one stage each); when there are fewer tiles than warps, each tile's column
+// groups split into `ksplit` ranges so every warp works.
+struct SegPlan {
+    int ntiles, ncs, ksplit, items;
+};
+
+__device__ __forceinline__ SegPlan plan_segment(int64_t rows, int C) {
+    SegPlan s;
+    s.ntiles = static_cast<int>((rows + kTileRows - 1) / kTileRows);
+    s.ncs = (C + kLanesPerRow - 1) / kLanesPerRow;
+    s.ksplit = s.ntiles >= kWarps ? 1 : max(1, min(s.ncs, kWarps / s.ntiles));
+    s.items = s.ntiles * s.ksplit;
+    return s;
+}
+
+// Column-group range [cs_begin, cs_end) of k-group kg.
+__device__ __forceinline__ void kgroup_range(const SegPlan& sp, int kg, int& cb, int& ce) {
+    cb = kg * sp.ncs / sp.ksplit;
+    ce = (kg + 1) * sp.ncs / sp.ksplit;
+}
+
+// One warp's walk through its stages: segment -> its items (item = warp, warp + kWarps,
+// ...) -> column pairs of the item. Uniform across the lanes of the warp.
+struct WarpCursor {
+    Segment seg;
+    SegPlan plan;
+    int item, tile;
+    int cs, ce;           // current column group and end of the item's range
+    bool valid;
+};
+
+// Tile and column-group range of the cursor's item. No division when ksplit == 1, the
+// common case (every stage of a K <= 2048 Q4_0 problem is its own item).
+__device__ __forceinline__ void item_bounds(const SegPlan& sp, int item, int& tile, int& cb,
+                                            int& ce) {
+    if (sp.ksplit == 1) {
+        tile = item;
+        cb = 0;
+        ce = sp.ncs;
+    } else {
+        tile = item / sp.ksplit;
+        kgroup_range(sp, item - tile * sp.ksplit, cb, ce);
+    }
+}
+
+template <int kMaxProbs>
+__device__ void cursor_item(const GemvParams<kMaxProbs>& P, WarpCursor& c) {
+    item_bounds(c.plan, c.item, c.tile, c.cs, c.ce);
+}
+
+template <int kMaxProbs>
+__device__ void cursor_enter(const GemvParams<kMaxProbs>& P, WarpCursor& c, Segment seg,
+                             int warp, int p_end, int64_t r_end) {
+    while (seg.valid) {
+        const SegPlan sp = plan_segment(seg.re - seg.rb, P.p[seg.p].C);
+        if (warp < sp.items) {
+            c.seg = seg;
+            c.plan = sp;
+            c.item = warp;
+            c.valid = true;
+            cursor_item(P, c);
+            return;
+        }
+        seg = find_segment(P, seg.p + 1, 0, p_end, r_end);
+    }
+    c.valid = false;
+}
+
+template <int kMaxProbs>
+__device__ void cursor_advance(const GemvParams<kMaxProbs>& P, WarpCursor& c, int warp,
+                               int p_end, int64_t r_end) {
+    if (++c.cs < c.ce) return;
+    c.item += kWarps;
+    if (c.item < c.plan.items) {
+        cursor_item(P, c);
+        return;
+    }
+    cursor_enter(P, c, find_segment(P, c.seg.p + 1, 0, p_end, r_end), warp, p_end, r_end);
+}
+
+__device__ __forceinline__ uint32_t word_at(const uint32_t* r, int byte_off) {
+    const int w = byte_off >> 2;
+    return (byte_off & 3) ? __funnelshift_r(r[w], r[w + 1], 16) : r[w];
+}
+
+__device__ __forceinline__ uint32_t u16_at(const uint32_t* r, int byte_off) {
+    const int w = byte_off >> 2;
+    return (byte_off & 3) ? (r[w] >> 16) : (r[w] & 0xFFFFu);
+}
+
+// Swish(z) = z / (1 + e^-z) ("Development Guide for Small AI Models (TinyLLaMA, etc.)
+// Using C++", section 4.4).
+__device__ __forceinline__ float swish(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// RMSNorm scale of each token of the problem ("Development Guide for Small AI Models
+// (TinyLLaMA, etc.) Using C++", section 4.1): inv[t] = 1 / sqrt(mean_k x^2 + eps). The sum
+// of squares runs in a fixed order (thread strides, a fixed shuffle tree, then the warps
+// in order through `scratch`, kWarps * kNT floats), so it does not depend on timing. All
+// threads of the CTA call it.
+template <int kNT>
+__device__ void rms_scales(const GemvProb& pr, int n_tok, float* scratch, float (&inv)[kNT]) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        float ss = 0.0f;
+        if (t < n_tok) {
+            const float* x = pr.X + static_cast<int64_t>(t) * pr.K;
+            for (int k = threadIdx.x; k < pr.K; k += kThreads) ss = fmaf(x[k], x[k], ss);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        if (lane == 0) scratch[warp * kNT + t] = ss;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        float ss = 0.0f;
+        for (int w = 0; w < kWarps; ++w) ss += scratch[w * kNT + t];
+        inv[t] = 1.0f / sqrtf(ss / static_cast<float>(pr.K) + pr.eps);
+    }
+    __syncthreads();   // scratch is the k-split buffer of the segment that follows
+}
+
+// X (n_tok x K fp32) -> x16 records, one per (token, chunk column). Warp per record.
+// With kNorm (pr.gamma set), each x is first RMS-normalized: x * inv_rms[t] * gamma[k].
+template <int kType, int kNT, bool kNorm>
+__device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbuf,
+                          float* scratch) {
+    using G = Geo<kType>;
+    constexpr int kPerLane = G::kWPC / 32;   // 8 (Q4_0) or 4 (Q8_0) elements
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int C = pr.C;
+    float inv[kNT];
+    if constexpr (kNorm) rms_scales<kNT>(pr, n_tok, scratch, inv);
+    for (int idx = warp; idx < kNT * C; idx += kWarps) {
+        const int t = idx / C;
+        const int col = idx - t * C;
+        uint8_t* rec = xbuf + (t * max_c + col) * G::kXRec;
+        float v[kPerLane];
+        if (t < n_tok) {
+            const float4* src = reinterpret_cast<const float4*>(
+                pr.X + static_cast<int64_t>(t) * pr.K + col * G::kWPC + lane * kPerLane);
+#pragma unroll
+            for (int i = 0; i < kPerLane / 4; ++i) {
+                const float4 f = __ldg(src + i);
+                v[4 * i] = f.x;
+                v[4 * i + 1] = f.y;
+                v[4 * i + 2] = f.z;
+                v[4 * i + 3] = f.w;
+            }
+            if constexpr (kNorm) {
+                float inv_t = inv[0];   // inv[t], kept in registers
+#pragma unroll
+                for (int tt = 1; tt < kNT; ++tt)
+                    if (tt == t) inv_t = inv[tt];
+                const float4* gsrc =
+                    reinterpret_cast<const float4*>(pr.gamma + col * G::kWPC + lane * kPerLane);
+#pragma unroll
+                for (int i = 0; i < kPerLane / 4; ++i) {
+                    const float4 gm = __ldg(gsrc + i);
+                    v[4 * i] = v[4 * i] * inv_t * gm.x;
+                    v[4 * i + 1] = v[4 * i + 1] * inv_t * gm.y;
+                    v[4 * i + 2] = v[4 * i + 2] * inv_t * gm.z;
+                    v[4 * i + 3] = v[4 * i + 3] * inv_t * gm.w;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = warp_max(amax);
+        int e = 0;
+        frexpf(amax, &e);   // amax = f * 2^e, f in [0.5, 1); e = 0 for amax = 0
+        // x16 = rint(x * 2^(15 - e)): an exact power-of-two scaling, then one rounding.
+        // 2^(15-e) as two normal floats (e spans -148..128 for finite inputs).
+        const int sh = 15 - e, sh_a = sh / 2;
+        const float f_a = __int_as_float((sh_a + 127) << 23);
+        const float f_b = __int_as_float((sh - sh_a + 127) << 23);
+        uint32_t packed[kPerLane / 2];
+        int lane_sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPerLane / 2; ++i) {
+            const int a = max(-32767, min(32767, __float2int_rn((v[2 * i] * f_a) * f_b)));
+            const int b = max(-32767, min(32767, __float2int_rn((v[2 * i + 1] * f_a) * f_b)));
+            lane_sum += a + b;
+            packed[i] = (static_cast<uint32_t>(a) & 0xFFFFu) | (static_cast<uint32_t>(b) << 16);
+        }
+        if constexpr (kPerLane == 8) {
+            *reinterpret_cast<uint4*>(rec + lane * 16) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            // Q4_0 block j covers lanes 4j..4j+3 (32 elements): bias = -128 * their sum.
+            lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 1);
+            lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 2);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<int*>(rec + G::kBiasOff + lane) = -128 * lane_sum;
+        } else {
+            *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
+        }
+        if (lane == 0) {
+            // Partial sums come out scaled by 2^(15 - e + kCodeShift); undo with two
+            // power-of-two factors, each a normal float.
+            const int u = e - 15 - Fmt<kType>::kCodeShift, u_a = u / 2;
+            float* sc = reinterpret_cast<float*>(rec + G::kScaleOff);
+            sc[0] = __int_as_float((u_a + 127) << 23);
+            sc[1] = __int_as_float((u - u_a + 127) << 23);
+        }
+    }
+}
+
+__device__ __forceinline__ int dp2a_lo_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// ---------------------------------------------------------------------------------------
+// Quantized activations ("A Complete Guide to llama.cpp and Customization with C++",
+// section 2.2: x_i ~= Delta_x q_x,i, and a block's dot product Delta Delta_x sum q q_x is
+// a pure integer operation). Every 32-element block of x is quantized like a Q8_0 weight
+// block: Delta = max |x| / 127 (IEEE division), q_x = round(x / Delta) (halves away from
+// zero) clamped to [-127, 127], Delta_x = the fp16 value of Delta. Per block the integer
+// sum S = sum q_i q_x,i comes from dp4a (four 8-bit products per instruction), and
+// y += (Delta_w * Delta_x) * S: the scale product is exact in fp32 (11 + 11 bits), S is
+// exact (|S| <= 127 * 127 * 32 < 2^24), one rounding per block.
+// Record of one chunk for one token: kWPC int8 codes, then Delta_x per block (float),
+// then for Q4_0 the sum of the block's codes (int; folds in the weights' -8 offset).
+// Strides of 84 / 36 words (20 / 4 mod 32) put the 8 columns a warp reads in different
+// bank groups.
+// ---------------------------------------------------------------------------------------
+template <int kType>
+struct Q8xRec {
+    using G = Geo<kType>;
+    static constexpr int kScaleOff = G::kWPC;
+    static constexpr int kSumOff = kScaleOff + 4 * G::kBPC;
+    static constexpr int kUsed = kSumOff + (kType == GQ_TYPE_Q4_0 ? 4 * G::kBPC : 0);
+    static constexpr int kXRec = kType == GQ_TYPE_Q4_0 ? 336 : 144;
+    static_assert(kUsed <= kXRec && kXRec % 16 == 0, "record layout");
+};
+
+// Bytes of one chunk's activation record: x16 fixed point (kXM = 0) or Q8_0 codes (1).
+template <int kType, int kXM>
+__host__ __device__ constexpr int xrec_bytes() {
+    return kXM ? Q8xRec<kType>::kXRec : Geo<kType>::kXRec;
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <int kType, int kNT>
+__device__ void prepare_x_q8x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbuf) {
+    using G = Geo<kType>;
+    using R = Q8xRec<kType>;
+    constexpr int kPerLane = G::kWPC / 32;         // 8 (Q4_0 chunk) or 4 (Q8_0 chunk)
+    constexpr int kLanesPerBlock = 32 / kPerLane;  // lanes that share one 32-element block
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int C = pr.C;
+    for (int idx = warp; idx < kNT * C; idx += kWarps) {
+        const int t = idx / C;
+        const int col = idx - t * C;
+        uint8_t* rec = xbuf + (t * max_c + col) * R::kXRec;
+        float v[kPerLane];
+        if (t < n_tok) {
+            const float4* src = reinterpret_cast<const float4*>(
+                pr.X + static_cast<int64_t>(t) * pr.K + col * G::kWPC + lane * kPerLane);
+#pragma unroll
+            for (int i = 0; i < kPerLane / 4; ++i) {
+                const float4 f = __ldg(src + i);
+                v[4 * i] = f.x;
+                v[4 * i + 1] = f.y;
+                v[4 * i + 2] = f.z;
+                v[4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int o = 1; o < kLanesPerBlock; o <<= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float d = amax / 127.0f;
+        uint32_t packed[kPerLane / 4];
+        int sum = 0;
+#pragma unroll
+        for (int w = 0; w < kPerLane / 4; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                int c = 0;
+                if (d != 0.0f) c = max(-127, min(127, static_cast<int>(roundf(v[4 * w + i] / d))));
+                sum += c;
+                word |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * i);
+            }
+            packed[w] = word;
+        }
+        if constexpr (kPerLane == 8)
+            *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
+        else
+            *reinterpret_cast<uint32_t*>(rec + lane * 4) = packed[0];
+#pragma unroll
+        for (int o = 1; o < kLanesPerBlock; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (lane % kLanesPerBlock == 0) {
+            const int j = lane / kLanesPerBlock;
+            reinterpret_cast<float*>(rec + R::kScaleOff)[j] = __half2float(__float2half_rn(d));
+            if constexpr (kType == GQ_TYPE_Q4_0) reinterpret_cast<int*>(rec + R::kSumOff)[j] = sum;
+        }
+    }
+}
+
+// One chunk against every token's Q8_0 record: out[t] += sum over the chunk's blocks of
+// (Delta_w * Delta_x) * S.
+template <int kType, int kNT>
+__device__ __forceinline__ void chunk_dot_q8x(const uint8_t* raw, const uint8_t* xrec0,
+                                              int rec_stride, float (&out)[kNT]) {
+    using G = Geo<kType>;
+    using R = Q8xRec<kType>;
+    uint32_t r[G::kChunkWords];
+    if constexpr (kType == GQ_TYPE_Q4_0) {
+#pragma unroll
+        for (int i = 0; i < G::kChunkWords / 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 * i);
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < G::kChunkWords / 2; ++i) {
+            const uint2 v = *reinterpret_cast<const uint2*>(raw + 8 * i);
+            r[2 * i] = v.x;
+            r[2 * i + 1] = v.y;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < G::kBPC; ++j) {
+        const int base = j * G::kBB;
+        const float dw = half_bits_to_float(u16_at(r, base));
+        uint32_t q[8];
+        if constexpr (kType == GQ_TYPE_Q4_0) {
+            // unsigned codes c: elements 4i..4i+3 in the low nibbles, 16+4i.. in the high
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = word_at(r, base + 2 + 4 * i);
+                q[i] = w & 0x0F0F0F0Fu;
+                q[4 + i] = (w >> 4) & 0x0F0F0F0Fu;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = word_at(r, base + 2 + 4 * i);
+        }
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            const uint8_t* rec = xrec0 + t * rec_stride;
+            const int4 x0 = *reinterpret_cast<const int4*>(rec + 32 * j);
+            const int4 x1 = *reinterpret_cast<const int4*>(rec + 32 * j + 16);
+            const int xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            int S;
+            if constexpr (kType == GQ_TYPE_Q4_0) {
+                S = -8 * reinterpret_cast<const int*>(rec + R::kSumOff)[j];   // sum (c - 8) q_x
+#pragma unroll
+                for (int i = 0; i < 8; ++i) S = dp4a_us(q[i], xs[i], S);
+            } else {
+                S = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) S = __dp4a(static_cast<int>(q[i]), xs[i], S);
+            }
+            const float dx = reinterpret_cast<const float*>(rec + R::kScaleOff)[j];
+            out[t] = fmaf(dw * dx, static_cast<float>(S), out[t]);
+        }
+    }
+}
+
+// One chunk against every token's x16 record: out[t] += chunk partial (scaled by 2^e).
+template <int kType, int kNT>
+__device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xrec0,
+                                          int rec_stride, float (&out)[kNT]) {
+    using G = Geo<kType>;
+    uint32_t r[G::kChunkWords];
+    if constexpr (kType == GQ_TYPE_Q4_0) {
+#pragma unroll
+        for (int i = 0; i < G::kChunkWords / 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 * i);
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < G::kChunkWords / 2; ++i) {
+            const uint2 v = *reinterpret_cast<const uint2*>(raw + 8 * i);
+            r[2 * i] = v.x;
+            r[2 * i + 1] = v.y;
+        }
+    }
+    float acc[kNT];
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) acc[t] = 0.0f;
+
+#pragma unroll
+    for (int j = 0; j < G::kBPC; ++j) {
+        const int base = j * G::kBB;
+        const float d = half_bits_to_float(u16_at(r, base));
+        if constexpr (kType == GQ_TYPE_Q4_0) {
+            // Unsigned codes: lo bytes c (elements 4i..4i+3), hi bytes 16c (16+4i..).
+            // 16 * sum (c - 8) x = 16 * sum_lo c x + sum_hi (16c) x - 128 * sum x.
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t q = word_at(r, base + 2 + 4 * i);
+                lo[i] = q & 0x0F0F0F0Fu;
+                hi[i] = q & 0xF0F0F0F0u;
+            }
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+                const uint8_t* rec = xrec0 + t * rec_stride;
+                const uint4* xw = reinterpret_cast<const uint4*>(rec + 64 * j);
+                const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
+                int sl = 0;
+                int sh = *reinterpret_cast<const int*>(rec + G::kBiasOff + 4 * j);
+                sl = dp2a_lo_su(static_cast<int>(x0.x), lo[0], sl);
+                sl = dp2a_hi_su(static_cast<int>(x0.y), lo[0], sl);
+                sl = dp2a_lo_su(static_cast<int>(x0.z), lo[1], sl);
+                sl = dp2a_hi_su(static_cast<int>(x0.w), lo[1], sl);
+                sh = dp2a_lo_su(static_cast<int>(x2.x), hi[0], sh);
+                sh = dp2a_hi_su(static_cast<int>(x2.y), hi[0], sh);
+                sh = dp2a_lo_su(static_cast<int>(x2.z), hi[1], sh);
+                sh = dp2a_hi_su(static_cast<int>(x2.w), hi[1], sh);
+                sl = dp2a_lo_su(static_cast<int>(x1.x), lo[2], sl);
+                sl = dp2a_hi_su(static_cast<int>(x1.y), lo[2], sl);
+                sl = dp2a_lo_su(static_cast<int>(x1.z), lo[3], sl);
+                sl = dp2a_hi_su(static_cast<int>(x1.w), lo[3], sl);
+                sh = dp2a_lo_su(static_cast<int>(x3.x), hi[2], sh);
+                sh = dp2a_hi_su(static_cast<int>(x3.y), hi[2], sh);
+                sh = dp2a_lo_su(static_cast<int>(x3.z), hi[3], sh);
+                sh = dp2a_hi_su(static_cast<int>(x3.w), hi[3], sh);
+                acc[t] = fmaf(d, static_cast<float>(16 * sl + sh), acc[t]);
+            }
+        } else {
+            uint32_t q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = word_at(r, base + 2 + 4 * i);
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+                const uint4* xw = reinterpret_cast<const uint4*>(xrec0 + t * rec_stride + 64 * j);
+                int s0 = 0, s1 = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 xv = xw[i];
+                    s0 = __dp2a_lo(static_cast<int>(xv.x), static_cast<int>(q[2 * i]), s0);
+                    s0 = __dp2a_hi(static_cast<int>(xv.y), static_cast<int>(q[2 * i]), s0);
+                    s1 = __dp2a_lo(static_cast<int>(xv.z), static_cast<int>(q[2 * i + 1]), s1);
+                    s1 = __dp2a_hi(static_cast<int>(xv.w), static_cast<int>(q[2 * i + 1]), s1);
+                }
+                acc[t] = fmaf(d, static_cast<float>(s0 + s1), acc[t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        const float2 sc = *reinterpret_cast<const float2*>(xrec0 + t * rec_stride + G::kScaleOff);
+        out[t] = fmaf(acc[t] * sc.x, sc.y, out[t]);
+    }
+}
+
+// kXM selects the activation form: 0 = 16-bit block fixed point (exact mul_mat within a
+// proven bound), 1 = Q8_0-quantized activations (the quantized-activation product).
+template <int kType, int kNT, int kMaxProbs, int kXM, int kFuse>
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
+    // kFuse: 0 plain, 1 RMSNorm of X in the preparation, 2 gate/up row pairs (Swish * up)
+    constexpr bool kPair = kFuse == 2;
+    constexpr bool kNorm = kFuse == 1;
+    using G = Geo<kType>;
+    constexpr int kRec = xrec_bytes<kType, kXM>();
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int S = ring_stages<kNT>();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* ring = smem + warp * S * G::kStageBytes;                    // this warp's stages
+    uint8_t* xbuf = smem + kWarps * S * G::kStageBytes;
+    const int rec_stride = P.max_c * kRec;
+    // Partial row sums of k-split items: [item < kWarps][row][token].
+    float* red = reinterpret_cast<float*>(xbuf + kNT * rec_stride);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(red + kWarps * kTileRows * kNT) + warp * S;
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // The next mul_mat of the stream may start on SMs this grid leaves and fill its rings.
+    griddep_launch_dependents();
+
+    // This CTA's rows: from the first row starting at or after byte c*T/G to the first
+    // row starting at or after byte (c+1)*T/G.
+    int p0, p1;
+    int64_t r0, r1;
+    row_at_cost(P, P.total_cost * blockIdx.x / gridDim.x, p0, r0);
+    row_at_cost(P, P.total_cost * (blockIdx.x + 1) / gridDim.x, p1, r1);
+    const Segment first = find_segment(P, p0, r0, p1, r1);
+
+    // Producer side of this warp's ring: the cursor's tile rows, one column group (up to 8
+    // chunks) each. When a column group is a whole row, the tile's rows are contiguous in
+    // memory and one copy fills the stage; otherwise one copy per row.
+    WarpCursor prod;
+    cursor_enter(P, prod, first, warp, p1, r1);
+    int issued = 0;
+    auto issue = [&](int s) {
+        const GemvProb& pr = P.p[prod.seg.p];
+        const int64_t row0 = prod.seg.rb + static_cast<int64_t>(prod.tile) * kTileRows;
+        const int rows = static_cast<int>(min(static_cast<int64_t>(kTileRows), prod.seg.re - row0));
+        const int c0 = kLanesPerRow * prod.cs;
+        const int nc = min(kLanesPerRow, pr.C - c0);
+        const uint32_t row_copy = static_cast<uint32_t>(nc * G::kChunkBytes);
+        const uint32_t bar = smem_addr(&bars[s]);
+        const uint32_t dst = smem_addr(ring + s * G::kStageBytes);
+        const uint8_t* src = pr.W + row0 * pr.row_bytes + static_cast<int64_t>(c0) * G::kChunkBytes;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, row_copy * rows);
+            if constexpr (kPair) {
+                // row 2m + h of the sequence is row m of the gate (h = 0) or up (h = 1) matrix
+                for (int r = 0; r < rows; ++r) {
+                    const int64_t q = row0 + r;
+                    const uint8_t* base_w = (q & 1) ? pr.W2 : pr.W;
+                    bulk_g2s_evict_first(dst + r * G::kRowStride,
+                                         base_w + (q >> 1) * pr.row_bytes +
+                                             static_cast<int64_t>(c0) * G::kChunkBytes,
+                                         row_copy, bar);
+                }
+            } else if (pr.C <= kLanesPerRow) {
+                bulk_g2s_evict_first(dst, src, row_copy * rows, bar);
+            } else {
+                for (int r = 0; r < rows; ++r)
+                    bulk_g2s_evict_first(dst + r * G::kRowStride, src + r * pr.row_bytes,
+                                         row_copy, bar);
+            }
+        }
+        cursor_advance(P, prod, warp, p1, r1);
+        ++issued;
+    };
+    for (int s = 0; s < S && prod.valid; ++s) issue(s);
+    // Only the weights, which no kernel of the call sequence writes, are read above; X and
+    // Y may belong to the previous kernel of the stream, so everything after waits for it.
+    griddep_wait();
+
+    // Consumer side: all warps walk the CTA's segments together (x16 is per problem);
+    // inside a segment each warp works through its own tiles.
+    const int lc = lane % kLanesPerRow;   // which chunk of the column group this lane takes
+    const int rrow = lane / kLanesPerRow; // which row of the tile
+    int consumed = 0;
+    bool timed_out = false;
+    for (Segment seg = first; seg.valid; seg = find_segment(P, seg.p + 1, 0, p1, r1)) {
+        if (__syncthreads_or(timed_out)) break;   // previous segment done everywhere
+        const GemvProb& pr = P.p[seg.p];
+        if constexpr (kXM == 0)
+            prepare_x<kType, kNT, kNorm>(pr, P.n_tok, P.max_c, xbuf, red);
+        else
+            prepare_x_q8x<kType, kNT>(pr, P.n_tok, P.max_c, xbuf);
+        __syncthreads();
+        const SegPlan sp = plan_segment(seg.re - seg.rb, pr.C);
+        for (int item = warp; item < sp.items && !timed_out; item += kWarps) {
+            int tile, cb, ce;
+            item_bounds(sp, item, tile, cb, ce);
+            const int64_t row0 = seg.rb + static_cast<int64_t>(tile) * kTileRows;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(kTileRows), seg.re - row0));
+            float acc[kNT];
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) acc[t] = 0.0f;
+            for (int cs = cb; cs < ce; ++cs) {
+                const int s = consumed % S;
+                if (!mbar_wait(smem_addr(&bars[s]), (consumed / S) & 1)) {
+                    timed_out = true;
+                    break;
+                }
+                const int col = kLanesPerRow * cs + lc;
+                // Whole-row stages hold rows at their global stride; others at kRowStride.
+                const int rs = (!kPair && pr.C <= kLanesPerRow) ? static_cast<int>(pr.row_bytes)
+                                                                 : G::kRowStride;
+                if (rrow < rows && col < pr.C) {
+                    const uint8_t* raw = ring + s * G::kStageBytes + rrow * rs + lc * G::kChunkBytes;
+                    if constexpr (kXM == 0)
+                        chunk_dot<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                    else
+                        chunk_dot_q8x<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                }
+                release_warp_to_async_proxy(__float_as_uint(acc[0]));   // lane 0 refills it
+                ++consumed;
+                if (prod.valid) issue(s);   // refill the stage just read
+            }
+            if (timed_out) break;
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+#pragma unroll
+                for (int o = 1; o < kLanesPerRow; o <<= 1)
+                    acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+            }
+            if constexpr (kPair) {
+                // The up row's sums sit kLanesPerRow lanes above the gate row's.
+                float up[kNT];
+#pragma unroll
+                for (int t = 0; t < kNT; ++t)
+                    up[t] = __shfl_down_sync(0xFFFFFFFFu, acc[t], kLanesPerRow);
+                if (sp.ksplit == 1 && lc == 0 && (rrow & 1) == 0 && rrow < rows) {
+                    const int64_t mh = pr.M >> 1;
+#pragma unroll
+                    for (int t = 0; t < kNT; ++t)
+                        if (t < P.n_tok) pr.Y[t * mh + ((row0 + rrow) >> 1)] = swish(acc[t]) * up[t];
+                }
+            }
+            if (lc == 0 && rrow < rows) {
+                if (sp.ksplit == 1) {
+                    if constexpr (!kPair) {
+#pragma unroll
+                        for (int t = 0; t < kNT; ++t)
+                            if (t < P.n_tok) pr.Y[t * pr.M + row0 + rrow] = acc[t];
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < kNT; ++t) red[(item * kTileRows + rrow) * kNT + t] = acc[t];
+                }
+            }
+        }
+        if (sp.ksplit > 1) {
+            // Sum the k-groups of each row in group order (deterministic).
+            if (__syncthreads_or(timed_out)) break;
+            if constexpr (kPair) {
+                // one output per (gate, up) row pair: Swish(gate) * up
+                const int n_out = sp.ntiles * (kTileRows / 2) * kNT;
+                for (int idx = threadIdx.x; idx < n_out; idx += kThreads) {
+                    const int t = idx % kNT;
+                    const int rr = 2 * ((idx / kNT) % (kTileRows / 2));
+                    const int tile = idx / (kNT * (kTileRows / 2));
+                    const int64_t row = seg.rb + static_cast<int64_t>(tile) * kTileRows + rr;
+                    if (row >= seg.re || t >= P.n_tok) continue;
+                    float g = 0.0f, u = 0.0f;
+                    for (int kg = 0; kg < sp.ksplit; ++kg) {
+                        g += red[((tile * sp.ksplit + kg) * kTileRows + rr) * kNT + t];
+                        u += red[((tile * sp.ksplit + kg) * kTileRows + rr + 1) * kNT + t];
+                    }
+                    pr.Y[t * (pr.M >> 1) + (row >> 1)] = swish(g) * u;
+                }
+            } else {
+                const int n_out = sp.ntiles * kTileRows * kNT;
+                for (int idx = threadIdx.x; idx < n_out; idx += kThreads) {
+                    const int t = idx % kNT;
+                    const int rr = (idx / kNT) % kTileRows;
+                    const int tile = idx / (kNT * kTileRows);
+                    const int64_t row = seg.rb + static_cast<int64_t>(tile) * kTileRows + rr;
+                    if (row >= seg.re || t >= P.n_tok) continue;
+                    float v = 0.0f;
+                    for (int kg = 0; kg < sp.ksplit; ++kg)
+                        v += red[((tile * sp.ksplit + kg) * kTileRows + rr) * kNT + t];
+                    pr.Y[t * pr.M + row] = v;
+                }
+            }
+        }
+    }
+    if (timed_out && lane == 0) report_status(P.status, kStatusTimeout);
+    // Copies still in flight (only after a timeout) must land before the CTA exits.
+    for (int i = consumed; i < issued; ++i)
+        mbar_wait(smem_addr(&bars[i % S]), (i / S) & 1, 100000000ull);
+}
+
+// Any K % 32 == 0: one warp per row, lanes over blocks, fp32 FMA, xor-shuffle reduction
+// (fixed order, so deterministic). Up to kMaxTok tokens per pass.
+template <int kType>
+__global__ void __launch_bounds__(256)
+gemv_generic_kernel(const uint8_t* __restrict__ W, int64_t M, int64_t K,
+                    const float* __restrict__ X, int n_tok, float* __restrict__ Y) {
+    constexpr int kBB = Fmt<kType>::kBB;
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = K / 32;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+         row < M; row += warps) {
+        float acc[kMaxTok] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int64_t b = lane; b < nb; b += 32) {
+            const unsigned short* blk =
+                reinterpret_cast<const unsigned short*>(W + (row * nb + b) * kBB);
+            const float d = half_bits_to_float(__ldg(blk));
+            float w[32];
+            if constexpr (kType == GQ_TYPE_Q4_0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t v = __ldg(blk + 1 + j);
+                    w[2 * j] = static_cast<float>(static_cast<int>(v & 15) - 8) * d;
+                    w[2 * j + 16] = static_cast<float>(static_cast<int>((v >> 4) & 15) - 8) * d;
+                    w[2 * j + 1] = static_cast<float>(static_cast<int>((v >> 8) & 15) - 8) * d;
+                    w[2 * j + 17] = static_cast<float>(static_cast<int>((v >> 12) & 15) - 8) * d;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t v = __ldg(blk + 1 + j);
+                    w[2 * j] = static_cast<float>(static_cast<int8_t>(v & 0xFF)) * d;
+                    w[2 * j + 1] = static_cast<float>(static_cast<int8_t>(v >> 8)) * d;
+                }
+            }
+            for (int t = 0; t < n_tok; ++t) {
+                const float* x = X + t * K + b * 32;
+                float a = acc[t];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a = fmaf(w[i], __ldg(x + i), a);
+                acc[t] = a;
+            }
+        }
+        for (int t = 0; t < n_tok; ++t) {
+            float a = acc[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            if (lane == 0) Y[t * M + row] = a;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------
+template <int kType, int kXM = 0>
+int64_t stream_smem_bytes(int n_tok_template, int max_c) {
+    using G = Geo<kType>;
+    const int stages = n_tok_template <= 3 ? GQ_GEMV_STAGES : GQ_GEMV_STAGES_N4;
+    return static_cast<int64_t>(kWarps) * stages * G::kStageBytes +
+           static_cast<int64_t>(n_tok_template) * max_c * xrec_bytes<kType, kXM>() +
+           static_cast<int64_t>(kWarps) * kTileRows * n_tok_template * 4 +
+           static_cast<int64_t>(kWarps) * stages * 8;
+}
+
+// cudaFuncSetAttribute once per (kernel, device) for the largest size asked so far.
+// Keyed by the kernel's address: instantiations share a function type.
+template <typename KernelT>
+cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int64_t> set_bytes;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), device);
+    auto it = set_bytes.find(key);
+    if (it != set_bytes.end() && it->second >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e == cudaSuccess) set_bytes[key] = bytes;
+    return e;
+}
+
+template <int kType, int kNT, int kMaxProbs, int kXM, int kFuse>
+cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
+    auto kernel = gemv_stream_kernel<kType, kNT, kMaxProbs, kXM, kFuse>;
+    const int64_t smem = stream_smem_bytes<kType, kXM>(kNT, P.max_c);
+    if (smem > info->max_smem_optin) return cudaErrorInvalidValue;   // see stream_eligible
+    cudaError_t e = ensure_smem(kernel, info->device, smem);
+    if (e != cudaSuccess) return e;
+    // Enough CTAs that each streams at least ~32 KB, at most one per SM.
+    int64_t grid = (P.total_bytes + 32767) / 32768;
+    grid = std::max<int64_t>(1, std::min<int64_t>(grid, info->sm_count));
+    // Programmatic dependent launch: this grid's CTAs may start filling their weight rings
+    // while the previous kernel of the stream finishes (the kernel waits for it before it
+    // touches X or Y).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&P};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
+}
+
+template <int kType, int kMaxProbs, int kXM, int kFuse>
+cudaError_t launch_stream_nt(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cudaStream_t s) {
+    switch (P.n_tok) {
+        case 1: return launch_stream_t<kType, 1, kMaxProbs, kXM, kFuse>(P, info, s);
+        case 2: return launch_stream_t<kType, 2, kMaxProbs, kXM, kFuse>(P, info, s);
+        case 3: return launch_stream_t<kType, 3, kMaxProbs, kXM, kFuse>(P, info, s);
+        default: return launch_stream_t<kType, 4, kMaxProbs, kXM, kFuse>(P, info, s);
+    }
+}
+
+template <int kMaxProbs, int kXM = 0, int kFuse = 0>
+cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t tok0,
+                          int n_tok, const DeviceInfo* info, cudaStream_t s) {
+    GemvParams<kMaxProbs> P{};
+    P.count = count;
+    P.n_tok = n_tok;
+    P.status = info->status;
+    const int wpc = t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kWPC : Geo<GQ_TYPE_Q8_0>::kWPC;
+    const int cb = t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kChunkBytes
+                                     : Geo<GQ_TYPE_Q8_0>::kChunkBytes;
+    int64_t bytes = 0, cost = 0;
+    int max_c = 1;
+    for (int i = 0; i < count; ++i) {
+        GemvProb& g = P.p[i];
+        g.W = probs[i].W;
+        g.X = probs[i].X + tok0 * probs[i].K;
+        g.Y = probs[i].Y + tok0 * probs[i].M;
+        g.W2 = probs[i].W2;
+        g.gamma = probs[i].gamma;
+        g.eps = probs[i].eps;
+        g.M = kFuse == 2 ? 2 * probs[i].M : probs[i].M;   // gate/up pairs: two rows per output
+        g.K = static_cast<int32_t>(probs[i].K);
+        g.C = static_cast<int32_t>(probs[i].K / wpc);
+        g.row_bytes = static_cast<int64_t>(g.C) * cb;
+        g.row_cost = g.row_bytes + kGroupCost * ((g.C + kLanesPerRow - 1) / kLanesPerRow);
+        g.cost_begin = cost;
+        bytes += g.M * g.row_bytes;
+        cost += g.M * g.row_cost;
+        max_c = std::max(max_c, g.C);
+    }
+    P.total_bytes = bytes;
+    P.total_cost = cost;
+    P.max_c = max_c;
+    if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs, kXM, kFuse>(P, info, s);
+    return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs, kXM, kFuse>(P, info, s);
+}
+
+cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_tok,
+                           const DeviceInfo* info, cudaStream_t s) {
+    const int64_t blocks = (p.M + 7) / 8;
+    const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(info->sm_count) * 8));
+    const float* X = p.X + tok0 * p.K;
+    float* Y = p.Y + tok0 * p.M;
+    if (t == GQ_TYPE_Q4_0)
+        gemv_generic_kernel<GQ_TYPE_Q4_0><<<grid, 256, 0, s>>>(p.W, p.M, p.K, X, n_tok, Y);
+    else
+        gemv_generic_kernel<GQ_TYPE_Q8_0><<<grid, 256, 0, s>>>(p.W, p.M, p.K, X, n_tok, Y);
+    return cudaGetLastError();
+}
+
+// Shapes and pointers the streaming kernel takes at all (any token count).
+bool stream_shape_ok(const MatProblem& p) {
+    if (p.K % 256 != 0 || p.K > (int64_t(1) << 24)) return false;
+    if (reinterpret_cast<uintptr_t>(p.X) % 16 != 0) return false;
+    return reinterpret_cast<uintptr_t>(p.W) % 16 == 0;
+}
+
+// Whether the shared-memory plan for `n_tok` tokens of this problem fits the device.
+template <int kXM = 0>
+bool stream_fits(gq_type t, const MatProblem& p, int n_tok, const DeviceInfo* info) {
+    const int c = static_cast<int>(p.K / (t == GQ_TYPE_Q4_0 ? 256 : 128));
+    const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0, kXM>(n_tok, c)
+                                           : stream_smem_bytes<GQ_TYPE_Q8_0, kXM>(n_tok, c);
+    return smem <= info->max_smem_optin;
+}
+
+}  // namespace
+
+cudaError_t launch_mul_mat(gq_type t, const MatProblem* probs, int count, int64_t N,
+                           cudaStream_t s) {
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    MatProblem fast[GQ_MAX_BATCH];
+    int64_t step = 0;
+    for (int64_t tok0 = 0; tok0 < N; tok0 += step) {
+        // Tokens in this pass: as many as the x16 buffers of the streamable problems allow
+        // (up to kMaxTok); a problem that does not fit even one token goes to the generic
+        // kernel.
+        int n_tok = static_cast<int>(std::min<int64_t>(kMaxTok, N - tok0));
+        for (; n_tok > 1; --n_tok) {
+            bool all_fit = true;
+            for (int i = 0; i < count && all_fit; ++i)
+                if (stream_shape_ok(probs[i]) && stream_fits(t, probs[i], 1, info))
+                    all_fit = stream_fits(t, probs[i], n_tok, info);
+            if (all_fit) break;
+        }
+        step = n_tok;
+        int n_fast = 0;
+        for (int i = 0; i < count; ++i) {
+            if (stream_shape_ok(probs[i]) && stream_fits(t, probs[i], n_tok, info)) {
+                fast[n_fast++] = probs[i];
+            } else {
+                e = launch_generic(t, probs[i], tok0, n_tok, info, s);
+                if (e != cudaSuccess) return e;
+            }
+        }
+        if (n_fast == 0) continue;
+        if (n_fast == 1)
+            e = launch_stream<1>(t, fast, n_fast, tok0, n_tok, info, s);
+        else if (n_fast <= 16)
+            e = launch_stream<16>(t, fast, n_fast, tok0, n_tok, info, s);
+        else
+            e = launch_stream<GQ_MAX_BATCH>(t, fast, n_fast, tok0, n_tok, info, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+bool q8x_eligible(gq_type t, const MatProblem& p) {
+    DeviceInfo* info = nullptr;
+    if (current_device_info(&info) != cudaSuccess) return false;
+    return stream_shape_ok(p) && stream_fits<1>(t, p, 1, info);
+}
+
+cudaError_t launch_mul_mat_q8x(gq_type t, const MatProblem* probs, int count, int64_t N,
+                               cudaStream_t s) {
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    int64_t step = 0;
+    for (int64_t tok0 = 0; tok0 < N; tok0 += step) {
+        // As many tokens per pass (<= kMaxTokQ8x) as every problem's records allow.
+        int n_tok = static_cast<int>(std::min<int64_t>(kMaxTokQ8x, N - tok0));
+        for (; n_tok > 1; --n_tok) {
+            bool all_fit = true;
+            for (int i = 0; i < count && all_fit; ++i) all_fit = stream_fits<1>(t, probs[i], n_tok, info);
+            if (all_fit) break;
+        }
+        step = n_tok;
+        if (count == 1)
+            e = launch_stream<1, 1>(t, probs, count, tok0, n_tok, info, s);
+        else
+            e = launch_stream<GQ_MAX_BATCH, 1>(t, probs, count, tok0, n_tok, info, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gq
+
+namespace gq {
+
+// Fused forms on the CUDA-core decode kernel: RMSNorm of X in the activation preparation
+// (p.gamma) and the gate/up pair with Swish(gate) * up written directly (p.W2). Shapes the
+// streaming kernel takes only; the caller composes the other shapes from plain kernels.
+bool fused_decode_eligible(gq_type t, const MatProblem& p) {
+    DeviceInfo* info = nullptr;
+    if (current_device_info(&info) != cudaSuccess) return false;
+    if (p.gamma && reinterpret_cast<uintptr_t>(p.gamma) % 16 != 0) return false;   // float4
+    if (p.W2 && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0) return false;         // bulk copies
+    return stream_shape_ok(p) && stream_fits(t, p, 1, info);
+}
+
+cudaError_t launch_mul_mat_fused(gq_type t, const MatProblem& p, int64_t N, cudaStream_t s) {
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    int64_t step = 0;
+    for (int64_t tok0 = 0; tok0 < N; tok0 += step) {
+        int n_tok = static_cast<int>(std::min<int64_t>(kMaxTok, N - tok0));
+        while (n_tok > 1 && !stream_fits(t, p, n_tok, info)) --n_tok;
+        step = n_tok;
+        e = p.W2 ? launch_stream<1, 0, 2>(t, &p, 1, tok0, n_tok, info, s)
+                 : launch_stream<1, 0, 1>(t, &p, 1, tok0, n_tok, info, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gq
