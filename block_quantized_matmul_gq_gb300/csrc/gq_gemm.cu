@@ -368,6 +368,240 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Wide tile: 128 weight rows x 512 tokens per CTA. Each dequantized A stage feeds two
+// MMAs of N = 256 (token halves h = 0, 1, accumulators in TMEM columns [256 h, 256 h +
+// 256)), so the A path -- dequantization, swizzled stores, proxy fence, waits -- is paid
+// once per 2 x 256 tokens. The X tiles of the two halves are separate 32 KB units in a
+// ring of their own; the A stages have theirs.
+// ---------------------------------------------------------------------------------------
+template <int kType>
+struct WideLayout {
+    static constexpr int kHalfN = 256;
+    static constexpr int kRawStages = kType == GQ_TYPE_Q4_0 ? 1 : 2;
+    static constexpr int kAStages = 2;
+    static constexpr int kUnits = kType == GQ_TYPE_Q4_0 ? 5 : 3;
+    static constexpr int kA = kBM * kBK * 2;
+    static constexpr int kU = kHalfN * kBK * 2;
+    static constexpr int kRaw = kBM * RawFmt<kType>::kRow;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kAStages * kA;
+    static constexpr int kOffRaw = kOffB + kUnits * kU;
+    static constexpr int kOffBar = kOffRaw + kRawStages * kRaw;
+    static constexpr int kNumBars = 2 * kAStages + 2 * kUnits + 2 * kRawStages + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr int kTmemCols = 512;
+    static_assert(kU % 1024 == 0 && kA % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned stages");
+    static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
+};
+
+template <int kType>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                 const __grid_constant__ CUtensorMap tmap_x, int M, int N, int K,
+                 float* __restrict__ Y, unsigned* status) {
+    using L = WideLayout<kType>;
+    constexpr int SA = L::kAStages, SU = L::kUnits, R = L::kRawStages;
+    constexpr int kRawWords = RawFmt<kType>::kRow / 4;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_addr - raw_addr);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t sA = base_addr + L::kOffA;
+    const uint32_t sB = base_addr + L::kOffB;
+    const uint32_t sRaw = base_addr + L::kOffRaw;
+    const uint32_t bar0 = base_addr + L::kOffBar;
+    // barrier order: a_full[SA], a_empty[SA], u_full[SU], u_empty[SU], raw_full[R],
+    // raw_empty[R], acc_full
+    auto a_full = [&](int s) { return bar0 + 8u * s; };
+    auto a_empty = [&](int s) { return bar0 + 8u * (SA + s); };
+    auto u_full = [&](int u) { return bar0 + 8u * (2 * SA + u); };
+    auto u_empty = [&](int u) { return bar0 + 8u * (2 * SA + SU + u); };
+    auto raw_full = [&](int r) { return bar0 + 8u * (2 * SA + 2 * SU + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * SA + 2 * SU + R + r); };
+    const uint32_t acc_full = bar0 + 8u * (2 * SA + 2 * SU + 2 * R);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kOffMisc);
+
+    const int m0 = blockIdx.x * kBM;
+    const int n0 = blockIdx.y * (2 * L::kHalfN);
+    const int nsuper = K / kSuperK;
+    const int nk = K / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(a_full(s), 32 * kDequantWarps);
+            mbar_init(a_empty(s), 1);
+        }
+        for (int u = 0; u < SU; ++u) {
+            mbar_init(u_full(u), 1);
+            mbar_init(u_empty(u), 1);
+        }
+        for (int r = 0; r < R; ++r) {
+            mbar_init(raw_full(r), 1);
+            mbar_init(raw_empty(r), 32 * kDequantWarps);
+        }
+        mbar_init(acc_full, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_w);
+            prefetch_tensormap(&tmap_x);
+            int raw_issued = 0, u_issued = 0;
+            bool ok = true;
+            for (int ks = 0; ks < nk && ok; ++ks) {
+                const int want = min(ks / 4 + 2, nsuper);
+                while (raw_issued < want) {
+                    const int j = raw_issued, r = j % R;
+                    if (!mbar_wait(raw_empty(r), ((j / R) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(raw_full(r), L::kRaw);
+                    tma_load_2d(sRaw + r * L::kRaw, &tmap_w,
+                                j * (RawFmt<kType>::kRow / RawFmt<kType>::kElem), m0, raw_full(r));
+                    ++raw_issued;
+                }
+                if (!ok) break;
+                if (ks == 0) griddep_wait();   // the bf16 X of this call is complete
+                for (int h = 0; h < 2; ++h) {
+                    const int ub = 2 * ks + h, u = ub % SU;
+                    if (!mbar_wait(u_empty(u), ((ub / SU) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(u_full(u), L::kU);
+                    tma_load_2d(sB + u * L::kU, &tmap_x, ks * kBK, n0 + h * L::kHalfN, u_full(u));
+                    ++u_issued;
+                }
+            }
+            if (!ok) report_status(status, kStatusTimeout);
+            // Every copy this thread issued must land before the CTA's memory is released.
+            for (int i = max(0, u_issued - SU); i < u_issued; ++i)
+                mbar_wait(u_full(i % SU), (i / SU) & 1, kDrainNs);
+            for (int j = max(0, raw_issued - R); j < raw_issued; ++j)
+                mbar_wait(raw_full(j % R), (j / R) & 1, kDrainNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, L::kHalfN);
+            bool ok = true;
+            for (int ks = 0; ks < nk && ok; ++ks) {
+                const int sa = ks % SA;
+                if (!mbar_wait(a_full(sa), (ks / SA) & 1)) {
+                    ok = false;
+                    break;
+                }
+                for (int h = 0; h < 2; ++h) {
+                    const int ub = 2 * ks + h, u = ub % SU;
+                    if (!mbar_wait(u_full(u), (ub / SU) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t adesc = sw128_kmajor_desc(sA + sa * L::kA + kk * 32);
+                        const uint64_t bdesc = sw128_kmajor_desc(sB + u * L::kU + kk * 32);
+                        umma_bf16(tmem + h * L::kHalfN, adesc, bdesc, idesc,
+                                  (ks | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(u_empty(u));   // X unit u is free once these MMAs have read it
+                }
+                umma_commit(a_empty(sa));      // and A stage sa once both halves have
+            }
+            umma_commit(acc_full);             // accumulators complete (also after a timeout)
+            if (!ok) report_status(status, kStatusTimeout);
+        }
+    } else {
+        // ---------------- dequantize, then epilogue ----------------
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int row = quad * 32 + lane;
+        bool ok = true;
+        for (int j = 0; j < nsuper && ok; ++j) {
+            const int r = j % R;
+            if (!mbar_wait(raw_full(r), (j / R) & 1)) {
+                ok = false;
+                break;
+            }
+            uint32_t raw[kRawWords];
+            const uint8_t* src = base + L::kOffRaw + r * L::kRaw + row * RawFmt<kType>::kRow;
+#pragma unroll
+            for (int i = 0; i < kRawWords / 4; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
+                raw[4 * i] = v.x;
+                raw[4 * i + 1] = v.y;
+                raw[4 * i + 2] = v.z;
+                raw[4 * i + 3] = v.w;
+            }
+            {
+                uint32_t dep = 0;
+#pragma unroll
+                for (int i = 0; i < kRawWords / 4; ++i) dep ^= raw[4 * i];
+                release_to_async_proxy(dep);
+            }
+            mbar_arrive(raw_empty(r));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int ks = 4 * j + q, sa = ks % SA;
+                if (!mbar_wait(a_empty(sa), ((ks / SA) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                dequant_stage<kType>(q, half, raw, base + L::kOffA + sa * L::kA + row * 128, row);
+                fence_proxy_async_smem();
+                mbar_arrive(a_full(sa));
+            }
+        }
+        if (!ok) report_status(status, kStatusTimeout);
+        // Epilogue: warp (quad, half) writes token half `half` of its 32 rows.
+        const bool done = mbar_wait(acc_full, 0);
+        tc_fence_after();
+        if (done && ok) {
+            const int m = m0 + row;
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+            const int c_begin = half * L::kHalfN;
+            const int c_end = min(c_begin + L::kHalfN, N - n0);
+            for (int c = c_begin; c < c_end; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tbase + c, v);
+                if (m < M) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int n = n0 + c + jj;
+                        if (n < N) Y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[jj]);
+                    }
+                }
+            }
+        } else if (!done) {
+            report_status(status, kStatusTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
 // X (fp32, n4 * 4 elements) -> bf16, round to nearest even.
 __global__ void __launch_bounds__(256)
 x_to_bf16_kernel(const float* __restrict__ X, int64_t n, __nv_bfloat16* __restrict__ out) {
@@ -468,6 +702,43 @@ int split_k_ways(KernelT kernel, int smem_bytes, const DeviceInfo* info, int64_t
     return 1;
 }
 
+// Wide (512-token) tiles where their waves, each twice the work, are no more than the
+// 256-token waves: then they save half the per-CTA fill, and Q8_0 also the cost of its
+// longer dequantization. Measured (A/B, one box): TinyLLaMA lm_head N = 512 69.3 -> 61.2 us,
+// LLaMA-7B attn N = 2048 60.8 -> 55.3 us, down 155.4 -> 152.1 us, lm_head Q4_0 399 -> 399 us
+// and Q8_0 533 -> 492 us; gate_up (3 wide waves against 4.5 narrow ones) 148 -> 161 us,
+// which this rule keeps narrow.
+bool use_wide(int64_t mt, int64_t N, int sms) {
+    if (N <= 256) return false;
+    const int64_t w256 = (mt * ((N + 255) / 256) + sms - 1) / sms;
+    const int64_t w512 = (mt * ((N + 511) / 512) + sms - 1) / sms;
+    return 2 * w512 <= w256;
+}
+
+template <int kType>
+cudaError_t launch_wide(CUtensorMap tw, CUtensorMap tx, const MatProblem& p, int64_t N,
+                        int64_t mt, const DeviceInfo* info, cudaStream_t s) {
+    using WL = WideLayout<kType>;
+    auto kernel = gemm_wide_kernel<kType>;
+    cudaError_t e = ensure_smem(kernel, info->device, WL::kAlloc);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(mt), static_cast<unsigned>((N + 511) / 512));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = WL::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int M = static_cast<int>(p.M), n = static_cast<int>(N), K = static_cast<int>(p.K);
+    float* Y = p.Y;
+    unsigned* status = info->status;
+    void* args[] = {&tw, &tx, &M, &n, &K, &Y, &status};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kernel), args);
+}
+
 template <int kType, int kBN>
 cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* xb,
                           const DeviceInfo* info, cudaStream_t s) {
@@ -508,6 +779,8 @@ cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* x
     if (e != cudaSuccess) return e;
     const int64_t mt = (p.M + kBM - 1) / kBM, nt = (N + kBN - 1) / kBN;
     const int Z = split_k_ways(split_kernel, L::kAlloc, info, mt * nt, p.K / kSuperK);
+    if (kBN == 256 && Z == 1 && use_wide(mt, N, info->sm_count))
+        return launch_wide<kType>(tw, tx, p, N, mt, info, s);
     // A programmatic dependent of x_to_bf16_kernel: barrier setup, TMEM allocation, the
     // first weight copies and their dequantization overlap the conversion of X; the
     // producer waits for it (griddepcontrol.wait) before its first X tile copy. Nothing

@@ -412,6 +412,30 @@ def test_llama7b_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
                         rows_per_mat=2)
 
 
+# Shapes whose 256-token tiles fill two or more waves take 512-token tiles (two N = 256
+# MMAs per dequantized A stage): N = 300 leaves the second half mostly empty, N = 777 a
+# 9-token second half in the last tile.
+GEMM_WIDE = [(10240, 512, 300), (9728, 768, 777)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", GEMM_WIDE)
+def test_gemm_wide_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 7, t, N, [workloads.MatShape("wide", M, K)],
+                        rows_per_mat=24)
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+def test_gemm_wide_tiles_deterministic(gq_lib, cuda_dev, t):
+    M, K, N = GEMM_WIDE[1]
+    q = gq_lib.quantize(workloads.weights(M, K, 8, device=cuda_dev), t)
+    X = workloads.activations(N, K, 9, device=cuda_dev)
+    y1 = gq_lib.mul_mat(q, t, M, K, X)
+    y2 = gq_lib.mul_mat(q, t, M, K, X)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert gq_lib.get_last_error() == 0
+
+
 # ------------------------------------------------------------------------------------
 # Tensor-core decode (3 <= N <= 64, K % 256 == 0): grouped, bf16 operands
 # ------------------------------------------------------------------------------------
