@@ -21,6 +21,8 @@
 //               reads. After the K loop the same warps read the accumulator out of TMEM
 //               (tcgen05.ld; warp w owns lanes 32*(w%4).., half the token columns) and
 //               write Y.
+// Shapes whose 256-token tiles fill two or more waves use 512-token tiles instead
+// (gemm_wide_kernel): each dequantized A stage feeds two N = 256 MMAs.
 // With fewer tiles than half the SMs, a tile is shared by a cluster of 2 or 4 CTAs along
 // grid z, each taking a contiguous share of K; each parks its fp32 partial in its own
 // shared memory and, after a cluster barrier, sums a quarter (or half) of the tile's token
