@@ -425,6 +425,18 @@ def test_gemm_wide_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
                         rows_per_mat=24)
 
 
+# Enough 256-token tiles to fill the SMs, too few tokens for 512-token tiles: the plain
+# tile kernel, with a last tile of 124 (M % 4 == 0) or 127 rows and a 200-token tail.
+GEMM_UNSPLIT = [(10236, 256, 200), (10239, 256, 200)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("M,K,N", GEMM_UNSPLIT)
+def test_gemm_unsplit_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 8, t, N, [workloads.MatShape("tile", M, K)],
+                        rows_per_mat=24)
+
+
 @pytest.mark.parametrize("t", ["q4_0", "q8_0"])
 def test_gemm_wide_tiles_deterministic(gq_lib, cuda_dev, t):
     M, K, N = GEMM_WIDE[1]
