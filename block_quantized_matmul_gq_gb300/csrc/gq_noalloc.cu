@@ -8,8 +8,10 @@
 // (its tensor-core path grows a library-owned workspace); this entry point instead uses a
 // fixed array compiled into the library as that workspace.
 //
-// The array below is a file-scope __device__ variable, so every GPU that loads the
-// library holds it (kNoAllocScratchBytes) until the process exits. Host code must not
+// The array below is a file-scope __device__ variable of this module. A GPU holds it
+// (kNoAllocScratchBytes) from the module's first use on that device (CUDA's default lazy
+// module loading), or from context creation when modules load eagerly
+// (CUDA_MODULE_LOADING=EAGER), until the process exits. Host code must not
 // use its name as a pointer: on the host it is only a stand-in. Its device address is
 // looked up once per device with cudaGetSymbolAddress, with that device current, and
 // passed to the kernels.
@@ -23,14 +25,17 @@
 namespace gq {
 namespace {
 
-// Fixed workspace of the tensor-core path: a bf16 copy of X, N * K * 2 bytes, so it
-// covers N * K <= 32 Mi elements (e.g. 2048 tokens x K = 11008, or 4096 x 8192).
+// Fixed workspace of the tensor-core paths. Prefill keeps a bf16 copy of X there, N * K * 2
+// bytes, so it covers N * K <= 32 Mi elements (e.g. 2048 tokens x K = 11008, or 4096 x
+// 8192); the tensor-core decode needs at most 64 * K * 2 + 16 MiB + 4 KiB.
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device, looked up on the first call
-// per device (the "set-up"); later calls reuse it.
+// per device (the "set-up"); later calls reuse it. The cache is never refreshed: after
+// cudaDeviceReset the module loads again at another address, so libgq must not be used
+// on a device again once the process has reset it.
 cudaError_t noalloc_scratch(void** out) {
     static std::mutex mu;
     static void* addr[64] = {};
@@ -72,14 +77,22 @@ extern "C" gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t
         return cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s) == cudaSuccess ? GQ_OK
                                                                             : GQ_ERR_CUDA;
     const gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
-    if (!gq::gemm_eligible(t, p, N))   // decode path: needs no workspace at all
+    const int64_t cap = static_cast<int64_t>(gq::kNoAllocScratchBytes);
+    // Tensor-core decode (3..64 tokens): its bf16 X tiles, partial sums and split-tile
+    // counters fit the array for any K up to ~390k; x_tiles_kernel rewrites the tiles and
+    // zeroes the counters at the start of every call. Past that size, the CUDA-core decode
+    // kernels, which need no workspace.
+    if (gq::gemv_tc_eligible(p, N)) {
+        if (gq::gemv_tc_workspace_bytes(&p, 1, N) > cap)
+            return gq::launch_mul_mat(t, &p, 1, N, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+        void* scratch = nullptr;
+        if (gq::noalloc_scratch(&scratch) != cudaSuccess) return GQ_ERR_CUDA;
+        return gq::launch_gemv_tc(t, &p, 1, N, scratch, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
+    }
+    if (!gq::gemm_eligible(t, p, N))   // CUDA-core decode: needs no workspace at all
         return gq::launch_mul_mat(t, &p, 1, N, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
-    if (static_cast<size_t>(gq::gemm_x_bytes(K, N)) > gq::kNoAllocScratchBytes)
-        return GQ_ERR_SHAPE;           // N * K beyond the fixed scratch
+    if (gq::gemm_x_bytes(K, N) > cap) return GQ_ERR_SHAPE;   // N * K beyond the fixed array
     void* scratch = nullptr;
     if (gq::noalloc_scratch(&scratch) != cudaSuccess) return GQ_ERR_CUDA;
-    return gq::launch_gemm(t, p, N, scratch, static_cast<int64_t>(gq::kNoAllocScratchBytes), s) ==
-                   cudaSuccess
-               ? GQ_OK
-               : GQ_ERR_CUDA;
+    return gq::launch_gemm(t, p, N, scratch, cap, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }

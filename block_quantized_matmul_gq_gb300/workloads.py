@@ -96,3 +96,72 @@ def activations(N: int, K: int, seed: int, device="cpu") -> torch.Tensor:
     """fp32 N x K, N(0, 1), row-major (token n is row n)."""
     g = _gen(seed, device)
     return torch.randn((N, K), generator=g, dtype=torch.float32, device=device).mul_(X_STD)
+
+
+# fp16 bit patterns of the hand-made blocks' scales
+_F16_MAX = 0x7BFF            # 65504, the largest finite fp16
+_F16_SIGN = 0x8000
+
+
+def edge_blocks(t: str, M: int, K: int, seed: int):
+    """Hand-made block bytes (numpy uint8, M x K/32 blocks, the public layout) that the
+    quantizer never writes but the layout allows. Row m has kind m % 8, so every kind
+    lands at every position of a tile:
+      0  every code at its minimum (Q4_0 code 0, i.e. -8; Q8_0 code -128), normal scales
+      1  every code at its minimum, every scale +-65504 (the largest finite fp16)
+      2  random codes, every scale an fp16 subnormal (magnitude 2^-24 .. 1023 * 2^-24)
+      3  random codes, every scale +0 or -0 (the row's outputs are exactly zero)
+      4  only the extreme codes (0 / 15, or -128 / 127), every scale negative
+      5-7 random codes, each block's scale drawn from a mixture of all the above and
+         ordinary N(0, 0.01) scales of either sign
+    Random codes are uniform over every byte value, so Q4_0 code 0 and Q8_0 code -128
+    occur throughout. Only bytes are drawn here; nothing of the method is computed."""
+    import numpy as np
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    rng = np.random.default_rng(seed)
+    nb = K // 32
+    bb = 18 if t == "q4_0" else 34
+    blocks = rng.integers(0, 256, size=(M, nb, bb), dtype=np.uint8)
+    codes = blocks[:, :, 2:]
+    low = 0x00 if t == "q4_0" else 0x80           # Q4_0: both nibbles 0; Q8_0: int8 -128
+    high = 0xFF if t == "q4_0" else 0x7F          # Q4_0: both nibbles 15; Q8_0: 127
+
+    def normal(shape):
+        return (rng.standard_normal(shape) * 0.01).astype(np.float16).view(np.uint16)
+
+    def subnormal(shape):
+        return (rng.integers(1, 1024, shape) | (rng.integers(0, 2, shape) << 15)).astype(np.uint16)
+
+    def huge(shape):
+        mag = rng.uniform(3.0e4, 65504.0, shape).astype(np.float16).view(np.uint16)
+        mag = np.where(rng.random(shape) < 0.5, np.uint16(_F16_MAX), mag)
+        return (mag | (rng.integers(0, 2, shape) << 15)).astype(np.uint16)
+
+    def zero(shape):
+        return (rng.integers(0, 2, shape) << 15).astype(np.uint16)
+
+    scales = np.empty((M, nb), np.uint16)
+    for m in range(M):
+        kind = m % 8
+        if kind == 0:
+            codes[m] = low
+            scales[m] = normal(nb)
+        elif kind == 1:
+            codes[m] = low
+            scales[m] = huge(nb)
+        elif kind == 2:
+            scales[m] = subnormal(nb)
+        elif kind == 3:
+            scales[m] = zero(nb)
+        elif kind == 4:
+            codes[m] = np.where(rng.random(codes[m].shape) < 0.5, low, high).astype(np.uint8)
+            scales[m] = normal(nb) | np.uint16(_F16_SIGN)
+        else:
+            pick = rng.integers(0, 6, nb)
+            cand = np.stack([normal(nb), normal(nb) | np.uint16(_F16_SIGN), subnormal(nb),
+                             zero(nb), huge(nb), normal(nb)])
+            scales[m] = cand[pick, np.arange(nb)]
+    blocks[:, :, 0] = (scales & 0xFF).astype(np.uint8)
+    blocks[:, :, 1] = (scales >> 8).astype(np.uint8)
+    return np.ascontiguousarray(blocks.reshape(M, nb * bb))

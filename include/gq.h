@@ -162,17 +162,22 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * arena, and real-time loops that must not stall or fail on an allocation mid-run. (The
  * pages have no counterpart: their engine allocates once from an arena; this entry point
  * exists for users of this library.)
- * Same arguments, results and accuracy as gq_mul_mat, except that 3 <= N <= 64 runs on
- * the CUDA-core decode kernels. On the prefill path (N >= 65, K % 256 == 0) its workspace
- * is a fixed 64 MiB device array compiled into the library,
- * which every GPU that loads the library holds until the process exits:
- *   - shapes whose workspace N * K * 2 exceeds 64 MiB (N * K > 32 Mi) return GQ_ERR_SHAPE;
+ * Same arguments, paths, results and accuracy as gq_mul_mat. The workspace of its
+ * tensor-core paths is a fixed 64 MiB device array compiled into the library:
+ *   - a GPU holds that array from this module's first use on it (CUDA's default lazy
+ *     module loading) or from context creation (CUDA_MODULE_LOADING=EAGER) until the
+ *     process exits;
+ *   - prefill (N >= 65, K % 256 == 0) keeps a bf16 copy of X there: shapes whose N * K * 2
+ *     exceeds 64 MiB (N * K > 32 Mi) return GQ_ERR_SHAPE;
+ *   - the tensor-core decode (3 <= N <= 64) needs at most 64 * K * 2 bytes + 16 MiB + 4 KiB
+ *     there; a larger K (beyond ~390k) runs on the CUDA-core decode kernels instead;
  *   - the first call on a device looks up that array's device address (set-up); make that
- *     first call before any stream capture on the device;
- *   - every call shares the array (each call rewrites all of it before use), so calls that
- *     overlap on the GPU -- on different streams or devices' concurrent work sharing a
- *     device -- race: serialize them.
- * Up to 64 tokens it uses the CUDA-core decode kernels, which need no workspace.
+ *     first call before any stream capture on the device. The address is kept for the
+ *     life of the process, so libgq must not be used again on a device the process has
+ *     reset with cudaDeviceReset;
+ *   - every call shares the array (each call rewrites what it reads there, and zeroes its
+ *     counters, before use), so calls that overlap on the GPU -- on different streams, or
+ *     from different threads -- race: serialize them.
  */
 gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                              const float* X, int64_t N, float* Y, void* stream);
