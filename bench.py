@@ -9,8 +9,9 @@ seeded N(0, 1) activation vector, run as one gq_mul_mat_batched launch replayed 
 CUDA graph. The weights (582 MB) are larger than the 129 MB L2, so every step streams
 them from HBM. Prints one JSON line (rank 0).
 
---impl reference times the CPU oracle (oracle/, one thread) on a bounded sample of the
-same workload: an R-row slice of every matrix, R sized so the run ends in minutes.
+--impl reference times the CPU oracle (oracle/, unchanged, on every host core: each thread
+runs it on its own rows of every matrix) on a bounded sample of the same workload: an
+R-row slice of every matrix, R sized so the run ends in minutes.
 Under torchrun every rank runs an independent replica of the step (the decode step does
 not shard across GPUs here: "replicas only"); value sums the ranks' bytes over the slowest
 rank's time.
@@ -201,43 +202,55 @@ def sample_bytes(sample) -> int:
     return sum(b.nbytes + X.nbytes + 4 * r * X.shape[0] for b, r, K, X in sample)
 
 
-def cpu_baseline(shapes, target_s: float = 12.0) -> dict:
-    """The oracle as it stands, one thread, on a 64-row slice of every matrix of the step,
-    repeated for about target_s seconds."""
-    sample = oracle_sample(shapes, 64, WORKLOAD_ID)
-    nbytes = sample_bytes(sample)
-    one = max(time_oracle(sample, 1), 1e-3)
-    reps = max(1, int(target_s / one))
-    dt = time_oracle(sample, reps)
-    return {"value": round(nbytes * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"64-row slice of each of the 155 matrices (N=1), {reps} passes, "
-                      f"{dt:.1f} s on one host core"}
+def cpu_baseline(shapes, target_s: float = 6.0) -> dict:
+    """The oracle as it stands on the TinyLLaMA step, repeated for about target_s seconds:
+    at all host cores on a (64 x cores)-row slice of every matrix (each thread runs it on
+    its own 64 rows of every matrix), and at one thread on a 64-row slice."""
+    cores = host_cores()
+    res = {}
+    for threads in (cores, 1):
+        sample = oracle_sample(shapes, 64 * threads, WORKLOAD_ID)
+        nbytes = sample_bytes(sample)
+        one = max(oracle_rows_time("q4_0", sample, threads), 1e-3)
+        reps = max(1, int(target_s / one))
+        dt = sum(oracle_rows_time("q4_0", sample, threads) for _ in range(reps))
+        res[threads] = (nbytes * reps / dt / 1e9, reps, dt)
+    v, reps, dt = res[cores]
+    v1, reps1, dt1 = res[1]
+    return {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{64 * cores}-row slice of each of the 155 matrices (N=1; whole matrix "
+                      f"where smaller), {reps} passes in {dt:.1f} s on {cores} host threads, "
+                      f"64 rows of every matrix per thread",
+            "single_core": {"value": round(v1, 4), "unit": UNIT, "cores": 1,
+                            "sample": f"64-row slice of each matrix, {reps1} passes in "
+                                      f"{dt1:.1f} s"}}
 
 
 def run_reference(args, shapes):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    # Per step: an R-row slice of every matrix; R sized so the whole run takes ~2 min.
-    per_row = 0.0
+    cores = host_cores()
+    # Per step: an R-row slice of every matrix on all host cores; R sized so the whole
+    # run takes about 2 minutes.
     probe = oracle_sample(shapes, 4, WORKLOAD_ID)
-    per_row = max(time_oracle(probe, 1), 1e-4) / 4
+    per_row = max(oracle_rows_time("q4_0", probe, 1), 1e-4) / 4 / cores
     budget = 120.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(2048, budget / per_row)))
+    rows = int(max(cores, min(4096, budget / per_row)))
     sample = oracle_sample(shapes, rows, WORKLOAD_ID)
     for _ in range(args.warmup):
-        time_oracle(sample, 1)
-    dt = time_oracle(sample, args.steps)
+        oracle_rows_time("q4_0", sample, cores)
+    dt = sum(oracle_rows_time("q4_0", sample, cores) for _ in range(args.steps))
     nbytes = sample_bytes(sample)
     value = nbytes * args.steps / dt / 1e9
-    desc = f"{rows}-row slice of each of the 155 matrices per step (N=1), one host core"
+    desc = (f"{rows}-row slice of each of the 155 matrices per step (N=1), {cores} host "
+            f"threads (rows of every matrix split between them)")
     emit({"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
           "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
           "config": {"workload": WORKLOAD_NAME, "sample": desc},
-          "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+          "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                            "kind": "oracle", "sample": desc},
           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0}})
@@ -250,52 +263,66 @@ def run_reference(args, shapes):
 PREFILL_SETS = [("tinyllama_prefill_n512", 4, 512), ("llama7b_prefill_n2048", 5, 2048)]
 
 
-def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None):
+def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None, types=("q4_0", "q8_0"),
+                    rotate: bool = True):
+    """Each prefill matrix as gq_mul_mat_ws calls replayed from a CUDA graph. Weight copies
+    (distinct seeds) are rotated so that every call reads its weights from HBM, not from L2
+    (TinyLLaMA gate / down are 6-7 MB, under the 129 MB L2); X and Y stay the same."""
     import torch
     from block_quantized_matmul_gq_gb300 import binding, workloads
     peak_tf = measured_bf16_peak()
     out = {}
-    for set_name, wl, N in PREFILL_SETS:
-        shapes = workloads.tinyllama_prefill_set() if wl == 4 else workloads.llama7b_set()
-        rows, tot_flop, tot_s = [], 0.0, 0.0
-        for j, sh in enumerate(shapes):
-            if only is not None and (set_name, sh.name) != only:
-                continue
-            W = workloads.weights(sh.M, sh.K, workloads.weight_seed(wl, j), device=dev)
-            q = binding.quantize(W, "q4_0")
-            del W
-            X = workloads.activations(N, sh.K, workloads.act_seed(wl, N, j), device=dev)
-            Y = torch.empty((N, sh.M), device=dev)
-            ws = torch.empty(max(256, binding.workspace_size("q4_0", sh.M, sh.K, N)),
-                             dtype=torch.uint8, device=dev)
-            for _ in range(3):
-                binding.mul_mat_ws(q, "q4_0", sh.M, sh.K, X, ws, out=Y)
-            torch.cuda.synchronize(dev)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for _ in range(reps):
-                    binding.mul_mat_ws(q, "q4_0", sh.M, sh.K, X, ws, out=Y)
-            g.replay()
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(iters):
+    for btype in types:
+        for set_name, wl, N in PREFILL_SETS:
+            shapes = workloads.tinyllama_prefill_set() if wl == 4 else workloads.llama7b_set()
+            rows, tot_flop, tot_s = [], 0.0, 0.0
+            for j, sh in enumerate(shapes):
+                if only is not None and (set_name, sh.name) != only:
+                    continue
+                wbytes = sh.M * binding.row_bytes(btype, sh.K)
+                copies = min(reps, max(1, -(-4 * L2_BYTES // wbytes))) if rotate else 1
+                qs = []
+                for c in range(copies):
+                    W = workloads.weights(sh.M, sh.K, workloads.weight_seed(wl, j) + 100 * c,
+                                          device=dev)
+                    qs.append(binding.quantize(W, btype))
+                    del W
+                X = workloads.activations(N, sh.K, workloads.act_seed(wl, N, j), device=dev)
+                Y = torch.empty((N, sh.M), device=dev)
+                ws = torch.empty(max(256, binding.workspace_size(btype, sh.M, sh.K, N)),
+                                 dtype=torch.uint8, device=dev)
+                for c in range(3):
+                    binding.mul_mat_ws(qs[c % copies], btype, sh.M, sh.K, X, ws, out=Y)
+                torch.cuda.synchronize(dev)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for r in range(reps):
+                        binding.mul_mat_ws(qs[r % copies], btype, sh.M, sh.K, X, ws, out=Y)
                 g.replay()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
-            flop = 2.0 * sh.M * N * sh.K
-            tf = flop / sec / 1e12
-            rows.append({"matrix": sh.name, "M": sh.M, "K": sh.K, "N": N,
-                         "us": round(sec * 1e6, 2), "tflops": round(tf, 1),
-                         "frac": round(tf / peak_tf, 4)})
-            tot_flop += flop
-            tot_s += sec
-            del q, X, Y, ws, g
-        if rows:
-            tf = tot_flop / tot_s / 1e12
-            out[set_name] = {"tflops": round(tf, 1), "frac": round(tf / peak_tf, 4),
-                             "matrices": rows}
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(iters):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+                flop = 2.0 * sh.M * N * sh.K
+                tf = flop / sec / 1e12
+                rows.append({"matrix": sh.name, "M": sh.M, "K": sh.K, "N": N,
+                             "us": round(sec * 1e6, 2), "tflops": round(tf, 1),
+                             "frac": round(tf / peak_tf, 4), "weight_copies_rotated": copies})
+                tot_flop += flop
+                tot_s += sec
+                del qs, X, Y, ws, g
+            if rows:
+                tf = tot_flop / tot_s / 1e12
+                key = set_name if btype == "q4_0" else f"{set_name}_q8_0"
+                out[key] = {"type": btype, "tflops": round(tf, 1), "frac": round(tf / peak_tf, 4),
+                            "matrices": rows}
+        if binding.get_last_error() != 0:
+            raise RuntimeError("device status word set during the prefill sets")
     return out
 
 
@@ -363,7 +390,187 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
             raise RuntimeError("device status word set during the decode sets")
         out[key] = {"type": btype, "matmuls": len(shapes), "weight_bytes": nb1["weights"],
                     "weight_copies_rotated": copies, "per_N": rows}
+        if which == "single":
+            out[key]["launch_floor"] = launch_floor(dev, reps, iters)
         del sets
+    return out
+
+
+def launch_floor(dev, reps: int = 20, iters: int = 5) -> dict:
+    """The same call on a 1 x 256 matrix (144 bytes of blocks), timed exactly like the
+    single 2048 x 2048 product: batched calls on one stream, each a programmatic dependent
+    of the one before, replayed from a CUDA graph. What one call costs when it moves
+    (almost) nothing: launch, grid start-up, one ring fill and the write of Y."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import workloads
+    from block_quantized_matmul_gq_gb300.weightset import QuantizedWeightSet
+    shapes = [workloads.MatShape("tiny", 1, 256)]
+    ws = QuantizedWeightSet.synthetic(9, shapes, "q4_0", dev)
+    xs, ys = ws.make_io(1, 9, dev)
+    arrays = ws.problem_arrays(xs, ys)
+    ws.run(arrays, 1)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            ws.run(arrays, 1)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    return {"M": 1, "K": 256, "us": round(e0.elapsed_time(e1) / (reps * iters) * 1e3, 2)}
+
+
+def dense_context_measure(dev, reps: int = 20, iters: int = 5) -> dict:
+    """Same-box context, not a target: torch.matmul on dense bf16 weights and bf16 X at the
+    workload shapes (the dense path that quantized decode avoids, and the library GEMM
+    that prefill competes with). Weight sets under 4x L2 are copied and rotated."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import workloads
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+
+    def mats(shapes, copies):
+        return [[torch.randn((s.M, s.K), generator=gen, device=dev, dtype=torch.bfloat16)
+                 for s in shapes] for _ in range(copies)]
+
+    def timed(fn):
+        fn(0)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for r in range(reps):
+                fn(r)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (reps * iters) * 1e3   # us
+
+    out = {"what": "torch.matmul, bf16 weights and activations, fp32 accumulate (cuBLAS)",
+           "decode_us": {}, "prefill": {}}
+    sets = [("single_2048x2048", [workloads.MatShape("proj", 2048, 2048)], (1,)),
+            ("tinyllama_decode_step", workloads.tinyllama_decode_set(), (1, 16)),
+            ("llama7b_set", workloads.llama7b_set(), (1, 16))]
+    for name, shapes, Ns in sets:
+        wbytes = sum(2 * s.M * s.K for s in shapes)
+        copies = min(64, max(1, -(-4 * L2_BYTES // wbytes)))
+        Ws = mats(shapes, copies)
+        for N in Ns:
+            Xs = [torch.randn((N, s.K), generator=gen, device=dev, dtype=torch.bfloat16)
+                  for s in shapes]
+            Ys = [torch.empty((N, s.M), device=dev, dtype=torch.bfloat16) for s in shapes]
+
+            def step(r, Ws=Ws, Xs=Xs, Ys=Ys):
+                for W, X, Y in zip(Ws[r % len(Ws)], Xs, Ys):
+                    torch.matmul(X, W.t(), out=Y)
+            out["decode_us"][f"{name}_N{N}"] = round(timed(step), 2)
+        del Ws
+    peak_tf = measured_bf16_peak()
+    for set_name, wl, N in PREFILL_SETS:
+        shapes = workloads.tinyllama_prefill_set() if wl == 4 else workloads.llama7b_set()
+        rows = []
+        for s in shapes:
+            W = torch.randn((s.M, s.K), generator=gen, device=dev, dtype=torch.bfloat16)
+            X = torch.randn((N, s.K), generator=gen, device=dev, dtype=torch.bfloat16)
+            Y = torch.empty((N, s.M), device=dev, dtype=torch.bfloat16)
+            us = timed(lambda r: torch.matmul(X, W.t(), out=Y))
+            tf = 2.0 * s.M * N * s.K / us / 1e6
+            rows.append({"matrix": s.name, "us": round(us, 2), "tflops": round(tf, 1),
+                         "frac": round(tf / peak_tf, 4)})
+            del W, X, Y
+        out["prefill"][set_name] = rows
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# The oracle per workload, on the host cores: one thread, and all cores (each thread runs
+# the unchanged oracle on its own slice of rows; ctypes releases the GIL during the call)
+# --------------------------------------------------------------------------------------
+ORACLE_ENTRIES = [(1, "q4_0", 1), (2, "q4_0", 1), (3, "q8_0", 1), (3, "q8_0", 2),
+                  (3, "q8_0", 4), (3, "q8_0", 8), (3, "q8_0", 16), (4, "q4_0", 512),
+                  (5, "q4_0", 1), (5, "q4_0", 16), (5, "q4_0", 2048)]
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rows_time(btype, sample, threads: int) -> float:
+    """Seconds for the oracle on every (blocks, rows, K, X) of `sample`, the rows of each
+    matrix cut into `threads` contiguous slices run on `threads` threads."""
+    import concurrent.futures
+    import numpy as np
+    import oracle
+    work = [[] for _ in range(threads)]
+    for blocks, r, K, X in sample:
+        for i in range(threads):
+            a, b = r * i // threads, r * (i + 1) // threads
+            if b > a:
+                work[i].append((np.ascontiguousarray(blocks[a:b]), b - a, K, X))
+
+    def run(items):
+        for blk, r, K, X in items:
+            oracle.mul_mat(btype, blk, r, K, X)
+
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(run, work))
+        return time.perf_counter() - t0
+
+
+def oracle_per_config(dev, target_s: float = 0.4) -> dict:
+    """The oracle (as it stands) timed per workload on a row sample of every matrix, at one
+    thread and at all host cores; rates scale to the full workload by its multiply-adds.
+    Inputs: the same seeds and shapes as the GPU arm, drawn on the device and copied."""
+    import oracle
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    cores = host_cores()
+    out = {"cores": cores, "entries": []}
+    for wl, btype, N in ORACLE_ENTRIES:
+        shapes = workloads.WORKLOADS[wl][3]
+        full_mac = sum(s.M * s.K * N for s in shapes)
+        sum_k = sum(s.K for s in shapes)
+        # rows per matrix for about target_s at one thread (about 1e9 multiply-adds per s)
+        r1 = max(1, int(target_s * 1e9 / (N * sum_k)))
+        ra = r1 * cores
+        sample = []
+        for j, s in enumerate(shapes):
+            r = min(ra, s.M)
+            W = workloads.weights(s.M, s.K, workloads.weight_seed(wl, j), device=dev)[:r]
+            sample.append((oracle.quantize(btype, W.cpu().numpy()), r, s.K,
+                           workloads.activations(N, s.K, workloads.act_seed(wl, N, j),
+                                                 device=dev).cpu().numpy()))
+            del W
+        one = [(b[:min(r1, r)], min(r1, r), K, X) for b, r, K, X in sample]
+        t1 = oracle_rows_time(btype, one, 1)
+        ta = oracle_rows_time(btype, sample, cores)
+        mac1 = sum(r * K * N for _, r, K, _ in one)
+        maca = sum(r * K * N for _, r, K, _ in sample)
+        s1 = t1 * full_mac / mac1
+        sa = ta * full_mac / maca
+        e = {"workload": wl, "type": btype, "N": N,
+             "rows_per_matrix": {"one_core": r1, "all_cores": ra},
+             "full_workload_s": {"one_core": round(s1, 3), "all_cores": round(sa, 3)}}
+        if N >= 65:
+            e["tflops"] = {"one_core": round(2 * full_mac / s1 / 1e12, 6),
+                           "all_cores": round(2 * full_mac / sa / 1e12, 6)}
+        else:
+            b = step_bytes(shapes, N, binding.block_bytes(btype))["total"]
+            e["GBps"] = {"one_core": round(b / s1 / 1e9, 4), "all_cores": round(b / sa / 1e9, 4)}
+        out["entries"].append(e)
+        del sample, one
     return out
 
 
@@ -644,6 +851,28 @@ def run_gb300(args, shapes):
     e2e_t, e2e_bytes = aggregate(e2e_t, nb["total"] * e2e_steps, world, dev)
     e2e_value = e2e_bytes / e2e_t / 1e9
 
+    # Where an end-to-end step's time goes: each part alone, recorded and replayed the same
+    # way with a host synchronize per step.
+    def per_step_us(record):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            record()
+        for _ in range(5):
+            g.replay()
+            torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(200):
+            g.replay()
+            torch.cuda.synchronize(dev)
+        return round((time.perf_counter() - t0) / 200 * 1e6, 2)
+
+    e2e_parts = {
+        "h2d_copy_and_sync_us": per_step_us(lambda: X_flat.copy_(X_host, non_blocking=True)),
+        "kernel_and_sync_us": per_step_us(lambda: ws.run(arrays, N)),
+        "d2h_copy_and_sync_us": per_step_us(lambda: Y_host.copy_(Y_flat, non_blocking=True)),
+        "e2e_step_us": round(e2e_t / e2e_steps * 1e6, 2),
+    }
+
     peak, peak_src = measured_peaks()
     traffic = profiled_traffic()
     clk = clocks.summary()
@@ -669,27 +898,65 @@ def run_gb300(args, shapes):
                      "per_launch": "one launch per step: achieved = algorithmic bytes per "
                                    "launch / (CUDA-event step time)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
-                "h2d_bytes_per_step": nb["x"], "d2h_bytes_per_step": nb["y"]},
+                "h2d_bytes_per_step": nb["x"], "d2h_bytes_per_step": nb["y"],
+                "parts": e2e_parts},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     if rank == 0:
-        line["decode"] = {"unit": "GB/s", "peak": peak, "peak_source": line["roofline"]["peak_source"],
-                          **decode_measure(dev)}
-        line["decode_q8x"] = q8x_measure(dev)
-        line["fused"] = fused_measure(dev)
+        # keys in the order they should be read: the compact per-workload summary first,
+        # the details after it
+        line["summary"] = None
+        line["cpu_baseline"] = None
+        dec = decode_measure(dev)
+        q8x = q8x_measure(dev)
+        fused = fused_measure(dev)
         pf = prefill_measure(dev)
+        dense = dense_context_measure(dev)
+        line["summary"] = summarize(dec, pf, dense, peak)
+        line["decode"] = {"unit": "GB/s", "peak": peak,
+                          "peak_source": line["roofline"]["peak_source"], **dec}
+        line["decode_q8x"] = q8x
+        line["fused"] = fused
         line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16 operands, fp32 accumulate",
                            "peak": measured_bf16_peak(),
                            "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json), burst",
                            **pf}
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(shapes)
-    if rank == 0:
+        line["dense_bf16_context"] = dense
+        if args.no_cpu_baseline:
+            del line["cpu_baseline"]
+        else:
+            line["cpu_baseline"] = cpu_baseline(shapes)
+            line["oracle_per_workload"] = oracle_per_config(dev)
         emit(line)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def summarize(dec: dict, pf: dict, dense: dict, peak: float) -> dict:
+    """One short entry per workload (time, rate, fraction of the measured peak), placed
+    ahead of the detailed sections of the line."""
+    def per_n(key):
+        return {f"N{r['N']}": [r["us"], r["GBps"], r["frac"]] for r in dec[key]["per_N"]}
+
+    single = dec["single_q4_0_2048x2048"]
+    r1 = single["per_N"][0]
+    out = {
+        "format": "decode: [us, GB/s, frac of measured HBM]; prefill: [TFLOP/s, frac of "
+                  "measured bf16]",
+        "w1_single_q4_0_2048x2048_N1": [r1["us"], r1["GBps"], r1["frac"]],
+        "w1_launch_floor_us": single["launch_floor"]["us"],
+        "w2_tinyllama_q4_0": per_n("tinyllama_decode_q4_0"),
+        "w3_tinyllama_q8_0": per_n("tinyllama_decode_q8_0"),
+        "w5_llama7b_q4_0": per_n("llama7b_decode_q4_0"),
+    }
+    for key, v in pf.items():
+        out["prefill_" + key] = [v["tflops"], v["frac"]]
+    ctx = dense.get("decode_us", {})
+    if ctx:
+        out["dense_bf16_decode_us"] = ctx
+    return out
 
 
 def main(argv=None):
@@ -704,7 +971,8 @@ def main(argv=None):
                     help="for ncu: warm-up and the timed steps only (no load phase, no e2e, "
                          "no clock sampling, no oracle); prints the device-timed line")
     ap.add_argument("--profile-prefill", metavar="MATRIX", default=None,
-                    help="for ncu: time one prefill GEMM only, e.g. llama7b_prefill_n2048/lm_head")
+                    help="for ncu: time one prefill GEMM only, e.g. llama7b_prefill_n2048/lm_head "
+                         "(llama7b_prefill_n2048_q8_0/lm_head for Q8_0)")
     ap.add_argument("--profile-decode", metavar="TYPE/N", default=None,
                     help="for ncu: the TinyLLaMA decode step at N tokens, e.g. q8_0/16")
     args = ap.parse_args(argv)
@@ -715,7 +983,10 @@ def main(argv=None):
     if args.profile_prefill:
         import torch
         set_name, matrix = args.profile_prefill.split("/")
-        emit(prefill_measure(torch.device("cuda", 0), reps=2, iters=1, only=(set_name, matrix)))
+        btype = "q8_0" if set_name.endswith("_q8_0") else "q4_0"
+        set_name = set_name.replace("_q8_0", "")
+        emit(prefill_measure(torch.device("cuda", 0), reps=2, iters=1, only=(set_name, matrix),
+                             types=(btype,), rotate=False))
         return
     from block_quantized_matmul_gq_gb300 import workloads
     shapes = workloads.tinyllama_decode_set()

@@ -62,7 +62,11 @@ cudaError_t launch_rmsnorm_x(const float* X, const float* gamma, float eps, int6
 
 cudaError_t launch_swiglu(const float* G, const float* U, float* H, int64_t n, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>((n + 255) / 256, int64_t(152) * 16);
+    DeviceInfo* info = nullptr;
+    cudaError_t e = current_device_info(&info);
+    if (e != cudaSuccess) return e;
+    // grid-stride: 16 blocks of 256 threads per SM at most
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, int64_t(info->sm_count) * 16);
     swiglu_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(G, U, H, n);
     return cudaGetLastError();
 }

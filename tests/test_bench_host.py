@@ -70,3 +70,41 @@ def test_reference_arm_sample_sizes():
     sample = bench.oracle_sample(shapes, 2, 2)
     assert [r for _, r, _, _ in sample] == [2, 2, 2]
     assert bench.sample_bytes(sample) == sum(2 * 18 * s.K // 32 + 4 * s.K + 8 for s in shapes)
+
+
+def test_oracle_rows_time_runs_every_slice(monkeypatch):
+    """The all-core oracle timing cuts each matrix's rows into one slice per thread and
+    runs the unchanged oracle on every slice: together the slices are the matrix."""
+    import oracle
+    seen = []
+    real = oracle.mul_mat
+
+    def spy(t, blocks, M, K, X):
+        seen.append((K, blocks.copy()))
+        return real(t, blocks, M, K, X)
+
+    monkeypatch.setattr(oracle, "mul_mat", spy)
+    step = workloads.tinyllama_decode_set()
+    sample = bench.oracle_sample([step[0], step[6]], 7, 2)     # K = 2048 and 5632
+    assert bench.oracle_rows_time("q4_0", sample, 3) > 0
+    assert len(seen) == 3 * len(sample)
+    for blocks, r, K, X in sample:
+        parts = [b for k, b in seen if k == K]
+        assert sum(len(b) for b in parts) == r
+        assert sorted(bytes(row) for b in parts for row in b) == sorted(bytes(row) for row in blocks)
+    assert bench.host_cores() >= 1
+
+
+def test_summarize_keeps_every_workload():
+    row = {"N": 1, "us": 3.0, "GBps": 800.0, "frac": 0.12}
+    dec = {"single_q4_0_2048x2048": {"per_N": [row], "launch_floor": {"us": 2.0}},
+           "tinyllama_decode_q4_0": {"per_N": [dict(row, N=2)]},
+           "tinyllama_decode_q8_0": {"per_N": [row]},
+           "llama7b_decode_q4_0": {"per_N": [row, dict(row, N=16)]}}
+    pf = {"tinyllama_prefill_n512": {"tflops": 900.0, "frac": 0.46},
+          "llama7b_prefill_n2048_q8_0": {"tflops": 1100.0, "frac": 0.56}}
+    s = bench.summarize(dec, pf, {"decode_us": {"single_2048x2048_N1": 4.0}}, 6796.9)
+    assert s["w1_single_q4_0_2048x2048_N1"] == [3.0, 800.0, 0.12]
+    assert s["w1_launch_floor_us"] == 2.0
+    assert set(s["w5_llama7b_q4_0"]) == {"N1", "N16"}
+    assert s["prefill_llama7b_prefill_n2048_q8_0"] == [1100.0, 0.56]
