@@ -11,15 +11,24 @@
 //  * One persistent CTA per SM. All problems of a launch form one sequence of rows; each
 //    CTA takes a contiguous, row-aligned share of equal estimated time (bytes plus a fixed
 //    cost per ring stage), so small matrices (GQA k/v projections) ride along with large
-//    ones and no CTA idles on a tail.
-//  * Inside a CTA, each warp owns tiles of 4 rows; eight lanes share a row and walk its K
-//    columns eight "chunks" at a time (a chunk is 8 Q4_0 blocks = 144 B = 256 weights, or
-//    4 Q8_0 blocks = 136 B = 128 weights), one chunk per lane. Every warp streams its own
+//    ones and no CTA idles on a tail. The host computes the shares and passes them in the
+//    kernel parameters: searching the problem table on the device cost every CTA one
+//    dependent parameter load per earlier problem before its first copy (0.18 us per
+//    problem of the launch, measured).
+//  * Inside a CTA, each warp owns tiles of 4 rows and walks their K columns in column
+//    groups of eight "chunks" (a chunk is 8 Q4_0 blocks = 144 B = 256 weights, or 4 Q8_0
+//    blocks = 136 B = 128 weights), one ring stage per group. Every warp streams its own
 //    tiles through a private ring of shared-memory stages filled by 1-D bulk copies (TMA
 //    cp.async.bulk, L2 evict-first) issued by one lane -- a single copy when the stage
 //    holds whole rows (K <= 2048 for Q4_0), else one per row -- completing on a per-warp
 //    mbarrier; warps never wait for each other inside a problem. Rows are whole chunks
 //    (K % 256 == 0), so copies are 16-byte aligned.
+//  * Lanes and data. Q4_0: lane l takes block pair l (36 bytes) of the column group in all
+//    four rows of the tile, so it reads the pair's activations from shared memory once
+//    per tile, not once per row (with a lane per row and chunk, every 16-byte activation
+//    load cost four shared-memory wavefronts, one per quarter warp, and the wavefronts
+//    ran at 59 % of the pipe's peak). Q8_0 and the quantized-activation form: lane l
+//    takes chunk l % 8 of row l / 8.
 //  * Activations: at each problem boundary the CTA converts X into 16-bit block fixed
 //    point in shared memory (one power-of-two scale 2^e per chunk), so the inner product
 //    of a 32-weight block is EXACT integer arithmetic with dp2a (two 16x8-bit products
@@ -29,12 +38,13 @@
 //    then acc += d * float(S) and, per chunk, partial = acc * 2^e. The only approximation
 //    is x16 = rint(x / 2^e) with |x16| <= 32767, i.e. |error| <= sqrt(256) / 65534 *
 //    ||x|| ||What|| = 0.24 of the bound 1e-3 ||x|| ||What|| (Cauchy-Schwarz per chunk),
-//    whatever the inputs. All lanes of a warp read the same x16 columns (broadcast).
-//  * A lane keeps its row's running sum in registers across all columns; the eight lanes
-//    of a row add their sums with three shuffles at the end. When a CTA's part of a problem
-//    has fewer 4-row tiles than warps, each tile's columns are split between warps and
-//    the per-warp sums are added in a fixed order in shared memory: deterministic, no
-//    atomics.
+//    whatever the inputs.
+//  * A lane keeps its running sums in registers across all columns; at the tile's end
+//    the lanes' sums of each row are added with shuffles in a fixed order (Q4_0: a
+//    transposed reduction of the four rows; otherwise the eight lanes of a row). When a
+//    CTA's part of a problem has fewer 4-row tiles than warps, each tile's columns are
+//    split between warps and the per-warp sums are added in a fixed order in shared
+//    memory: deterministic, no atomics.
 //  * Waits are bounded: a stage that never arrives sets the device status word; the CTA
 //    leaves at the next problem boundary after draining its own copies.
 //  * Fused forms of the same kernel: RMSNorm of X folded into the activation preparation
@@ -106,14 +116,19 @@ struct Geo {
     static constexpr int kRowStride = kLanesPerRow * kChunkBytes;  // 1152 or 1088 in a stage
     // One stage of one warp: 4 rows x 8 chunks, padded to 128-byte multiples.
     static constexpr int kStageBytes = (kTileRows * kRowStride + 127) / 128 * 128;
-    // x16 record of one chunk for one token: kWPC int16; for Q4_0 one int bias per block
-    // (-128 * sum of the block's x16, the code offset 8 folded in); then two float
-    // factors whose product is the chunk's power-of-two scale. Record strides are
-    // 140 / 68 words (12 / 4 mod 32), so the 8 columns a warp reads sit in 8 different
-    // groups of 4 banks: one wavefront per 16-byte load.
-    static constexpr int kBiasOff = kWPC * 2;
-    static constexpr int kScaleOff = kBiasOff + (kType == GQ_TYPE_Q4_0 ? 4 * kBPC : 0);
-    static constexpr int kXRec = kScaleOff + 16;                   // 560 or 272
+    // x16 record of one chunk for one token.
+    //  Q4_0: four 144-byte pair records, one per pair of blocks (64 elements): their 64
+    //   int16, one int bias per block (-128 * sum of the block's x16, the code offset 8
+    //   folded in), then two float factors whose product is the chunk's power-of-two
+    //   scale. A lane reads one pair record (pair_dot_q4); records 9 units of 16 bytes
+    //   apart put the 8 lanes of a quarter warp in 8 different groups of 4 banks.
+    //  Q8_0: kWPC int16, then the two scale factors; record stride 68 words (4 mod 32),
+    //   so the 8 columns a warp reads sit in 8 different groups of 4 banks.
+    static constexpr int kPairRec = 144;
+    static constexpr int kPairBiasOff = 128;
+    static constexpr int kPairScaleOff = 136;
+    static constexpr int kScaleOff = kWPC * 2;                     // Q8_0
+    static constexpr int kXRec = kType == GQ_TYPE_Q4_0 ? 4 * kPairRec : kScaleOff + 16;  // 576 / 272
 };
 
 struct GemvProb {
@@ -136,8 +151,18 @@ struct GemvProb {
     int32_t pad_;
 };
 
+// Largest grid of the streaming kernel: the CTA shares travel as a table of kMaxGrid + 1
+// cuts in the kernel parameters.
+constexpr int kMaxGrid = 256;
+
 template <int kMaxProbs>
 struct GemvParams {
+    // CTA c streams from row cut_r[c] of problem cut_p[c] up to (not including) row
+    // cut_r[c + 1] of problem cut_p[c + 1]; (count, 0) is the end. Computed on the host:
+    // finding them on the device meant a scan of the problem table, one dependent
+    // parameter load per problem, before the CTA's first copy.
+    int64_t cut_r[kMaxGrid + 1];
+    int32_t cut_p[kMaxGrid + 1];
     int32_t count;
     int32_t n_tok;        // valid tokens of this pass, 1..kMaxTok
     int32_t max_c;        // largest C: the x buffer holds kNT * max_c records
@@ -156,9 +181,11 @@ struct GemvParams {
 constexpr int64_t kGroupCost = 576;
 
 // First row (problem p, row r) whose weight begins at or after `cost`; (count, 0) = end.
+// Host side: the cuts of the CTA shares (GemvParams::cut_p / cut_r). Costs increase with
+// the cut, so the search starts at the previous cut's problem `p`.
 template <int kMaxProbs>
-__device__ void row_at_cost(const GemvParams<kMaxProbs>& P, int64_t cost, int& p, int64_t& r) {
-    p = 0;
+void row_at_cost(const GemvParams<kMaxProbs>& P, int64_t cost, int& p, int64_t& r) {
+    p = std::min(p, P.count - 1);
     while (p + 1 < P.count && P.p[p + 1].cost_begin <= cost) ++p;
     const int64_t off = cost - P.p[p].cost_begin;
     r = off <= 0 ? 0 : (off + P.p[p].row_cost - 1) / P.p[p].row_cost;
@@ -385,24 +412,28 @@ __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbu
             lane_sum += a + b;
             packed[i] = (static_cast<uint32_t>(a) & 0xFFFFu) | (static_cast<uint32_t>(b) << 16);
         }
+        // Partial sums come out scaled by 2^(15 - e + kCodeShift); undo with two power-of-two
+        // factors, each a normal float.
+        const int u = e - 15 - Fmt<kType>::kCodeShift, u_a = u / 2;
+        const float sc0 = __int_as_float((u_a + 127) << 23);
+        const float sc1 = __int_as_float((u - u_a + 127) << 23);
         if constexpr (kPerLane == 8) {
-            *reinterpret_cast<uint4*>(rec + lane * 16) =
+            // Q4_0: lane l holds elements 8l..8l+7, i.e. block l / 4 of pair l / 8.
+            uint8_t* prec = rec + (lane >> 3) * G::kPairRec;
+            *reinterpret_cast<uint4*>(prec + (lane & 7) * 16) =
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            // Q4_0 block j covers lanes 4j..4j+3 (32 elements): bias = -128 * their sum.
+            // block j covers lanes 4j..4j+3 (32 elements): bias = -128 * their sum
             lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 1);
             lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 2);
             if ((lane & 3) == 0)
-                *reinterpret_cast<int*>(rec + G::kBiasOff + lane) = -128 * lane_sum;
+                *reinterpret_cast<int*>(prec + G::kPairBiasOff + 4 * ((lane >> 2) & 1)) =
+                    -128 * lane_sum;
+            if ((lane & 7) == 0)
+                *reinterpret_cast<float2*>(prec + G::kPairScaleOff) = make_float2(sc0, sc1);
         } else {
             *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
-        }
-        if (lane == 0) {
-            // Partial sums come out scaled by 2^(15 - e + kCodeShift); undo with two
-            // power-of-two factors, each a normal float.
-            const int u = e - 15 - Fmt<kType>::kCodeShift, u_a = u / 2;
-            float* sc = reinterpret_cast<float*>(rec + G::kScaleOff);
-            sc[0] = __int_as_float((u_a + 127) << 23);
-            sc[1] = __int_as_float((u - u_a + 127) << 23);
+            if (lane == 0)
+                *reinterpret_cast<float2*>(rec + G::kScaleOff) = make_float2(sc0, sc1);
         }
     }
 }
@@ -583,90 +614,42 @@ __device__ __forceinline__ void chunk_dot_q8x(const uint8_t* raw, const uint8_t*
     }
 }
 
-// One chunk against every token's x16 record: out[t] += chunk partial (scaled by 2^e).
-template <int kType, int kNT>
-__device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xrec0,
-                                          int rec_stride, float (&out)[kNT]) {
-    using G = Geo<kType>;
+// Q8_0: one chunk (4 blocks) of one row against every token's x16 record:
+// out[t] += chunk partial (scaled by 2^e).
+template <int kNT>
+__device__ __forceinline__ void chunk_dot_q8(const uint8_t* raw, const uint8_t* xrec0,
+                                             int rec_stride, float (&out)[kNT]) {
+    using G = Geo<GQ_TYPE_Q8_0>;
     uint32_t r[G::kChunkWords];
-    if constexpr (kType == GQ_TYPE_Q4_0) {
 #pragma unroll
-        for (int i = 0; i < G::kChunkWords / 4; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 * i);
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < G::kChunkWords / 2; ++i) {
-            const uint2 v = *reinterpret_cast<const uint2*>(raw + 8 * i);
-            r[2 * i] = v.x;
-            r[2 * i + 1] = v.y;
-        }
+    for (int i = 0; i < G::kChunkWords / 2; ++i) {
+        const uint2 v = *reinterpret_cast<const uint2*>(raw + 8 * i);
+        r[2 * i] = v.x;
+        r[2 * i + 1] = v.y;
     }
     float acc[kNT];
 #pragma unroll
     for (int t = 0; t < kNT; ++t) acc[t] = 0.0f;
-
 #pragma unroll
     for (int j = 0; j < G::kBPC; ++j) {
         const int base = j * G::kBB;
         const float d = half_bits_to_float(u16_at(r, base));
-        if constexpr (kType == GQ_TYPE_Q4_0) {
-            // Unsigned codes: lo bytes c (elements 4i..4i+3), hi bytes 16c (16+4i..).
-            // 16 * sum (c - 8) x = 16 * sum_lo c x + sum_hi (16c) x - 128 * sum x.
-            uint32_t lo[4], hi[4];
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = word_at(r, base + 2 + 4 * i);
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            const uint4* xw = reinterpret_cast<const uint4*>(xrec0 + t * rec_stride + 64 * j);
+            int s0 = 0, s1 = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t q = word_at(r, base + 2 + 4 * i);
-                lo[i] = q & 0x0F0F0F0Fu;
-                hi[i] = q & 0xF0F0F0F0u;
+                const uint4 xv = xw[i];
+                s0 = __dp2a_lo(static_cast<int>(xv.x), static_cast<int>(q[2 * i]), s0);
+                s0 = __dp2a_hi(static_cast<int>(xv.y), static_cast<int>(q[2 * i]), s0);
+                s1 = __dp2a_lo(static_cast<int>(xv.z), static_cast<int>(q[2 * i + 1]), s1);
+                s1 = __dp2a_hi(static_cast<int>(xv.w), static_cast<int>(q[2 * i + 1]), s1);
             }
-#pragma unroll
-            for (int t = 0; t < kNT; ++t) {
-                const uint8_t* rec = xrec0 + t * rec_stride;
-                const uint4* xw = reinterpret_cast<const uint4*>(rec + 64 * j);
-                const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
-                int sl = 0;
-                int sh = *reinterpret_cast<const int*>(rec + G::kBiasOff + 4 * j);
-                sl = dp2a_lo_su(static_cast<int>(x0.x), lo[0], sl);
-                sl = dp2a_hi_su(static_cast<int>(x0.y), lo[0], sl);
-                sl = dp2a_lo_su(static_cast<int>(x0.z), lo[1], sl);
-                sl = dp2a_hi_su(static_cast<int>(x0.w), lo[1], sl);
-                sh = dp2a_lo_su(static_cast<int>(x2.x), hi[0], sh);
-                sh = dp2a_hi_su(static_cast<int>(x2.y), hi[0], sh);
-                sh = dp2a_lo_su(static_cast<int>(x2.z), hi[1], sh);
-                sh = dp2a_hi_su(static_cast<int>(x2.w), hi[1], sh);
-                sl = dp2a_lo_su(static_cast<int>(x1.x), lo[2], sl);
-                sl = dp2a_hi_su(static_cast<int>(x1.y), lo[2], sl);
-                sl = dp2a_lo_su(static_cast<int>(x1.z), lo[3], sl);
-                sl = dp2a_hi_su(static_cast<int>(x1.w), lo[3], sl);
-                sh = dp2a_lo_su(static_cast<int>(x3.x), hi[2], sh);
-                sh = dp2a_hi_su(static_cast<int>(x3.y), hi[2], sh);
-                sh = dp2a_lo_su(static_cast<int>(x3.z), hi[3], sh);
-                sh = dp2a_hi_su(static_cast<int>(x3.w), hi[3], sh);
-                acc[t] = fmaf(d, static_cast<float>(16 * sl + sh), acc[t]);
-            }
-        } else {
-            uint32_t q[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = word_at(r, base + 2 + 4 * i);
-#pragma unroll
-            for (int t = 0; t < kNT; ++t) {
-                const uint4* xw = reinterpret_cast<const uint4*>(xrec0 + t * rec_stride + 64 * j);
-                int s0 = 0, s1 = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 xv = xw[i];
-                    s0 = __dp2a_lo(static_cast<int>(xv.x), static_cast<int>(q[2 * i]), s0);
-                    s0 = __dp2a_hi(static_cast<int>(xv.y), static_cast<int>(q[2 * i]), s0);
-                    s1 = __dp2a_lo(static_cast<int>(xv.z), static_cast<int>(q[2 * i + 1]), s1);
-                    s1 = __dp2a_hi(static_cast<int>(xv.w), static_cast<int>(q[2 * i + 1]), s1);
-                }
-                acc[t] = fmaf(d, static_cast<float>(s0 + s1), acc[t]);
-            }
+            acc[t] = fmaf(d, static_cast<float>(s0 + s1), acc[t]);
         }
     }
 #pragma unroll
@@ -674,6 +657,145 @@ __device__ __forceinline__ void chunk_dot(const uint8_t* raw, const uint8_t* xre
         const float2 sc = *reinterpret_cast<const float2*>(xrec0 + t * rec_stride + G::kScaleOff);
         out[t] = fmaf(acc[t] * sc.x, sc.y, out[t]);
     }
+}
+
+// Q4_0 activations of one lane for one pair of blocks (64 elements), one token: the x16
+// values, the two blocks' biases and the chunk's two scale factors, read from the pair
+// record (Geo<GQ_TYPE_Q4_0>).
+struct PairX {
+    uint4 x[2][4];
+    int bias[2];
+    float2 sc;
+};
+
+__device__ __forceinline__ void load_pair_x(const uint8_t* rec, PairX& X) {
+    using G = Geo<GQ_TYPE_Q4_0>;
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) X.x[b][i] = *reinterpret_cast<const uint4*>(rec + 64 * b + 16 * i);
+    const int4 tail = *reinterpret_cast<const int4*>(rec + G::kPairBiasOff);
+    X.bias[0] = tail.x;
+    X.bias[1] = tail.y;
+    X.sc = make_float2(__int_as_float(tail.z), __int_as_float(tail.w));
+}
+
+// 16 * sum over one Q4_0 block of (c - 8) x16, from its code words split into lo bytes c
+// (elements 4i..4i+3) and hi bytes 16c (elements 16+4i..):
+//     16 * sum_lo c x + sum_hi (16 c) x + bias,   bias = -128 * sum x
+// in four dp2a chains of four (asm is opaque to the compiler, which keeps each chain's
+// order; independent chains give the scheduler work to interleave).
+__device__ __forceinline__ int q4_block_dot(const uint4& x0, const uint4& x1, const uint4& x2,
+                                            const uint4& x3, int bias, const uint32_t (&lo)[4],
+                                            const uint32_t (&hi)[4]) {
+    int sl0 = 0, sl1 = 0, sh1 = 0, sh0 = bias;
+    sl0 = dp2a_lo_su(static_cast<int>(x0.x), lo[0], sl0);
+    sl1 = dp2a_lo_su(static_cast<int>(x0.z), lo[1], sl1);
+    sh0 = dp2a_lo_su(static_cast<int>(x2.x), hi[0], sh0);
+    sh1 = dp2a_lo_su(static_cast<int>(x2.z), hi[1], sh1);
+    sl0 = dp2a_hi_su(static_cast<int>(x0.y), lo[0], sl0);
+    sl1 = dp2a_hi_su(static_cast<int>(x0.w), lo[1], sl1);
+    sh0 = dp2a_hi_su(static_cast<int>(x2.y), hi[0], sh0);
+    sh1 = dp2a_hi_su(static_cast<int>(x2.w), hi[1], sh1);
+    sl0 = dp2a_lo_su(static_cast<int>(x1.x), lo[2], sl0);
+    sl1 = dp2a_lo_su(static_cast<int>(x1.z), lo[3], sl1);
+    sh0 = dp2a_lo_su(static_cast<int>(x3.x), hi[2], sh0);
+    sh1 = dp2a_lo_su(static_cast<int>(x3.z), hi[3], sh1);
+    sl0 = dp2a_hi_su(static_cast<int>(x1.y), lo[2], sl0);
+    sl1 = dp2a_hi_su(static_cast<int>(x1.w), lo[3], sl1);
+    sh0 = dp2a_hi_su(static_cast<int>(x3.y), hi[2], sh0);
+    sh1 = dp2a_hi_su(static_cast<int>(x3.w), hi[3], sh1);
+    return 16 * (sl0 + sl1) + (sh0 + sh1);
+}
+
+// Block b (0 or 1) of a lane's pair in one row: bytes 18b .. 18b + 17 of the pair's 36,
+// held by the five words from byte 16b (block 0: scale in the low half of word 0, codes
+// from byte 2; block 1: scale in the high half of word 0, codes in words 1..4).
+__device__ __forceinline__ float q4_pair_block(const uint8_t* row_pair, int b, uint32_t (&lo)[4],
+                                               uint32_t (&hi)[4]) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(row_pair + 16 * b);
+    uint32_t v[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) v[i] = w[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t q = b == 0 ? __funnelshift_r(v[i], v[i + 1], 16) : v[i + 1];
+        lo[i] = q & 0x0F0F0F0Fu;
+        hi[i] = q & 0xF0F0F0F0u;
+    }
+    return half_bits_to_float(b == 0 ? (v[0] & 0xFFFFu) : (v[0] >> 16));
+}
+
+// Q4_0: one pair of blocks (36 bytes, 64 weights) of each of the tile's `rows` rows against
+// every token's pair record: out[r][t] += the pair's partial (scaled by 2^e). The lane
+// reads the pair's activations once for all four rows of the tile (at one token all of
+// them up front, at more tokens one block at a time), not once per row.
+template <int kNT>
+__device__ __forceinline__ void pair_dot_q4(const uint8_t* raw, int rs, int rows,
+                                            const uint8_t* xp, int rec_stride,
+                                            float (&out)[kTileRows][kNT]) {
+    using G = Geo<GQ_TYPE_Q4_0>;
+    PairX X;
+    if constexpr (kNT == 1) load_pair_x(xp, X);
+    float acc[kTileRows][kNT];
+#pragma unroll
+    for (int r = 0; r < kTileRows; ++r)
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) acc[r][t] = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        uint4 xv[kNT][4];
+        int bias[kNT];
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            if constexpr (kNT == 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xv[t][i] = X.x[b][i];
+                bias[t] = X.bias[b];
+            } else {
+                const uint8_t* x = xp + t * rec_stride + 64 * b;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xv[t][i] = *reinterpret_cast<const uint4*>(x + 16 * i);
+                bias[t] = *reinterpret_cast<const int*>(xp + t * rec_stride + G::kPairBiasOff + 4 * b);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kTileRows; ++r) {
+            if (r >= rows) break;   // uniform across the warp
+            uint32_t lo[4], hi[4];
+            const float d = q4_pair_block(raw + r * rs, b, lo, hi);
+#pragma unroll
+            for (int t = 0; t < kNT; ++t)
+                acc[r][t] = fmaf(d, static_cast<float>(q4_block_dot(xv[t][0], xv[t][1], xv[t][2],
+                                                                    xv[t][3], bias[t], lo, hi)),
+                                 acc[r][t]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kNT; ++t) {
+        const float2 sc = kNT == 1 ? X.sc
+                                   : *reinterpret_cast<const float2*>(xp + t * rec_stride +
+                                                                      G::kPairScaleOff);
+#pragma unroll
+        for (int r = 0; r < kTileRows; ++r) out[r][t] = fmaf(acc[r][t] * sc.x, sc.y, out[r][t]);
+    }
+}
+
+// Sums each row of a 4-row tile over the 32 lanes (lane l holds v[r] for row r) in a fixed
+// order, and leaves row r's total in lanes 8r .. 8r + 7 -- the lanes that own row r in the
+// row-per-8-lanes layout -- with six shuffles: two exchanges halve the rows a lane carries
+// (xor 16: rows 0-1 / 2-3; xor 8: one row each), three more add within groups of eight.
+__device__ __forceinline__ float tile_row_sums(const float (&v)[kTileRows], int lane) {
+    const bool up16 = lane & 16, up8 = lane & 8;
+    float k0 = up16 ? v[2] : v[0], k1 = up16 ? v[3] : v[1];
+    const float s0 = up16 ? v[0] : v[2], s1 = up16 ? v[1] : v[3];
+    k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+    k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+    float k = up8 ? k1 : k0;
+    k += __shfl_xor_sync(0xFFFFFFFFu, up8 ? k0 : k1, 8);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) k += __shfl_xor_sync(0xFFFFFFFFu, k, o);
+    return k;
 }
 
 // kXM selects the activation form: 0 = 16-bit block fixed point (exact mul_mat within a
@@ -684,6 +806,7 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     // kFuse: 0 plain, 1 RMSNorm of X in the preparation, 2 gate/up row pairs (Swish * up)
     constexpr bool kPair = kFuse == 2;
     constexpr bool kNorm = kFuse == 1;
+    constexpr bool kPairMap = kType == GQ_TYPE_Q4_0 && kXM == 0;
     using G = Geo<kType>;
     constexpr int kRec = xrec_bytes<kType, kXM>();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -707,10 +830,8 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
 
     // This CTA's rows: from the first row starting at or after byte c*T/G to the first
     // row starting at or after byte (c+1)*T/G.
-    int p0, p1;
-    int64_t r0, r1;
-    row_at_cost(P, P.total_cost * blockIdx.x / gridDim.x, p0, r0);
-    row_at_cost(P, P.total_cost * (blockIdx.x + 1) / gridDim.x, p1, r1);
+    const int p0 = P.cut_p[blockIdx.x], p1 = P.cut_p[blockIdx.x + 1];
+    const int64_t r0 = P.cut_r[blockIdx.x], r1 = P.cut_r[blockIdx.x + 1];
     const Segment first = find_segment(P, p0, r0, p1, r1);
 
     // Producer side of this warp's ring: the cursor's tile rows, one column group (up to 8
@@ -780,33 +901,65 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
             float acc[kNT];
 #pragma unroll
             for (int t = 0; t < kNT; ++t) acc[t] = 0.0f;
+            // Q4_0 with x16: lane l takes block pair l of the column group in every row of
+            // the tile (acc4[r][t]); otherwise lane l takes chunk lc of row rrow (acc[t]).
+            float acc4[kTileRows][kNT];
+#pragma unroll
+            for (int r = 0; r < kTileRows; ++r)
+#pragma unroll
+                for (int t = 0; t < kNT; ++t) acc4[r][t] = 0.0f;
             for (int cs = cb; cs < ce; ++cs) {
                 const int s = consumed % S;
                 if (!mbar_wait(smem_addr(&bars[s]), (consumed / S) & 1)) {
                     timed_out = true;
                     break;
                 }
-                const int col = kLanesPerRow * cs + lc;
                 // Whole-row stages hold rows at their global stride; others at kRowStride.
                 const int rs = (!kPair && pr.C <= kLanesPerRow) ? static_cast<int>(pr.row_bytes)
                                                                  : G::kRowStride;
-                if (rrow < rows && col < pr.C) {
-                    const uint8_t* raw = ring + s * G::kStageBytes + rrow * rs + lc * G::kChunkBytes;
-                    if constexpr (kXM == 0)
-                        chunk_dot<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
-                    else
-                        chunk_dot_q8x<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                const uint8_t* stage = ring + s * G::kStageBytes;
+                uint32_t dep;   // depends on every shared load of the stage by this lane
+                if constexpr (kPairMap) {
+                    const int col = kLanesPerRow * cs + (lane >> 2);
+                    if (col < pr.C) {
+                        pair_dot_q4<kNT>(stage + lane * (G::kChunkBytes / 4), rs, rows,
+                                         xbuf + col * kRec + (lane & 3) * G::kPairRec,
+                                         rec_stride, acc4);
+                    }
+                    dep = __float_as_uint(acc4[0][0]) ^ __float_as_uint(acc4[1][0]) ^
+                          __float_as_uint(acc4[2][0]) ^ __float_as_uint(acc4[3][0]);
+                } else {
+                    const int col = kLanesPerRow * cs + lc;
+                    if (rrow < rows && col < pr.C) {
+                        const uint8_t* raw = stage + rrow * rs + lc * G::kChunkBytes;
+                        if constexpr (kXM == 0)
+                            chunk_dot_q8<kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                        else
+                            chunk_dot_q8x<kType, kNT>(raw, xbuf + col * kRec, rec_stride, acc);
+                    }
+                    dep = __float_as_uint(acc[0]);
                 }
-                release_warp_to_async_proxy(__float_as_uint(acc[0]));   // lane 0 refills it
+                release_warp_to_async_proxy(dep);   // lane 0 refills it
                 ++consumed;
                 if (prod.valid) issue(s);   // refill the stage just read
             }
             if (timed_out) break;
+            if constexpr (kPairMap) {
+                // row rrow's sum lands in lanes 8 rrow .. 8 rrow + 7, as below
 #pragma unroll
-            for (int t = 0; t < kNT; ++t) {
+                for (int t = 0; t < kNT; ++t) {
+                    float v[kTileRows];
 #pragma unroll
-                for (int o = 1; o < kLanesPerRow; o <<= 1)
-                    acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+                    for (int r = 0; r < kTileRows; ++r) v[r] = acc4[r][t];
+                    acc[t] = tile_row_sums(v, lane);
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < kNT; ++t) {
+#pragma unroll
+                    for (int o = 1; o < kLanesPerRow; o <<= 1)
+                        acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
+                }
             }
             if constexpr (kPair) {
                 // The up row's sums sit kLanesPerRow lanes above the gate row's.
@@ -965,7 +1118,18 @@ cudaError_t launch_stream_t(GemvParams<kMaxProbs>& P, const DeviceInfo* info, cu
     if (e != cudaSuccess) return e;
     // Enough CTAs that each streams at least ~32 KB, at most one per SM.
     int64_t grid = (P.total_bytes + 32767) / 32768;
-    grid = std::max<int64_t>(1, std::min<int64_t>(grid, info->sm_count));
+    grid = std::max<int64_t>(1, std::min<int64_t>({grid, int64_t(info->sm_count), int64_t(kMaxGrid)}));
+    // Each CTA's share: from the first row starting at or after cost c T / G to the first
+    // row starting at or after cost (c + 1) T / G.
+    int p = 0;
+    for (int64_t c = 0; c <= grid; ++c) {
+        int64_t r = 0;
+        int q = p;
+        row_at_cost(P, P.total_cost * c / grid, q, r);
+        P.cut_p[c] = q;
+        P.cut_r[c] = r;
+        p = std::min(q, P.count - 1);
+    }
     // Programmatic dependent launch: this grid's CTAs may start filling their weight rings
     // while the previous kernel of the stream finishes (the kernel waits for it before it
     // touches X or Y).
