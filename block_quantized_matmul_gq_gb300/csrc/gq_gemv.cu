@@ -124,12 +124,17 @@ struct Geo {
     //   apart put the 8 lanes of a quarter warp in 8 different groups of 4 banks.
     //  Q8_0: kWPC int16, then the two scale factors; record stride 68 words (4 mod 32),
     //   so the 8 columns a warp reads sit in 8 different groups of 4 banks.
-    static constexpr int kPairRec = 144;
-    static constexpr int kPairBiasOff = 128;
-    static constexpr int kPairScaleOff = 136;
     static constexpr int kScaleOff = kWPC * 2;                     // Q8_0
-    static constexpr int kXRec = kType == GQ_TYPE_Q4_0 ? 4 * kPairRec : kScaleOff + 16;  // 576 / 272
+    static constexpr int kXRec = kType == GQ_TYPE_Q4_0 ? 4 * 144 : kScaleOff + 16;  // 576 / 272
 };
+
+// Q4_0 pair record (see Geo): 64 int16 x16, two int biases, two float scale factors.
+struct Q4Pair {
+    static constexpr int kRec = 144;
+    static constexpr int kBiasOff = 128;
+    static constexpr int kScaleOff = 136;
+};
+static_assert(Geo<GQ_TYPE_Q4_0>::kXRec == 4 * Q4Pair::kRec, "four pair records per chunk");
 
 struct GemvProb {
     const uint8_t* W;
@@ -419,17 +424,17 @@ __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbu
         const float sc1 = __int_as_float((u - u_a + 127) << 23);
         if constexpr (kPerLane == 8) {
             // Q4_0: lane l holds elements 8l..8l+7, i.e. block l / 4 of pair l / 8.
-            uint8_t* prec = rec + (lane >> 3) * G::kPairRec;
+            uint8_t* prec = rec + (lane >> 3) * Q4Pair::kRec;
             *reinterpret_cast<uint4*>(prec + (lane & 7) * 16) =
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
             // block j covers lanes 4j..4j+3 (32 elements): bias = -128 * their sum
             lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 1);
             lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 2);
             if ((lane & 3) == 0)
-                *reinterpret_cast<int*>(prec + G::kPairBiasOff + 4 * ((lane >> 2) & 1)) =
+                *reinterpret_cast<int*>(prec + Q4Pair::kBiasOff + 4 * ((lane >> 2) & 1)) =
                     -128 * lane_sum;
             if ((lane & 7) == 0)
-                *reinterpret_cast<float2*>(prec + G::kPairScaleOff) = make_float2(sc0, sc1);
+                *reinterpret_cast<float2*>(prec + Q4Pair::kScaleOff) = make_float2(sc0, sc1);
         } else {
             *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
             if (lane == 0)
@@ -674,7 +679,7 @@ __device__ __forceinline__ void load_pair_x(const uint8_t* rec, PairX& X) {
     for (int b = 0; b < 2; ++b)
 #pragma unroll
         for (int i = 0; i < 4; ++i) X.x[b][i] = *reinterpret_cast<const uint4*>(rec + 64 * b + 16 * i);
-    const int4 tail = *reinterpret_cast<const int4*>(rec + G::kPairBiasOff);
+    const int4 tail = *reinterpret_cast<const int4*>(rec + Q4Pair::kBiasOff);
     X.bias[0] = tail.x;
     X.bias[1] = tail.y;
     X.sc = make_float2(__int_as_float(tail.z), __int_as_float(tail.w));
@@ -756,7 +761,7 @@ __device__ __forceinline__ void pair_dot_q4(const uint8_t* raw, int rs, int rows
                 const uint8_t* x = xp + t * rec_stride + 64 * b;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) xv[t][i] = *reinterpret_cast<const uint4*>(x + 16 * i);
-                bias[t] = *reinterpret_cast<const int*>(xp + t * rec_stride + G::kPairBiasOff + 4 * b);
+                bias[t] = *reinterpret_cast<const int*>(xp + t * rec_stride + Q4Pair::kBiasOff + 4 * b);
             }
         }
 #pragma unroll
@@ -775,7 +780,7 @@ __device__ __forceinline__ void pair_dot_q4(const uint8_t* raw, int rs, int rows
     for (int t = 0; t < kNT; ++t) {
         const float2 sc = kNT == 1 ? X.sc
                                    : *reinterpret_cast<const float2*>(xp + t * rec_stride +
-                                                                      G::kPairScaleOff);
+                                                                      Q4Pair::kScaleOff);
 #pragma unroll
         for (int r = 0; r < kTileRows; ++r) out[r][t] = fmaf(acc[r][t] * sc.x, sc.y, out[r][t]);
     }
@@ -923,7 +928,7 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
                     const int col = kLanesPerRow * cs + (lane >> 2);
                     if (col < pr.C) {
                         pair_dot_q4<kNT>(stage + lane * (G::kChunkBytes / 4), rs, rows,
-                                         xbuf + col * kRec + (lane & 3) * G::kPairRec,
+                                         xbuf + col * kRec + (lane & 3) * Q4Pair::kRec,
                                          rec_stride, acc4);
                     }
                     dep = __float_as_uint(acc4[0][0]) ^ __float_as_uint(acc4[1][0]) ^
