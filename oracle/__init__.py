@@ -9,6 +9,9 @@ Every function follows the pages as cited in ``gq_oracle.c``:
   - quantize: "A Complete Guide to llama.cpp and Customization with C++", section 2.2
     (Delta = max |w| / 7, codes in [-8, 7]) and the Q4_0 layout of "Development Guide for
     Small AI Models (TinyLLaMA, etc.) Using C++", section 6.1 (fp16 scale + 16 code bytes).
+  - Q4_K super-blocks: named by the pages (the same two guides, sections 6 and 2.2) without
+    a layout; the oracle follows the published GGUF Q4_K block format (gq_oracle.c) and
+    its own plain min/max quantizer.
   - dequantize / mul_mat: "Development Guide ...", section 6.2 (load, unpack, dequantize,
     FMA) and "No Python! Building an AI Inference Engine Exclusively in C++", sections 6
     and 7.2 (C = A B; Y = X W^T in the cuBLAS call's layout).
@@ -32,7 +35,9 @@ import numpy as np
 
 TYPE_Q4_0 = 2
 TYPE_Q8_0 = 8
-_TYPES = {"q4_0": TYPE_Q4_0, "q8_0": TYPE_Q8_0, TYPE_Q4_0: TYPE_Q4_0, TYPE_Q8_0: TYPE_Q8_0}
+TYPE_Q4_K = 12
+_TYPES = {"q4_0": TYPE_Q4_0, "q8_0": TYPE_Q8_0, "q4_k": TYPE_Q4_K, TYPE_Q4_0: TYPE_Q4_0,
+          TYPE_Q8_0: TYPE_Q8_0, TYPE_Q4_K: TYPE_Q4_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gq_oracle.c")
@@ -70,6 +75,8 @@ def _load():
         lib.oracle_f32_from_fp16_array.restype = None
         lib.oracle_block_bytes.argtypes = [c_int]
         lib.oracle_block_bytes.restype = c_int64
+        lib.oracle_row_bytes.argtypes = [c_int, c_int64]
+        lib.oracle_row_bytes.restype = c_int64
         lib.oracle_quantize.argtypes = [c_int, vp, c_int64, c_int64, vp]
         lib.oracle_quantize.restype = c_int
         lib.oracle_dequantize.argtypes = [c_int, vp, c_int64, c_int64, vp]
@@ -100,12 +107,20 @@ def _f32(a) -> np.ndarray:
 
 
 def block_bytes(t) -> int:
-    """Bytes per 32-weight block: 18 for Q4_0, 34 for Q8_0."""
+    """Bytes per block: 18 for Q4_0 and 34 for Q8_0 (32 weights), 144 for Q4_K (256)."""
     return int(_load().oracle_block_bytes(_type(t)))
 
 
+def block_weights(t) -> int:
+    return 256 if _type(t) == TYPE_Q4_K else 32
+
+
 def row_bytes(t, K: int) -> int:
-    return (K // 32) * block_bytes(t)
+    """Bytes of one row of K weights (K a multiple of block_weights(t))."""
+    rb = int(_load().oracle_row_bytes(_type(t), K))
+    if rb < 0:
+        raise ValueError(f"K = {K} is not a multiple of the {t} block")
+    return rb
 
 
 def fp16_from_f32(x) -> np.ndarray:
@@ -127,8 +142,6 @@ def quantize(t, W) -> np.ndarray:
     """W (M x K fp32) -> uint8 array of shape (M, K/32 * block_bytes)."""
     W = _f32(W)
     M, K = W.shape
-    if K % 32:
-        raise ValueError("K must be a multiple of 32")
     out = np.empty((M, row_bytes(t, K)), dtype=np.uint8)
     rc = _load().oracle_quantize(_type(t), W.ctypes.data, M, K, out.ctypes.data)
     if rc:

@@ -49,6 +49,7 @@
 
 #define ORACLE_TYPE_Q4_0 2
 #define ORACLE_TYPE_Q8_0 8
+#define ORACLE_TYPE_Q4_K 12
 
 /* ---------------------------------------------------------------------------------- */
 /* IEEE 754 binary32 -> binary16, round to nearest, ties to even.                      */
@@ -183,25 +184,172 @@ static void quantize_block_q8_0(const float* w, uint8_t* out)
     }
 }
 
+/* ---------------------------------------------------------------------------------- */
+/* Q4_K super-blocks. The pages name Q4_K as the 4-bit format behind TinyLLaMA's      */
+/* "around 600 MB" ("Development Guide for Small AI Models (TinyLLaMA, etc.) Using    */
+/* C++", section 6; "A Complete Guide to llama.cpp and Customization with C++",       */
+/* section 2.2) but give no layout. This follows the published GGUF Q4_K block format:*/
+/* 256 weights in 8 sub-blocks of 32, 144 bytes:                                       */
+/*   bytes 0-1   d    (fp16): scale of the sub-block scales                            */
+/*   bytes 2-3   dmin (fp16): scale of the sub-block mins                              */
+/*   bytes 4-15  s[0..11]: eight 6-bit scales sc_j and eight 6-bit mins m_j:           */
+/*               j < 4:  sc_j = s[j] & 63,  m_j = s[j + 4] & 63                         */
+/*               j >= 4: sc_j = (s[j + 4] & 15) | (s[j - 4] >> 6) << 4,                 */
+/*                       m_j  = (s[j + 4] >> 4) | (s[j] >> 6) << 4                      */
+/*   bytes 16-143 codes: byte 16 + 32 g + l (g = 0..3, l = 0..31) holds weight         */
+/*               64 g + l in its low nibble and weight 64 g + 32 + l in its high one  */
+/*   What = d sc_j q - dmin m_j for weight with code q in sub-block j: both products  */
+/*   are exact in fp32 (11 + 6 + 4 and 11 + 6 bits), one rounding at the subtraction. */
+/* The quantizer is this oracle's reading (the format fixes only the dequantization): */
+/* per sub-block lo = min(0, min w), hi = max w, step = (hi - lo) / 15, min = -lo;     */
+/* d = max step / 63, dmin = max min / 63 (fp32, stored as fp16);                      */
+/* sc_j = round(step_j / d), m_j = round(min_j / dmin) (fp32 quotients, halves away   */
+/* from zero, clamped to [0, 63]; 0 where d or dmin is 0); codes                       */
+/* round((w + M_j) / D_j) in [0, 15] against the dequantization's own                 */
+/* D_j = fp16(d) sc_j and M_j = fp16(dmin) m_j (0 where D_j = 0).                     */
+/* ---------------------------------------------------------------------------------- */
+#define Q4K_WEIGHTS 256
+#define Q4K_BYTES 144
+
+static void q4k_get_scale_min(const uint8_t* s, int j, int* sc, int* m)
+{
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *m = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+static void q4k_put_scale_min(uint8_t* s, const int* sc, const int* m)
+{
+    for (int j = 0; j < 12; ++j) s[j] = 0;
+    for (int j = 0; j < 4; ++j) {
+        s[j] = (uint8_t)((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+        s[j + 4] = (uint8_t)((m[j] & 63) | ((m[j + 4] >> 4) << 6));
+        s[j + 8] = (uint8_t)((sc[j + 4] & 15) | ((m[j + 4] & 15) << 4));
+    }
+}
+
+static void quantize_superblock_q4_k(const float* w, uint8_t* out)
+{
+    float step[8], mn[8];
+    for (int j = 0; j < 8; ++j) {
+        const float* v = w + 32 * j;
+        float lo = v[0], hi = v[0];
+        for (int i = 1; i < 32; ++i) {
+            if (v[i] < lo) lo = v[i];
+            if (v[i] > hi) hi = v[i];
+        }
+        if (lo > 0.0f) lo = 0.0f;
+        step[j] = (hi - lo) / 15.0f;
+        mn[j] = 0.0f - lo;
+    }
+    float smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        if (step[j] > smax) smax = step[j];
+        if (mn[j] > mmax) mmax = mn[j];
+    }
+    const float d = smax / 63.0f;
+    const float dmin = mmax / 63.0f;
+    const uint16_t dh = oracle_fp16_from_f32(d);
+    const uint16_t dminh = oracle_fp16_from_f32(dmin);
+    int sc[8], m[8];
+    for (int j = 0; j < 8; ++j) {
+        int a = 0, b = 0;
+        if (d != 0.0f) {
+            a = (int)roundf(step[j] / d);
+            if (a < 0) a = 0;
+            if (a > 63) a = 63;
+        }
+        if (dmin != 0.0f) {
+            b = (int)roundf(mn[j] / dmin);
+            if (b < 0) b = 0;
+            if (b > 63) b = 63;
+        }
+        sc[j] = a;
+        m[j] = b;
+    }
+    put_u16_le(out, dh);
+    put_u16_le(out + 2, dminh);
+    q4k_put_scale_min(out + 4, sc, m);
+    const float df = oracle_f32_from_fp16(dh), dminf = oracle_f32_from_fp16(dminh);
+    int code[Q4K_WEIGHTS];
+    for (int j = 0; j < 8; ++j) {
+        const float D = df * (float)sc[j];
+        const float M = dminf * (float)m[j];
+        for (int i = 0; i < 32; ++i) {
+            int q = 0;
+            if (D != 0.0f) {
+                q = (int)roundf((w[32 * j + i] + M) / D);
+                if (q < 0) q = 0;
+                if (q > 15) q = 15;
+            }
+            code[32 * j + i] = q;
+        }
+    }
+    for (int g = 0; g < 4; ++g)
+        for (int l = 0; l < 32; ++l)
+            out[16 + 32 * g + l] = (uint8_t)(code[64 * g + l] | (code[64 * g + 32 + l] << 4));
+}
+
+static void dequantize_superblock_q4_k(const uint8_t* blk, float* w)
+{
+    const float d = oracle_f32_from_fp16(get_u16_le(blk));
+    const float dmin = oracle_f32_from_fp16(get_u16_le(blk + 2));
+    for (int j = 0; j < 8; ++j) {
+        int sc, m;
+        q4k_get_scale_min(blk + 4, j, &sc, &m);
+        const float D = d * (float)sc;         /* exact */
+        const float M = dmin * (float)m;       /* exact */
+        const int g = j / 2, high = j % 2;
+        for (int l = 0; l < 32; ++l) {
+            const int byte = blk[16 + 32 * g + l];
+            const int q = high ? (byte >> 4) : (byte & 15);
+            w[32 * j + l] = D * (float)q - M;  /* D q exact; one rounding */
+        }
+    }
+}
+
+/* Bytes of one block: 18 (Q4_0) and 34 (Q8_0) per 32 weights; 144 (Q4_K) per 256. */
 int64_t oracle_block_bytes(int type)
 {
     if (type == ORACLE_TYPE_Q4_0) return 2 + 16;
     if (type == ORACLE_TYPE_Q8_0) return 2 + 32;
+    if (type == ORACLE_TYPE_Q4_K) return Q4K_BYTES;
     return -1;
 }
 
-/* W: M x K fp32 row-major, K a multiple of 32. out: M * K/32 blocks, row-major. */
+/* Weights per block: 32, or 256 for Q4_K. */
+static int64_t block_weights(int type)
+{
+    return type == ORACLE_TYPE_Q4_K ? Q4K_WEIGHTS : 32;
+}
+
+/* Bytes of one row of K weights (K a multiple of the block's weights), else -1. */
+int64_t oracle_row_bytes(int type, int64_t K)
+{
+    const int64_t bb = oracle_block_bytes(type);
+    if (bb < 0 || K < 0 || K % block_weights(type) != 0) return -1;
+    return K / block_weights(type) * bb;
+}
+
+/* W: M x K fp32 row-major, K a multiple of the block's weights. out: the blocks of each
+   row, rows in order. */
 int oracle_quantize(int type, const float* W, int64_t M, int64_t K, uint8_t* out)
 {
     const int64_t bb = oracle_block_bytes(type);
-    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0) return -1;
-    const int64_t nb = K / 32;
+    if (bb < 0 || M < 0 || oracle_row_bytes(type, K) < 0) return -1;
+    const int64_t bw = block_weights(type);
+    const int64_t nb = K / bw;
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t b = 0; b < nb; ++b) {
-            const float* w = W + m * K + b * 32;
+            const float* w = W + m * K + b * bw;
             uint8_t* o = out + (m * nb + b) * bb;
             if (type == ORACLE_TYPE_Q4_0) quantize_block_q4_0(w, o);
-            else quantize_block_q8_0(w, o);
+            else if (type == ORACLE_TYPE_Q8_0) quantize_block_q8_0(w, o);
+            else quantize_superblock_q4_k(w, o);
         }
     }
     return 0;
@@ -213,6 +361,10 @@ int oracle_quantize(int type, const float* W, int64_t M, int64_t K, uint8_t* out
 /* ---------------------------------------------------------------------------------- */
 static void dequantize_block(int type, const uint8_t* blk, float* w)
 {
+    if (type == ORACLE_TYPE_Q4_K) {
+        dequantize_superblock_q4_k(blk, w);
+        return;
+    }
     const float d = oracle_f32_from_fp16(get_u16_le(blk));
     if (type == ORACLE_TYPE_Q4_0) {
         for (int j = 0; j < 16; ++j) {
@@ -227,14 +379,18 @@ static void dequantize_block(int type, const uint8_t* blk, float* w)
     }
 }
 
+/* One row of K weights (all its blocks) into w. */
+static void dequantize_row(int type, const uint8_t* row, int64_t K, float* w)
+{
+    const int64_t bb = oracle_block_bytes(type), bw = block_weights(type);
+    for (int64_t b = 0; b < K / bw; ++b) dequantize_block(type, row + b * bb, w + b * bw);
+}
+
 int oracle_dequantize(int type, const uint8_t* blocks, int64_t M, int64_t K, float* out)
 {
-    const int64_t bb = oracle_block_bytes(type);
-    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0) return -1;
-    const int64_t nb = K / 32;
-    for (int64_t m = 0; m < M; ++m)
-        for (int64_t b = 0; b < nb; ++b)
-            dequantize_block(type, blocks + (m * nb + b) * bb, out + m * K + b * 32);
+    const int64_t rb = oracle_row_bytes(type, K);
+    if (rb < 0 || M < 0) return -1;
+    for (int64_t m = 0; m < M; ++m) dequantize_row(type, blocks + m * rb, K, out + m * K);
     return 0;
 }
 
@@ -246,12 +402,10 @@ int oracle_dequantize(int type, const uint8_t* blocks, int64_t M, int64_t K, flo
 int oracle_mul_mat(int type, const uint8_t* blocks, int64_t M, int64_t K,
                    const float* X, int64_t N, float* Y, float* wrow)
 {
-    const int64_t bb = oracle_block_bytes(type);
-    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0 || N < 0) return -1;
-    const int64_t nb = K / 32;
+    const int64_t rb = oracle_row_bytes(type, K);
+    if (rb < 0 || M < 0 || N < 0) return -1;
     for (int64_t m = 0; m < M; ++m) {
-        for (int64_t b = 0; b < nb; ++b)
-            dequantize_block(type, blocks + (m * nb + b) * bb, wrow + b * 32);
+        dequantize_row(type, blocks + m * rb, K, wrow);
         for (int64_t n = 0; n < N; ++n) {
             const float* x = X + n * K;
             double acc = 0.0;
@@ -289,6 +443,7 @@ int oracle_mul_mat_q8x(int type, const uint8_t* blocks, int64_t M, int64_t K,
                        const float* X, int64_t N, float* Y, uint8_t* xq)
 {
     const int64_t bb = oracle_block_bytes(type);
+    if (type == ORACLE_TYPE_Q4_K) return -1;   /* defined for the 32-weight block types */
     if (bb < 0 || K % 32 != 0 || M < 0 || K < 0 || N < 0) return -1;
     const int64_t nb = K / 32;
     if (oracle_quantize(ORACLE_TYPE_Q8_0, X, N, K, xq) != 0) return -1;
@@ -324,9 +479,8 @@ int oracle_mul_mat_rmsnorm(int type, const uint8_t* blocks, int64_t M, int64_t K
                            const float* X, const float* gamma, double eps, int64_t N,
                            float* Y, float* wrow, double* xhat)
 {
-    const int64_t bb = oracle_block_bytes(type);
-    if (bb < 0 || K % 32 != 0 || M < 0 || K <= 0 || N < 0) return -1;
-    const int64_t nb = K / 32;
+    const int64_t rb = oracle_row_bytes(type, K);
+    if (rb < 0 || M < 0 || K <= 0 || N < 0) return -1;
     for (int64_t n = 0; n < N; ++n) {
         const float* x = X + n * K;
         double ss = 0.0;
@@ -334,8 +488,7 @@ int oracle_mul_mat_rmsnorm(int type, const uint8_t* blocks, int64_t M, int64_t K
         const double rms = sqrt(ss / (double)K + eps);
         for (int64_t k = 0; k < K; ++k) xhat[k] = (double)x[k] / rms * (double)gamma[k];
         for (int64_t m = 0; m < M; ++m) {
-            for (int64_t b = 0; b < nb; ++b)
-                dequantize_block(type, blocks + (m * nb + b) * bb, wrow + b * 32);
+            dequantize_row(type, blocks + m * rb, K, wrow);
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) acc += (double)wrow[k] * xhat[k];
             Y[n * M + m] = (float)acc;
@@ -355,16 +508,13 @@ int oracle_mul_mat_rmsnorm(int type, const uint8_t* blocks, int64_t M, int64_t K
 int oracle_mul_mat_swiglu(int type, const uint8_t* gate, const uint8_t* up, int64_t M,
                           int64_t K, const float* X, int64_t N, float* H, float* wrow)
 {
-    const int64_t bb = oracle_block_bytes(type);
-    if (bb < 0 || K % 32 != 0 || M < 0 || K < 0 || N < 0) return -1;
-    const int64_t nb = K / 32;
+    const int64_t rb = oracle_row_bytes(type, K);
+    if (rb < 0 || M < 0 || N < 0) return -1;
     float* wg = wrow;
     float* wu = wrow + K;
     for (int64_t m = 0; m < M; ++m) {
-        for (int64_t b = 0; b < nb; ++b) {
-            dequantize_block(type, gate + (m * nb + b) * bb, wg + b * 32);
-            dequantize_block(type, up + (m * nb + b) * bb, wu + b * 32);
-        }
+        dequantize_row(type, gate + m * rb, K, wg);
+        dequantize_row(type, up + m * rb, K, wu);
         for (int64_t n = 0; n < N; ++n) {
             const float* x = X + n * K;
             double g = 0.0, u = 0.0;

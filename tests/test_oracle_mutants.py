@@ -49,7 +49,21 @@ MUTANTS = {
                      "H[n * M + m] = (float)(g / (1.0 + exp(-g)));"),
     "swiglu_roles_swapped": ("H[n * M + m] = (float)(g / (1.0 + exp(-g)) * u);",
                              "H[n * M + m] = (float)(u / (1.0 + exp(-u)) * g);"),
+    # Q4_K super-blocks
+    "q4k_nibble_order": ("(uint8_t)(code[64 * g + l] | (code[64 * g + 32 + l] << 4))",
+                         "(uint8_t)(code[64 * g + 32 + l] | (code[64 * g + l] << 4))"),
+    "q4k_min_added": ("w[32 * j + l] = D * (float)q - M;", "w[32 * j + l] = D * (float)q + M;"),
+    "q4k_scale_high_bits": ("*sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);",
+                            "*sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 3);"),
+    "q4k_min_high_bits": ("*m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);",
+                          "*m = (s[j + 4] >> 4) | ((s[j - 4] >> 6) << 4);"),
+    "q4k_step_divisor": ("step[j] = (hi - lo) / 15.0f;", "step[j] = (hi - lo) / 16.0f;"),
+    "q4k_no_zero_in_range": ("if (lo > 0.0f) lo = 0.0f;", ""),
+    "q4k_scale_divisor": ("const float d = smax / 63.0f;", "const float d = smax / 64.0f;"),
+    "q4k_codes_from_unrounded_scale": ("const float D = df * (float)sc[j];",
+                                       "const float D = step[j];"),
 }
+PIN_FILES = ("test_oracle_pins.py", "test_oracle_q4k_pins.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -66,6 +80,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, GQ_ORACLE_SO=str(so_path))
     r = subprocess.run(
         [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+         *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
