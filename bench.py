@@ -63,8 +63,8 @@ def aggregate(seconds: float, units: float, world: int, device=None):
     return float(t.item()), float(u.item())
 
 
-def step_bytes(shapes, N: int, block_bytes: int) -> dict:
-    w = sum(s.M * (s.K // 32) * block_bytes for s in shapes)
+def step_bytes(shapes, N: int, block_bytes: int, block_weights: int = 32) -> dict:
+    w = sum(s.M * (s.K // block_weights) * block_bytes for s in shapes)
     x = sum(N * s.K * 4 for s in shapes)
     y = sum(N * s.M * 4 for s in shapes)
     return {"weights": w, "x": x, "y": y, "total": w + x + y}
@@ -333,6 +333,8 @@ DECODE_SETS = [
     ("tinyllama_decode_q4_0", 2, "q4_0", "tinyllama", (2, 4, 8, 16)),
     ("tinyllama_decode_q8_0", 3, "q8_0", "tinyllama", (1, 2, 4, 8, 16)),
     ("llama7b_decode_q4_0", 5, "q4_0", "llama7b", (1, 16)),
+    # the same TinyLLaMA weights (workload 2's seeds) in Q4_K super-blocks
+    ("tinyllama_decode_q4_k", 2, "q4_k", "tinyllama", (1, 2, 4)),
 ]
 L2_BYTES = 129 * 2 ** 20
 STEPS_PER_GRAPH = 10
@@ -351,13 +353,14 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
         shapes = {"single": [workloads.MatShape("proj", 2048, 2048)],
                   "tinyllama": workloads.tinyllama_decode_set(),
                   "llama7b": workloads.llama7b_set()}[which]
-        nb1 = step_bytes(shapes, 1, binding.block_bytes(btype))
+        bw = 256 if btype == "q4_k" else 32
+        nb1 = step_bytes(shapes, 1, binding.block_bytes(btype), bw)
         copies = min(64, max(1, -(-4 * L2_BYTES // nb1["weights"])))
         sets = [QuantizedWeightSet.synthetic(wl if c == 0 else 100 * wl + c, shapes, btype, dev)
                 for c in range(copies)]
         rows = []
         for N in Ns:
-            nb = step_bytes(shapes, N, binding.block_bytes(btype))
+            nb = step_bytes(shapes, N, binding.block_bytes(btype), bw)
             runs = []
             for c, ws in enumerate(sets):
                 xs, ys = ws.make_io(N, wl, dev)
@@ -384,7 +387,8 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
             gbs = nb["total"] / sec / 1e9
             rows.append({"N": N, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
                          "frac": round(gbs / peak, 4),
-                         "path": "CUDA-core decode" if N <= 2 else "tensor-core decode"})
+                         "path": "CUDA-core decode" if N <= 2 or btype == "q4_k"
+                         else "tensor-core decode"})
             del runs, g
         if binding.get_last_error() != 0:
             raise RuntimeError("device status word set during the decode sets")
@@ -497,7 +501,7 @@ def dense_context_measure(dev, reps: int = 20, iters: int = 5) -> dict:
 # --------------------------------------------------------------------------------------
 ORACLE_ENTRIES = [(1, "q4_0", 1), (2, "q4_0", 1), (3, "q8_0", 1), (3, "q8_0", 2),
                   (3, "q8_0", 4), (3, "q8_0", 8), (3, "q8_0", 16), (4, "q4_0", 512),
-                  (5, "q4_0", 1), (5, "q4_0", 16), (5, "q4_0", 2048)]
+                  (5, "q4_0", 1), (5, "q4_0", 16), (5, "q4_0", 2048), (2, "q4_k", 1)]
 
 
 def host_cores() -> int:
@@ -567,7 +571,8 @@ def oracle_per_config(dev, target_s: float = 0.4) -> dict:
             e["tflops"] = {"one_core": round(2 * full_mac / s1 / 1e12, 6),
                            "all_cores": round(2 * full_mac / sa / 1e12, 6)}
         else:
-            b = step_bytes(shapes, N, binding.block_bytes(btype))["total"]
+            b = step_bytes(shapes, N, binding.block_bytes(btype),
+                           256 if btype == "q4_k" else 32)["total"]
             e["GBps"] = {"one_core": round(b / s1 / 1e9, 4), "all_cores": round(b / sa / 1e9, 4)}
         out["entries"].append(e)
         del sample, one
@@ -950,6 +955,7 @@ def summarize(dec: dict, pf: dict, dense: dict, peak: float) -> dict:
         "w2_tinyllama_q4_0": per_n("tinyllama_decode_q4_0"),
         "w3_tinyllama_q8_0": per_n("tinyllama_decode_q8_0"),
         "w5_llama7b_q4_0": per_n("llama7b_decode_q4_0"),
+        "w2_tinyllama_q4_k": per_n("tinyllama_decode_q4_k"),
     }
     for key, v in pf.items():
         out["prefill_" + key] = [v["tflops"], v["frac"]]

@@ -24,7 +24,8 @@ lib = None
 
 Q4_0 = 2
 Q8_0 = 8
-TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, Q4_0: Q4_0, Q8_0: Q8_0}
+Q4_K = 12
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "q4_k": Q4_K, Q4_0: Q4_0, Q8_0: Q8_0, Q4_K: Q4_K}
 MAX_BATCH = 256
 
 STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
@@ -32,7 +33,7 @@ STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
 
 # Every symbol declared in include/gq.h.
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
-           "gq_quantize_q8_0", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
+           "gq_quantize_q8_0", "gq_quantize_q4_k", "gq_dequantize", "gq_mul_mat", "gq_mul_mat_workspace_size",
            "gq_mul_mat_ws", "gq_mul_mat_noalloc", "gq_mul_mat_batched",
            "gq_mul_mat_batched_workspace_size", "gq_mul_mat_batched_ws", "gq_mul_mat_q8x",
            "gq_mul_mat_q8x_batched", "gq_mul_mat_rmsnorm", "gq_mul_mat_swiglu",
@@ -55,7 +56,7 @@ def load(path: str = LIB_PATH):
     L.gq_abi_version.argtypes, L.gq_abi_version.restype = [], i32
     L.gq_block_bytes.argtypes, L.gq_block_bytes.restype = [ctypes.c_int], ctypes.c_size_t
     L.gq_row_bytes.argtypes, L.gq_row_bytes.restype = [ctypes.c_int, i64], ctypes.c_size_t
-    for q in (L.gq_quantize_q4_0, L.gq_quantize_q8_0):
+    for q in (L.gq_quantize_q4_0, L.gq_quantize_q8_0, L.gq_quantize_q4_k):
         q.argtypes, q.restype = [vp, i64, i64, vp, vp], ctypes.c_int
     L.gq_dequantize.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp]
     L.gq_dequantize.restype = ctypes.c_int
@@ -140,9 +141,9 @@ def quantize(W: torch.Tensor, t, out: torch.Tensor | None = None, stream=None) -
     """fp32 (M, K) CUDA tensor -> uint8 (M, row_bytes) blocks."""
     M, K = W.shape
     if out is None:
-        out = torch.empty((M, row_bytes(t, K) if K % 32 == 0 else 0), dtype=torch.uint8,
-                          device=W.device)
-    fn = lib.gq_quantize_q4_0 if _type(t) == Q4_0 else lib.gq_quantize_q8_0
+        out = torch.empty((M, row_bytes(t, K)), dtype=torch.uint8, device=W.device)
+    fn = {Q4_0: lib.gq_quantize_q4_0, Q8_0: lib.gq_quantize_q8_0,
+          Q4_K: lib.gq_quantize_q4_k}[_type(t)]
     _check(fn(_dev(W, torch.float32, "W"), M, K, _dev(out, torch.uint8, "W_blocks"),
               _stream(stream)), "gq_quantize")
     return out

@@ -51,13 +51,14 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;
 
 bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
-bool known_type(gq_type t) { return t == GQ_TYPE_Q4_0 || t == GQ_TYPE_Q8_0; }
+bool known_type(gq_type t) { return gq::block_bytes_of(t) != 0; }
 
 gq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GQ_OK : GQ_ERR_CUDA; }
 
-// Shapes: non-negative, K a multiple of 32, every dimension and product in range.
-gq_status check_shape(int64_t M, int64_t K, int64_t N) {
-    if (M < 0 || K < 0 || N < 0 || K % 32 != 0) return GQ_ERR_SHAPE;
+// Shapes: non-negative, K a multiple of the type's block (32 weights; 256 for Q4_K), every
+// dimension and product in range. The type must be known.
+gq_status check_shape(gq_type t, int64_t M, int64_t K, int64_t N) {
+    if (M < 0 || K < 0 || N < 0 || K % gq::block_weights_of(t) != 0) return GQ_ERR_SHAPE;
     if (M > kMaxDim || K > kMaxDim || N > kMaxDim) return GQ_ERR_SHAPE;
     if (M * K > kMaxElems || N * K > kMaxElems || N * M > kMaxElems) return GQ_ERR_SHAPE;
     return GQ_OK;
@@ -65,12 +66,13 @@ gq_status check_shape(int64_t M, int64_t K, int64_t N) {
 
 gq_status quantize_impl(gq_type t, const float* W, int64_t M, int64_t K, void* out,
                         void* stream) {
-    gq_status st = check_shape(M, K, 0);
+    gq_status st = check_shape(t, M, K, 0);
     if (st != GQ_OK) return st;
     if (M == 0 || K == 0) return GQ_OK;
     if (!W || !out) return GQ_ERR_NULL;
     if (!aligned(W, 4) || !aligned(out, 16)) return GQ_ERR_ALIGN;
-    return from_cuda(gq::launch_quantize(t, W, M * (K / 32), static_cast<uint8_t*>(out),
+    return from_cuda(gq::launch_quantize(t, W, M * (K / gq::block_weights_of(t)),
+                                         static_cast<uint8_t*>(out),
                                          static_cast<cudaStream_t>(stream)));
 }
 
@@ -78,7 +80,7 @@ gq_status quantize_impl(gq_type t, const float* W, int64_t M, int64_t K, void* o
 gq_status check_problem(const void* W, gq_type t, int64_t M, int64_t K, const float* X,
                         int64_t N, const float* Y, bool* empty) {
     if (!known_type(t)) return GQ_ERR_TYPE;
-    gq_status st = check_shape(M, K, N);
+    gq_status st = check_shape(t, M, K, N);
     if (st != GQ_OK) return st;
     *empty = (M == 0 || N == 0);
     if (*empty) return GQ_OK;
@@ -124,7 +126,7 @@ cudaError_t internal_workspace(cudaStream_t s, size_t bytes, void** out) {
 // else the decode kernels. `ws` may be NULL (library workspace is used then).
 gq_status run_one(gq_type t, const gq::MatProblem& p, int64_t N, void* ws, size_t ws_bytes,
                   cudaStream_t s) {
-    if (gq::gemv_tc_eligible(p, N)) {
+    if (gq::gemv_tc_eligible(t, p, N)) {
         const size_t need = static_cast<size_t>(gq::gemv_tc_workspace_bytes(&p, 1, N));
         void* w = ws;
         if (w == nullptr) {
@@ -158,8 +160,8 @@ size_t gq_block_bytes(gq_type t) { return static_cast<size_t>(gq::block_bytes_of
 
 size_t gq_row_bytes(gq_type t, int64_t K) {
     const int bb = gq::block_bytes_of(t);
-    if (bb == 0 || K < 0 || K % 32 != 0) return 0;
-    return static_cast<size_t>(K / 32) * static_cast<size_t>(bb);
+    if (bb == 0 || K < 0 || K % gq::block_weights_of(t) != 0) return 0;
+    return static_cast<size_t>(K / gq::block_weights_of(t)) * static_cast<size_t>(bb);
 }
 
 gq_status gq_quantize_q4_0(const float* W, int64_t M, int64_t K, void* W_blocks,
@@ -172,10 +174,15 @@ gq_status gq_quantize_q8_0(const float* W, int64_t M, int64_t K, void* W_blocks,
     return quantize_impl(GQ_TYPE_Q8_0, W, M, K, W_blocks, stream);
 }
 
+gq_status gq_quantize_q4_k(const float* W, int64_t M, int64_t K, void* W_blocks,
+                           void* stream) {
+    return quantize_impl(GQ_TYPE_Q4_K, W, M, K, W_blocks, stream);
+}
+
 gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K, float* W_out,
                         void* stream) {
     if (!known_type(t)) return GQ_ERR_TYPE;
-    gq_status st = check_shape(M, K, 0);
+    gq_status st = check_shape(t, M, K, 0);
     if (st != GQ_OK) return st;
     if (M == 0 || K == 0) return GQ_OK;
     if (!W_blocks || !W_out) return GQ_ERR_NULL;
@@ -196,10 +203,11 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K, cons
 }
 
 size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N) {
-    if (!known_type(t) || check_shape(M, K, N) != GQ_OK || M == 0 || N == 0 || K == 0) return 0;
+    if (!known_type(t) || check_shape(t, M, K, N) != GQ_OK || M == 0 || N == 0 || K == 0)
+        return 0;
     gq::MatProblem p{reinterpret_cast<const uint8_t*>(uintptr_t(256)),
                      reinterpret_cast<const float*>(uintptr_t(256)), nullptr, M, K};
-    if (gq::gemv_tc_eligible(p, N))
+    if (gq::gemv_tc_eligible(t, p, N))
         return static_cast<size_t>(gq::gemv_tc_workspace_bytes(&p, 1, N));
     return gq::gemm_eligible(t, p, N) ? static_cast<size_t>(gq::gemm_workspace_bytes(K, N)) : 0;
 }
@@ -213,7 +221,7 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return from_cuda(cudaMemsetAsync(Y, 0, sizeof(float) * N * M, s));
     gq::MatProblem p{static_cast<const uint8_t*>(W_blocks), X, Y, M, K};
-    if ((gq::gemm_eligible(t, p, N) || gq::gemv_tc_eligible(p, N)) && workspace == nullptr)
+    if ((gq::gemm_eligible(t, p, N) || gq::gemv_tc_eligible(t, p, N)) && workspace == nullptr)
         return GQ_ERR_NULL;
     return run_one(t, p, N, workspace, workspace_bytes, s);
 }
@@ -255,7 +263,7 @@ gq_status plan_batch(const gq_mul_mat_problem* problems, int32_t count, gq_type 
         if (gq::gemm_eligible(t, mp, N)) {
             plan->gemm[plan->n_gemm++] = mp;
             gemm_max = std::max(gemm_max, static_cast<size_t>(gq::gemm_workspace_bytes(p.K, N)));
-        } else if (gq::gemv_tc_eligible(mp, N)) {
+        } else if (gq::gemv_tc_eligible(t, mp, N)) {
             plan->tc[plan->n_tc++] = mp;
         } else {
             plan->cc[plan->n_cc++] = mp;
@@ -306,6 +314,7 @@ gq_status check_q8x(const void* W, gq_type t, int64_t M, int64_t K, const float*
                     float* Y, cudaStream_t s, bool zero_k0, bool* run) {
     bool empty = false;
     *run = false;
+    if (t == GQ_TYPE_Q4_K) return GQ_ERR_TYPE;   // Q8_0 activation blocks pair with 32-weight blocks
     gq_status st = check_problem(W, t, M, K, X, N, Y, &empty);
     if (st != GQ_OK || empty) return st;
     if (K == 0) {
@@ -395,7 +404,7 @@ gq_status gq_mul_mat_q8x(const void* W_blocks, gq_type t, int64_t M, int64_t K, 
 gq_status gq_mul_mat_q8x_batched(const gq_mul_mat_problem* problems, int32_t count, gq_type t,
                                  int64_t N, void* stream) {
     if (count < 0 || count > GQ_MAX_BATCH) return GQ_ERR_SHAPE;
-    if (!known_type(t)) return GQ_ERR_TYPE;
+    if (!known_type(t) || t == GQ_TYPE_Q4_K) return GQ_ERR_TYPE;
     if (count == 0) return GQ_OK;
     if (!problems) return GQ_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -465,8 +474,9 @@ const char* gq_status_string(gq_status s) {
     switch (s) {
         case GQ_OK: return "ok";
         case GQ_ERR_NULL: return "a required pointer is NULL";
-        case GQ_ERR_SHAPE: return "invalid shape (negative, K not a multiple of 32, too large)";
-        case GQ_ERR_TYPE: return "unknown block type";
+        case GQ_ERR_SHAPE:
+            return "invalid shape (negative, K not a multiple of the block, too large)";
+        case GQ_ERR_TYPE: return "unknown block type, or one this entry point does not take";
         case GQ_ERR_ALIGN: return "misaligned pointer (blocks need 16 bytes, fp32 arrays 4)";
         case GQ_ERR_CUDA: return "CUDA runtime error";
         case GQ_ERR_TIMEOUT: return "a device-side wait ran out of time";

@@ -817,7 +817,7 @@ int64_t gemm_x_bytes(int64_t K, int64_t N) { return (N * K * 2 + 255) / 256 * 25
 int64_t gemm_workspace_bytes(int64_t K, int64_t N) { return gemm_x_bytes(K, N); }
 
 bool gemm_eligible(gq_type t, const MatProblem& p, int64_t N) {
-    (void)t;
+    if (t != GQ_TYPE_Q4_0 && t != GQ_TYPE_Q8_0) return false;   // 32-weight block types
     if (N < kGemmMinTokens || p.K % kSuperK != 0 || p.M <= 0) return false;
     if (p.M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 24) || p.K > (int64_t(1) << 24))
         return false;

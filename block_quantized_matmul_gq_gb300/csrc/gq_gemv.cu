@@ -35,10 +35,17 @@
 //    per instruction):
 //        S = sum_i (16 (c_i - 8)) * x16_i       (Q4_0; codes become signed bytes 16(c-8))
 //        S = sum_i c_i * x16_i                  (Q8_0)
-//    then acc += d * float(S) and, per chunk, partial = acc * 2^e. The only approximation
-//    is x16 = rint(x / 2^e) with |x16| <= 32767, i.e. |error| <= sqrt(256) / 65534 *
-//    ||x|| ||What|| = 0.24 of the bound 1e-3 ||x|| ||What|| (Cauchy-Schwarz per chunk),
-//    whatever the inputs.
+//    then acc += d * float(S) and, per chunk, partial = acc * 2^(e - 15). The only
+//    approximation is x16 = rint(x * 2^(15 - e)), 2^(e - 1) <= max |x| < 2^e, clamped to
+//    +-32767: per element the rounding errs by at most 2^(e - 16) <= max |x| 2^-15 (the
+//    clamp, where it acts, by at most |x| / 32767.5), so per chunk ||x - xhat||_2 <=
+//    ||x_chunk|| (1 / 2048 + 1 / 32767.5), and by Cauchy-Schwarz |error| <= 0.52 of the
+//    bound 1e-3 ||x|| ||What||, whatever the inputs.
+//  * Q4_K super-blocks (the published GGUF Q4_K layout) stream in the geometry of Q4_0:
+//    a chunk is one 144-byte super-block, and lane l takes quarter l % 4 (sub-blocks 2g,
+//    2g + 1) of super-block l / 4 in all four rows of the tile; per row the sub-block sums
+//    S_j = sum q x16 and X_j = sum x16 are exact integers, combined as
+//    d (sc S + sc' S') - dmin (m X + m' X') in fp32 (quarter_dot_q4k).
 //  * A lane keeps its running sums in registers across all columns; at the tile's end
 //    the lanes' sums of each row are added with shuffles in a fixed order (Q4_0: a
 //    transposed reduction of the four rows; otherwise the eight lanes of a row). When a
@@ -96,13 +103,22 @@ struct Fmt;
 template <>
 struct Fmt<GQ_TYPE_Q4_0> {
     static constexpr int kBB = kQ4Bytes;
+    static constexpr int kWeights = 32;
     static constexpr int kBlocksPerChunk = 8;
     static constexpr int kCodeShift = 4;   // dp2a sums come out as 16 * sum (c - 8) x16
 };
 template <>
 struct Fmt<GQ_TYPE_Q8_0> {
     static constexpr int kBB = kQ8Bytes;
+    static constexpr int kWeights = 32;
     static constexpr int kBlocksPerChunk = 4;
+    static constexpr int kCodeShift = 0;
+};
+template <>
+struct Fmt<GQ_TYPE_Q4_K> {   // a chunk is one super-block
+    static constexpr int kBB = kQ4KBytes;
+    static constexpr int kWeights = kQ4KWeights;
+    static constexpr int kBlocksPerChunk = 1;
     static constexpr int kCodeShift = 0;
 };
 
@@ -112,7 +128,7 @@ struct Geo {
     static constexpr int kBPC = Fmt<kType>::kBlocksPerChunk;
     static constexpr int kChunkBytes = kBB * kBPC;                 // 144 or 136
     static constexpr int kChunkWords = kChunkBytes / 4;            // 36 or 34
-    static constexpr int kWPC = 32 * kBPC;                         // weights per chunk
+    static constexpr int kWPC = Fmt<kType>::kWeights * kBPC;       // weights per chunk: 256 / 128
     static constexpr int kRowStride = kLanesPerRow * kChunkBytes;  // 1152 or 1088 in a stage
     // One stage of one warp: 4 rows x 8 chunks, padded to 128-byte multiples.
     static constexpr int kStageBytes = (kTileRows * kRowStride + 127) / 128 * 128;
@@ -122,19 +138,26 @@ struct Geo {
     //   folded in), then two float factors whose product is the chunk's power-of-two
     //   scale. A lane reads one pair record (pair_dot_q4); records 9 units of 16 bytes
     //   apart put the 8 lanes of a quarter warp in 8 different groups of 4 banks.
+    //  Q4_K: the same four records, one per quarter of the super-block (sub-blocks 2g and
+    //   2g + 1); the two ints are the plain sums of the sub-blocks' x16 (for the mins).
     //  Q8_0: kWPC int16, then the two scale factors; record stride 68 words (4 mod 32),
     //   so the 8 columns a warp reads sit in 8 different groups of 4 banks.
     static constexpr int kScaleOff = kWPC * 2;                     // Q8_0
-    static constexpr int kXRec = kType == GQ_TYPE_Q4_0 ? 4 * 144 : kScaleOff + 16;  // 576 / 272
+    static constexpr int kXRec = kType == GQ_TYPE_Q8_0 ? kScaleOff + 16 : 4 * 144;  // 272 / 576
 };
 
-// Q4_0 pair record (see Geo): 64 int16 x16, two int biases, two float scale factors.
+// Q4_0 pair record and Q4_K quarter record (see Geo): 64 int16 x16, two ints (Q4_0: biases;
+// Q4_K: sub-block sums), two float scale factors.
 struct Q4Pair {
     static constexpr int kRec = 144;
     static constexpr int kBiasOff = 128;
     static constexpr int kScaleOff = 136;
 };
 static_assert(Geo<GQ_TYPE_Q4_0>::kXRec == 4 * Q4Pair::kRec, "four pair records per chunk");
+static_assert(Geo<GQ_TYPE_Q4_K>::kXRec == 4 * Q4Pair::kRec, "four quarter records per chunk");
+static_assert(Geo<GQ_TYPE_Q4_K>::kChunkBytes == Geo<GQ_TYPE_Q4_0>::kChunkBytes &&
+                  Geo<GQ_TYPE_Q4_K>::kChunkWords == Geo<GQ_TYPE_Q4_0>::kChunkWords,
+              "Q4_K streams in the stage geometry of Q4_0");
 
 struct GemvProb {
     const uint8_t* W;
@@ -355,7 +378,7 @@ template <int kType, int kNT, bool kNorm>
 __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbuf,
                           float* scratch) {
     using G = Geo<kType>;
-    constexpr int kPerLane = G::kWPC / 32;   // 8 (Q4_0) or 4 (Q8_0) elements
+    constexpr int kPerLane = G::kWPC / 32;   // 8 (Q4_0, Q4_K) or 4 (Q8_0) elements
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int C = pr.C;
@@ -424,15 +447,17 @@ __device__ void prepare_x(const GemvProb& pr, int n_tok, int max_c, uint8_t* xbu
         const float sc1 = __int_as_float((u - u_a + 127) << 23);
         if constexpr (kPerLane == 8) {
             // Q4_0: lane l holds elements 8l..8l+7, i.e. block l / 4 of pair l / 8.
+            // Q4_K: the same elements are part of sub-block l / 4 of quarter l / 8.
             uint8_t* prec = rec + (lane >> 3) * Q4Pair::kRec;
             *reinterpret_cast<uint4*>(prec + (lane & 7) * 16) =
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            // block j covers lanes 4j..4j+3 (32 elements): bias = -128 * their sum
+            // block j covers lanes 4j..4j+3 (32 elements): Q4_0 bias = -128 * their sum,
+            // Q4_K sub-block sum = their sum
             lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 1);
             lane_sum += __shfl_xor_sync(0xFFFFFFFFu, lane_sum, 2);
             if ((lane & 3) == 0)
                 *reinterpret_cast<int*>(prec + Q4Pair::kBiasOff + 4 * ((lane >> 2) & 1)) =
-                    -128 * lane_sum;
+                    kType == GQ_TYPE_Q4_0 ? -128 * lane_sum : lane_sum;
             if ((lane & 7) == 0)
                 *reinterpret_cast<float2*>(prec + Q4Pair::kScaleOff) = make_float2(sc0, sc1);
         } else {
@@ -482,7 +507,10 @@ struct Q8xRec {
 // Bytes of one chunk's activation record: x16 fixed point (kXM = 0) or Q8_0 codes (1).
 template <int kType, int kXM>
 __host__ __device__ constexpr int xrec_bytes() {
-    return kXM ? Q8xRec<kType>::kXRec : Geo<kType>::kXRec;
+    if constexpr (kXM != 0)
+        return Q8xRec<kType>::kXRec;
+    else
+        return Geo<kType>::kXRec;
 }
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
@@ -786,6 +814,143 @@ __device__ __forceinline__ void pair_dot_q4(const uint8_t* raw, int rs, int rows
     }
 }
 
+// Q4_K. The 6-bit scales sc and mins m of sub-blocks 2g and 2g + 1 of a super-block
+// whose 16 header bytes are hd (fp16 d | fp16 dmin << 16, then scale bytes s[0..11]), as
+// two 8-bit lanes of a word: bits 0..7 for sub-block 2g, 8..15 for 2g + 1. The published
+// packing: j < 4: sc_j = s[j] & 63, m_j = s[j + 4] & 63; j >= 4: sc_j = (s[j + 4] & 15) |
+// (s[j - 4] >> 6) << 4, m_j = (s[j + 4] >> 4) | (s[j] >> 6) << 4. Sub-blocks 2g, 2g + 1
+// take bytes 2 (g & 1) and 2 (g & 1) + 1 of each group of four scale bytes.
+__device__ __forceinline__ void q4k_scales(const uint4& hd, int g, uint32_t& sc, uint32_t& m) {
+    const int sh = 16 * (g & 1);
+    const uint32_t a = (hd.y >> sh) & 0xFFFFu;   // s[j'] pair
+    const uint32_t b = (hd.z >> sh) & 0xFFFFu;   // s[4 + j'] pair
+    const uint32_t c = (hd.w >> sh) & 0xFFFFu;   // s[8 + j'] pair
+    if (g < 2) {
+        sc = a & 0x3F3Fu;
+        m = b & 0x3F3Fu;
+    } else {
+        sc = (c & 0x0F0Fu) | ((a >> 2) & 0x3030u);
+        m = ((c >> 4) & 0x0F0Fu) | ((b >> 2) & 0x3030u);
+    }
+}
+
+// sum over one 32-element sub-block of q x16: x holds the sub-block's 32 int16 (word w =
+// elements 2w, 2w + 1), q[i] the codes of elements 4i .. 4i + 3 as bytes. Exact (|sum| <=
+// 15 * 32767 * 32 < 2^24); four independent dp2a chains.
+__device__ __forceinline__ int q4k_sub_dot(const uint4 (&x)[4], const uint32_t (&q)[8]) {
+    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+    s0 = dp2a_lo_su(static_cast<int>(x[0].x), q[0], s0);
+    s1 = dp2a_lo_su(static_cast<int>(x[0].z), q[1], s1);
+    s2 = dp2a_lo_su(static_cast<int>(x[1].x), q[2], s2);
+    s3 = dp2a_lo_su(static_cast<int>(x[1].z), q[3], s3);
+    s0 = dp2a_hi_su(static_cast<int>(x[0].y), q[0], s0);
+    s1 = dp2a_hi_su(static_cast<int>(x[0].w), q[1], s1);
+    s2 = dp2a_hi_su(static_cast<int>(x[1].y), q[2], s2);
+    s3 = dp2a_hi_su(static_cast<int>(x[1].w), q[3], s3);
+    s0 = dp2a_lo_su(static_cast<int>(x[2].x), q[4], s0);
+    s1 = dp2a_lo_su(static_cast<int>(x[2].z), q[5], s1);
+    s2 = dp2a_lo_su(static_cast<int>(x[3].x), q[6], s2);
+    s3 = dp2a_lo_su(static_cast<int>(x[3].z), q[7], s3);
+    s0 = dp2a_hi_su(static_cast<int>(x[2].y), q[4], s0);
+    s1 = dp2a_hi_su(static_cast<int>(x[2].w), q[5], s1);
+    s2 = dp2a_hi_su(static_cast<int>(x[3].y), q[6], s2);
+    s3 = dp2a_hi_su(static_cast<int>(x[3].w), q[7], s3);
+    return (s0 + s1) + (s2 + s3);
+}
+
+// Q4_K: quarter g (sub-blocks 2g and 2g + 1, 64 weights) of one super-block in each of the
+// tile's `rows` rows (sb = the super-block in row 0, rows rs bytes apart) against every
+// token's quarter record: out[r][t] += the quarter's partial (scaled by 2^e), with
+//     partial = d (sc_2g S_2g + sc_2g+1 S_2g+1) - dmin (m_2g X_2g + m_2g+1 X_2g+1),
+// S_j = sum q x16 and X_j = sum x16 over sub-block j (both sums exact in int32: at most
+// 63 * 2 * 15 * 32767 * 32 < 2^31 and 63 * 2 * 32767 * 32). At one token the record is
+// read once for all rows; at more tokens one sub-block at a time, and each row's codes
+// are read once per sub-block.
+template <int kNT>
+__device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs, int rows,
+                                                const uint8_t* xp, int rec_stride,
+                                                float (&out)[kTileRows][kNT]) {
+    float acc[kTileRows][kNT];
+#pragma unroll
+    for (int r = 0; r < kTileRows; ++r)
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) acc[r][t] = 0.0f;
+    if constexpr (kNT == 1) {
+        PairX X;
+        load_pair_x(xp, X);
+#pragma unroll
+        for (int r = 0; r < kTileRows; ++r) {
+            if (r >= rows) break;   // uniform across the warp
+            const uint8_t* row = sb + r * rs;
+            const uint4 hd = *reinterpret_cast<const uint4*>(row);
+            const uint4 c0 = *reinterpret_cast<const uint4*>(row + 16 + 32 * g);
+            const uint4 c1 = *reinterpret_cast<const uint4*>(row + 32 + 32 * g);
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t lo[8], hi[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                lo[i] = cw[i] & 0x0F0F0F0Fu;
+                hi[i] = (cw[i] >> 4) & 0x0F0F0F0Fu;
+            }
+            uint32_t sc, m;
+            q4k_scales(hd, g, sc, m);
+            const int S0 = q4k_sub_dot(X.x[0], lo);
+            const int S1 = q4k_sub_dot(X.x[1], hi);
+            const int T = static_cast<int>(sc & 0xFFu) * S0 + static_cast<int>(sc >> 8) * S1;
+            const int U = static_cast<int>(m & 0xFFu) * X.bias[0] +
+                          static_cast<int>(m >> 8) * X.bias[1];
+            const float d = half_bits_to_float(hd.x & 0xFFFFu);
+            const float dmin = half_bits_to_float(hd.x >> 16);
+            acc[r][0] = fmaf(-dmin, static_cast<float>(U), fmaf(d, static_cast<float>(T), acc[r][0]));
+        }
+#pragma unroll
+        for (int r = 0; r < kTileRows; ++r) out[r][0] = fmaf(acc[r][0] * X.sc.x, X.sc.y, out[r][0]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint4 xv[kNT][4];
+            int xs[kNT];
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+                const uint8_t* x = xp + t * rec_stride + 64 * h;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xv[t][i] = *reinterpret_cast<const uint4*>(x + 16 * i);
+                xs[t] = *reinterpret_cast<const int*>(xp + t * rec_stride + Q4Pair::kBiasOff + 4 * h);
+            }
+#pragma unroll
+            for (int r = 0; r < kTileRows; ++r) {
+                if (r >= rows) break;   // uniform across the warp
+                const uint8_t* row = sb + r * rs;
+                const uint4 hd = *reinterpret_cast<const uint4*>(row);
+                const uint4 c0 = *reinterpret_cast<const uint4*>(row + 16 + 32 * g);
+                const uint4 c1 = *reinterpret_cast<const uint4*>(row + 32 + 32 * g);
+                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint32_t q[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) q[i] = (cw[i] >> (4 * h)) & 0x0F0F0F0Fu;
+                uint32_t sc, m;
+                q4k_scales(hd, g, sc, m);
+                const int scj = static_cast<int>((sc >> (8 * h)) & 0xFFu);
+                const int mj = static_cast<int>((m >> (8 * h)) & 0xFFu);
+                const float d = half_bits_to_float(hd.x & 0xFFFFu);
+                const float dmin = half_bits_to_float(hd.x >> 16);
+#pragma unroll
+                for (int t = 0; t < kNT; ++t) {
+                    const int S = q4k_sub_dot(xv[t], q);
+                    acc[r][t] = fmaf(-dmin, static_cast<float>(mj * xs[t]),
+                                     fmaf(d, static_cast<float>(scj * S), acc[r][t]));
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) {
+            const float2 sc = *reinterpret_cast<const float2*>(xp + t * rec_stride + Q4Pair::kScaleOff);
+#pragma unroll
+            for (int r = 0; r < kTileRows; ++r) out[r][t] = fmaf(acc[r][t] * sc.x, sc.y, out[r][t]);
+        }
+    }
+}
+
 // Sums each row of a 4-row tile over the 32 lanes (lane l holds v[r] for row r) in a fixed
 // order, and leaves row r's total in lanes 8r .. 8r + 7 -- the lanes that own row r in the
 // row-per-8-lanes layout -- with six shuffles: two exchanges halve the rows a lane carries
@@ -811,7 +976,9 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
     // kFuse: 0 plain, 1 RMSNorm of X in the preparation, 2 gate/up row pairs (Swish * up)
     constexpr bool kPair = kFuse == 2;
     constexpr bool kNorm = kFuse == 1;
-    constexpr bool kPairMap = kType == GQ_TYPE_Q4_0 && kXM == 0;
+    // Q4_0 and Q4_K with x16: a lane takes 64 weights (a block pair, a super-block quarter)
+    // in every row of the tile.
+    constexpr bool kPairMap = kType != GQ_TYPE_Q8_0 && kXM == 0;
     using G = Geo<kType>;
     constexpr int kRec = xrec_bytes<kType, kXM>();
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -907,7 +1074,8 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
 #pragma unroll
             for (int t = 0; t < kNT; ++t) acc[t] = 0.0f;
             // Q4_0 with x16: lane l takes block pair l of the column group in every row of
-            // the tile (acc4[r][t]); otherwise lane l takes chunk lc of row rrow (acc[t]).
+            // the tile (acc4[r][t]); Q4_K: quarter l % 4 of super-block l / 4 in every row;
+            // otherwise lane l takes chunk lc of row rrow (acc[t]).
             float acc4[kTileRows][kNT];
 #pragma unroll
             for (int r = 0; r < kTileRows; ++r)
@@ -927,9 +1095,15 @@ gemv_stream_kernel(const __grid_constant__ GemvParams<kMaxProbs> P) {
                 if constexpr (kPairMap) {
                     const int col = kLanesPerRow * cs + (lane >> 2);
                     if (col < pr.C) {
-                        pair_dot_q4<kNT>(stage + lane * (G::kChunkBytes / 4), rs, rows,
-                                         xbuf + col * kRec + (lane & 3) * Q4Pair::kRec,
-                                         rec_stride, acc4);
+                        if constexpr (kType == GQ_TYPE_Q4_0)
+                            pair_dot_q4<kNT>(stage + lane * (G::kChunkBytes / 4), rs, rows,
+                                             xbuf + col * kRec + (lane & 3) * Q4Pair::kRec,
+                                             rec_stride, acc4);
+                        else
+                            quarter_dot_q4k<kNT>(stage + (lane >> 2) * G::kChunkBytes, lane & 3,
+                                                 rs, rows,
+                                                 xbuf + col * kRec + (lane & 3) * Q4Pair::kRec,
+                                                 rec_stride, acc4);
                     }
                     dep = __float_as_uint(acc4[0][0]) ^ __float_as_uint(acc4[1][0]) ^
                           __float_as_uint(acc4[2][0]) ^ __float_as_uint(acc4[3][0]);
@@ -1085,6 +1259,57 @@ gemv_generic_kernel(const uint8_t* __restrict__ W, int64_t M, int64_t K,
     }
 }
 
+// Q4_K, any K % 256 == 0: one warp per row, lanes over 32-weight sub-blocks, each weight
+// D_j q - M_j in fp32 (as gq_dequantize computes it), fp32 FMA, xor-shuffle reduction.
+__global__ void __launch_bounds__(256)
+gemv_generic_q4k_kernel(const uint8_t* __restrict__ W, int64_t M, int64_t K,
+                        const float* __restrict__ X, int n_tok, float* __restrict__ Y) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nsub = K / 32;
+    const int64_t row_bytes = (K / kQ4KWeights) * kQ4KBytes;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+         row < M; row += warps) {
+        float acc[kMaxTok] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int64_t b = lane; b < nsub; b += 32) {
+            const uint8_t* sb = W + row * row_bytes + (b >> 3) * kQ4KBytes;
+            const int j = static_cast<int>(b & 7);
+            const uint4 hd = __ldg(reinterpret_cast<const uint4*>(sb));
+            uint32_t sc2, m2;
+            q4k_scales(hd, j >> 1, sc2, m2);
+            const int h = j & 1;
+            const float D = __fmul_rn(half_bits_to_float(hd.x & 0xFFFFu),
+                                      static_cast<float>((sc2 >> (8 * h)) & 0xFFu));
+            const float Mj = __fmul_rn(half_bits_to_float(hd.x >> 16),
+                                       static_cast<float>((m2 >> (8 * h)) & 0xFFu));
+            const uint4* cp = reinterpret_cast<const uint4*>(sb + 16 + 32 * (j >> 1));
+            const uint4 c0 = __ldg(cp), c1 = __ldg(cp + 1);
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t q = (cw[i] >> (8 * k + 4 * h)) & 15u;
+                    w[4 * i + k] = __fsub_rn(__fmul_rn(D, static_cast<float>(q)), Mj);
+                }
+            for (int t = 0; t < n_tok; ++t) {
+                const float* x = X + t * K + b * 32;
+                float a = acc[t];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a = fmaf(w[i], __ldg(x + i), a);
+                acc[t] = a;
+            }
+        }
+        for (int t = 0; t < n_tok; ++t) {
+            float a = acc[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            if (lane == 0) Y[t * M + row] = a;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------
@@ -1162,6 +1387,17 @@ cudaError_t launch_stream_nt(GemvParams<kMaxProbs>& P, const DeviceInfo* info, c
     }
 }
 
+// Weights and bytes of one chunk (one ring-stage column) of a block type.
+int chunk_weights(gq_type t) {
+    return t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kWPC
+                             : (t == GQ_TYPE_Q8_0 ? Geo<GQ_TYPE_Q8_0>::kWPC : Geo<GQ_TYPE_Q4_K>::kWPC);
+}
+int chunk_bytes(gq_type t) {
+    return t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kChunkBytes
+                             : (t == GQ_TYPE_Q8_0 ? Geo<GQ_TYPE_Q8_0>::kChunkBytes
+                                                  : Geo<GQ_TYPE_Q4_K>::kChunkBytes);
+}
+
 template <int kMaxProbs, int kXM = 0, int kFuse = 0>
 cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t tok0,
                           int n_tok, const DeviceInfo* info, cudaStream_t s) {
@@ -1169,9 +1405,8 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
     P.count = count;
     P.n_tok = n_tok;
     P.status = info->status;
-    const int wpc = t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kWPC : Geo<GQ_TYPE_Q8_0>::kWPC;
-    const int cb = t == GQ_TYPE_Q4_0 ? Geo<GQ_TYPE_Q4_0>::kChunkBytes
-                                     : Geo<GQ_TYPE_Q8_0>::kChunkBytes;
+    const int wpc = chunk_weights(t);
+    const int cb = chunk_bytes(t);
     int64_t bytes = 0, cost = 0;
     int max_c = 1;
     for (int i = 0; i < count; ++i) {
@@ -1196,7 +1431,11 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
     P.total_cost = cost;
     P.max_c = max_c;
     if (t == GQ_TYPE_Q4_0) return launch_stream_nt<GQ_TYPE_Q4_0, kMaxProbs, kXM, kFuse>(P, info, s);
-    return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs, kXM, kFuse>(P, info, s);
+    if (t == GQ_TYPE_Q8_0) return launch_stream_nt<GQ_TYPE_Q8_0, kMaxProbs, kXM, kFuse>(P, info, s);
+    // Q4_K: plain products only (the callers route its other forms elsewhere)
+    if constexpr (kXM == 0 && kFuse == 0)
+        return launch_stream_nt<GQ_TYPE_Q4_K, kMaxProbs, kXM, kFuse>(P, info, s);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_tok,
@@ -1207,8 +1446,10 @@ cudaError_t launch_generic(gq_type t, const MatProblem& p, int64_t tok0, int n_t
     float* Y = p.Y + tok0 * p.M;
     if (t == GQ_TYPE_Q4_0)
         gemv_generic_kernel<GQ_TYPE_Q4_0><<<grid, 256, 0, s>>>(p.W, p.M, p.K, X, n_tok, Y);
-    else
+    else if (t == GQ_TYPE_Q8_0)
         gemv_generic_kernel<GQ_TYPE_Q8_0><<<grid, 256, 0, s>>>(p.W, p.M, p.K, X, n_tok, Y);
+    else
+        gemv_generic_q4k_kernel<<<grid, 256, 0, s>>>(p.W, p.M, p.K, X, n_tok, Y);
     return cudaGetLastError();
 }
 
@@ -1222,9 +1463,10 @@ bool stream_shape_ok(const MatProblem& p) {
 // Whether the shared-memory plan for `n_tok` tokens of this problem fits the device.
 template <int kXM = 0>
 bool stream_fits(gq_type t, const MatProblem& p, int n_tok, const DeviceInfo* info) {
-    const int c = static_cast<int>(p.K / (t == GQ_TYPE_Q4_0 ? 256 : 128));
-    const int64_t smem = t == GQ_TYPE_Q4_0 ? stream_smem_bytes<GQ_TYPE_Q4_0, kXM>(n_tok, c)
-                                           : stream_smem_bytes<GQ_TYPE_Q8_0, kXM>(n_tok, c);
+    const int c = static_cast<int>(p.K / chunk_weights(t));
+    const int64_t smem = t == GQ_TYPE_Q4_0   ? stream_smem_bytes<GQ_TYPE_Q4_0, kXM>(n_tok, c)
+                         : t == GQ_TYPE_Q8_0 ? stream_smem_bytes<GQ_TYPE_Q8_0, kXM>(n_tok, c)
+                                             : stream_smem_bytes<GQ_TYPE_Q4_K, 0>(n_tok, c);
     return smem <= info->max_smem_optin;
 }
 
@@ -1309,6 +1551,7 @@ namespace gq {
 // (p.gamma) and the gate/up pair with Swish(gate) * up written directly (p.W2). Shapes the
 // streaming kernel takes only; the caller composes the other shapes from plain kernels.
 bool fused_decode_eligible(gq_type t, const MatProblem& p) {
+    if (t != GQ_TYPE_Q4_0 && t != GQ_TYPE_Q8_0) return false;   // Q4_K: composite forms
     DeviceInfo* info = nullptr;
     if (current_device_info(&info) != cudaSuccess) return false;
     if (p.gamma && reinterpret_cast<uintptr_t>(p.gamma) % 16 != 0) return false;   // float4

@@ -1123,7 +1123,8 @@ cudaError_t launch_tc_type(const MatProblem* probs, int count, int64_t N, uint8_
 
 }  // namespace
 
-bool gemv_tc_eligible(const MatProblem& p, int64_t N) {
+bool gemv_tc_eligible(gq_type t, const MatProblem& p, int64_t N) {
+    if (t != GQ_TYPE_Q4_0 && t != GQ_TYPE_Q8_0) return false;   // 32-weight block types
     if (N < kGemvTcMinTokens || N > kGemvTcMaxTokens) return false;
     if (p.K % kSuperK != 0 || p.K > (int64_t(1) << 24) || p.M <= 0) return false;
     return reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 4 == 0;

@@ -9,11 +9,23 @@
 
 namespace gq {
 
-constexpr int kQ4Bytes = 18;   // fp16 scale + 16 bytes of nibble codes
-constexpr int kQ8Bytes = 34;   // fp16 scale + 32 int8 codes
+constexpr int kQ4Bytes = 18;    // fp16 scale + 16 bytes of nibble codes
+constexpr int kQ8Bytes = 34;    // fp16 scale + 32 int8 codes
+constexpr int kQ4KBytes = 144;  // Q4_K super-block: fp16 d, fp16 dmin, 12 scale bytes, 128 code bytes
+constexpr int kQ4KWeights = 256;
 
 inline int block_bytes_of(gq_type t) {
-    return t == GQ_TYPE_Q4_0 ? kQ4Bytes : (t == GQ_TYPE_Q8_0 ? kQ8Bytes : 0);
+    switch (t) {
+        case GQ_TYPE_Q4_0: return kQ4Bytes;
+        case GQ_TYPE_Q8_0: return kQ8Bytes;
+        case GQ_TYPE_Q4_K: return kQ4KBytes;
+    }
+    return 0;
+}
+
+// Weights per block: 32, or 256 for a Q4_K super-block; 0 for an unknown type.
+inline int block_weights_of(gq_type t) {
+    return t == GQ_TYPE_Q4_K ? kQ4KWeights : (block_bytes_of(t) ? 32 : 0);
 }
 
 // One validated, non-empty mul_mat problem (K > 0, M > 0) as the launchers see it.
@@ -39,6 +51,7 @@ struct DeviceInfo {
 };
 cudaError_t current_device_info(DeviceInfo** out);
 
+// n_blocks blocks of block_weights_of(t) weights each, consecutive in W and in out.
 cudaError_t launch_quantize(gq_type t, const float* W, int64_t n_blocks, uint8_t* out,
                             cudaStream_t s);
 cudaError_t launch_dequantize(gq_type t, const uint8_t* blocks, int64_t n_elems, float* out,
@@ -82,7 +95,7 @@ cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspa
 // bf16 X tiles, 16 / 32 / 64 token rows per problem), 256-byte aligned.
 constexpr int64_t kGemvTcMinTokens = 3;
 constexpr int64_t kGemvTcMaxTokens = 64;
-bool gemv_tc_eligible(const MatProblem& p, int64_t N);
+bool gemv_tc_eligible(gq_type t, const MatProblem& p, int64_t N);
 int64_t gemv_tc_workspace_bytes(const MatProblem* probs, int count, int64_t N);
 cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_t N,
                            void* workspace, cudaStream_t s);

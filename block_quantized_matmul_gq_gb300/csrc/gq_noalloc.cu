@@ -62,9 +62,9 @@ bool aligned_to(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>
 extern "C" gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                                         const float* X, int64_t N, float* Y, void* stream) {
     // Same argument contract as gq_mul_mat.
-    if (t != GQ_TYPE_Q4_0 && t != GQ_TYPE_Q8_0) return GQ_ERR_TYPE;
+    if (gq::block_bytes_of(t) == 0) return GQ_ERR_TYPE;
     const int64_t max_dim = (int64_t(1) << 31) - 1, max_elems = int64_t(1) << 40;
-    if (M < 0 || K < 0 || N < 0 || K % 32 != 0) return GQ_ERR_SHAPE;
+    if (M < 0 || K < 0 || N < 0 || K % gq::block_weights_of(t) != 0) return GQ_ERR_SHAPE;
     if (M > max_dim || K > max_dim || N > max_dim) return GQ_ERR_SHAPE;
     if (M * K > max_elems || N * K > max_elems || N * M > max_elems) return GQ_ERR_SHAPE;
     if (M == 0 || N == 0) return GQ_OK;
@@ -82,7 +82,7 @@ extern "C" gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t
     // counters fit the array for any K up to ~390k; x_tiles_kernel rewrites the tiles and
     // zeroes the counters at the start of every call. Past that size, the CUDA-core decode
     // kernels, which need no workspace.
-    if (gq::gemv_tc_eligible(p, N)) {
+    if (gq::gemv_tc_eligible(t, p, N)) {
         if (gq::gemv_tc_workspace_bytes(&p, 1, N) > cap)
             return gq::launch_mul_mat(t, &p, 1, N, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
         void* scratch = nullptr;

@@ -71,6 +71,60 @@ WORKLOADS = {
 }
 
 
+def q4k_superblocks(M: int, K: int, seed: int):
+    """Hand-made Q4_K super-block bytes (numpy uint8, M x K/256 super-blocks of 144 bytes,
+    the published GGUF Q4_K layout: fp16 d, fp16 dmin, 12 scale bytes, 128 code bytes).
+    Row m has kind m % 8:
+      0  random scale and code bytes, d and dmin N(0, 0.01) of either sign
+      1  every scale and min at 63 (all twelve scale bytes 0xFF), codes 0 and 15 only,
+         d and dmin +-65504 (the largest finite fp16)
+      2  random bytes, d and dmin fp16 subnormals of either sign
+      3  random bytes, d and dmin +0 or -0 (the row's weights are exactly zero)
+      4  random bytes, d and dmin both negative
+      5-7 random bytes, each super-block's d and dmin drawn from all of the above
+    Only bytes are drawn here; nothing of the method is computed."""
+    import numpy as np
+    if K % 256:
+        raise ValueError("K must be a multiple of 256")
+    rng = np.random.default_rng(seed)
+    nsb = K // 256
+    blocks = rng.integers(0, 256, size=(M, nsb, 144), dtype=np.uint8)
+
+    def normal(shape):
+        return (rng.standard_normal(shape) * 0.01).astype(np.float16).view(np.uint16)
+
+    def subnormal(shape):
+        return (rng.integers(1, 1024, shape) | (rng.integers(0, 2, shape) << 15)).astype(np.uint16)
+
+    def huge(shape):
+        return (np.uint16(_F16_MAX) | (rng.integers(0, 2, shape) << 15)).astype(np.uint16)
+
+    def zero(shape):
+        return (rng.integers(0, 2, shape) << 15).astype(np.uint16)
+
+    heads = np.empty((M, nsb, 2), np.uint16)
+    for m in range(M):
+        kind = m % 8
+        if kind == 0:
+            heads[m] = normal((nsb, 2))
+        elif kind == 1:
+            heads[m] = huge((nsb, 2))
+            blocks[m, :, 4:16] = 0xFF
+            blocks[m, :, 16:] = np.where(rng.random((nsb, 128)) < 0.5, 0x00, 0xFF)
+        elif kind == 2:
+            heads[m] = subnormal((nsb, 2))
+        elif kind == 3:
+            heads[m] = zero((nsb, 2))
+        elif kind == 4:
+            heads[m] = normal((nsb, 2)) | np.uint16(_F16_SIGN)
+        else:
+            pick = rng.integers(0, 4, (nsb, 2))
+            heads[m] = np.choose(pick, [normal((nsb, 2)), subnormal((nsb, 2)), huge((nsb, 2)),
+                                        zero((nsb, 2))]).astype(np.uint16)
+    blocks[:, :, 0:4] = heads.view(np.uint8).reshape(M, nsb, 4)
+    return blocks.reshape(M, nsb * 144)
+
+
 def weight_seed(workload: int, j: int) -> int:
     return 1000 * workload + j
 

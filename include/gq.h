@@ -61,14 +61,16 @@ extern "C" {
 
 typedef enum gq_type {
     GQ_TYPE_Q4_0 = 2,   /* 18-byte blocks: fp16 scale + 32 4-bit codes */
-    GQ_TYPE_Q8_0 = 8    /* 34-byte blocks: fp16 scale + 32 int8 codes */
+    GQ_TYPE_Q8_0 = 8,   /* 34-byte blocks: fp16 scale + 32 int8 codes */
+    GQ_TYPE_Q4_K = 12   /* 144-byte super-blocks of 256 weights (layout below) */
 } gq_type;
 
 typedef enum gq_status {
     GQ_OK = 0,
     GQ_ERR_NULL = -1,     /* a required pointer is NULL */
-    GQ_ERR_SHAPE = -2,    /* negative size, K not a multiple of 32, size overflow, count */
-    GQ_ERR_TYPE = -3,     /* unknown gq_type */
+    GQ_ERR_SHAPE = -2,    /* negative size, K not a multiple of the block (32 weights, 256
+                             for Q4_K), size overflow, count */
+    GQ_ERR_TYPE = -3,     /* unknown gq_type, or one the entry point does not take */
     GQ_ERR_ALIGN = -4,    /* W_blocks not 16-byte aligned, or an fp32 array not 4-byte */
     GQ_ERR_CUDA = -5,     /* a CUDA runtime call failed (launch, attribute, no device) */
     GQ_ERR_TIMEOUT = -6   /* a device-side wait ran out (reported by gq_get_last_error) */
@@ -77,11 +79,13 @@ typedef enum gq_status {
 /* Version of this ABI (GQ_ABI_VERSION of the header the library was built with). */
 int32_t gq_abi_version(void);
 
-/* Bytes of one 32-weight block: 18 (Q4_0) or 34 (Q8_0); 0 for an unknown type. */
+/* Bytes of one block: 18 (Q4_0) or 34 (Q8_0) per 32 weights, 144 (Q4_K) per 256; 0 for
+ * an unknown type. */
 size_t gq_block_bytes(gq_type t);
 
-/* Bytes of one quantized row of K weights: (K / 32) * gq_block_bytes(t); 0 if K is
- * negative or not a multiple of 32, or the type is unknown. */
+/* Bytes of one quantized row of K weights: (K / 32) * gq_block_bytes(t), or for Q4_K
+ * (K / 256) * 144; 0 if K is negative or not a multiple of the block, or the type is
+ * unknown. */
 size_t gq_row_bytes(gq_type t, int64_t K);
 
 /*
@@ -106,9 +110,39 @@ gq_status gq_quantize_q8_0(const float* W, int64_t M, int64_t K, void* W_blocks,
                            void* stream);
 
 /*
- * Expand blocks back to fp32: W_out[m][k] = (c - 8) * d (Q4_0) or c * d (Q8_0), exact in
- * fp32 ("Development Guide ...", section 6.2, the unpack and dequantize steps).
- * W_out receives M x K floats.
+ * Q4_K super-blocks. The pages name Q4_K as the 4-bit format of a ~600 MB TinyLLaMA
+ * ("Development Guide ...", section 6; "A Complete Guide to llama.cpp ...", section 2.2)
+ * without a layout; this is the published GGUF Q4_K block, 256 weights in eight
+ * sub-blocks of 32, 144 bytes:
+ *   bytes 0-1    d (fp16), the scale of the sub-block scales
+ *   bytes 2-3    dmin (fp16), the scale of the sub-block mins
+ *   bytes 4-15   s[0..11]: 6-bit sub-block scales sc_j and mins m_j,
+ *                j < 4:  sc_j = s[j] & 63, m_j = s[j + 4] & 63;
+ *                j >= 4: sc_j = (s[j + 4] & 15) | (s[j - 4] >> 6) << 4,
+ *                        m_j = (s[j + 4] >> 4) | (s[j] >> 6) << 4
+ *   bytes 16-143 4-bit codes q: byte 16 + 32 g + l holds weight 64 g + l (low nibble)
+ *                and weight 64 g + 32 + l (high nibble), g = 0..3, l = 0..31
+ *   What = d sc_j q - dmin m_j (both products exact in fp32, rounded once).
+ * gq_quantize_q4_k is this library's own quantizer (the format fixes only the
+ * dequantization): per sub-block lo = min(0, min w), hi = max w, step = (hi - lo) / 15,
+ * min = -lo; d = max step / 63 and dmin = max min / 63 (fp32 division, stored as fp16
+ * round to nearest even); sc_j = roundf(step_j / d), m_j = roundf(min_j / dmin), clamped
+ * to [0, 63] (0 where d or dmin is 0); codes roundf((w + M_j) / D_j) clamped to [0, 15]
+ * with D_j = fp16(d) sc_j and M_j = fp16(dmin) m_j (0 where D_j = 0). K must be a
+ * multiple of 256 (else GQ_ERR_SHAPE). Bit-for-bit reproducible.
+ * The mul_mat entry points take Q4_K on the CUDA-core decode kernels at every N (up to
+ * 4 tokens per pass over the weights; no workspace); gq_mul_mat_rmsnorm and
+ * gq_mul_mat_swiglu take it in their composite forms (norm kernel, then the product; two
+ * products, then the elementwise kernel); gq_mul_mat_q8x and gq_mul_mat_q8x_batched
+ * return GQ_ERR_TYPE for it (their activation blocks pair with 32-weight blocks).
+ */
+gq_status gq_quantize_q4_k(const float* W, int64_t M, int64_t K, void* W_blocks,
+                           void* stream);
+
+/*
+ * Expand blocks back to fp32: W_out[m][k] = (c - 8) * d (Q4_0), c * d (Q8_0), or
+ * d sc_j q - dmin m_j (Q4_K), exact up to Q4_K's one rounding ("Development Guide ...",
+ * section 6.2, the unpack and dequantize steps). W_out receives M x K floats.
  */
 gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                         float* W_out, void* stream);
@@ -184,7 +218,7 @@ gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t M, int64_t
 
 /* One independent problem of gq_mul_mat_batched. */
 typedef struct gq_mul_mat_problem {
-    const void* W_blocks;   /* M rows of K/32 blocks, 16-byte aligned */
+    const void* W_blocks;   /* M rows of gq_row_bytes(t, K) bytes, 16-byte aligned */
     const float* X;         /* N x K */
     float* Y;               /* N x M */
     int64_t M;

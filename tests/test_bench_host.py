@@ -23,6 +23,12 @@ def test_step_bytes_tinyllama():
     assert nb["total"] == nb["weights"] + nb["x"] + nb["y"]
 
 
+def test_step_bytes_q4_k_superblocks():
+    # 144 bytes per 256 weights: the same 0.5625 bytes per weight as Q4_0
+    nb = bench.step_bytes(workloads.tinyllama_decode_set(), 1, 144, 256)
+    assert nb["weights"] == 581_861_376
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
@@ -100,11 +106,13 @@ def test_summarize_keeps_every_workload():
     dec = {"single_q4_0_2048x2048": {"per_N": [row], "launch_floor": {"us": 2.0}},
            "tinyllama_decode_q4_0": {"per_N": [dict(row, N=2)]},
            "tinyllama_decode_q8_0": {"per_N": [row]},
-           "llama7b_decode_q4_0": {"per_N": [row, dict(row, N=16)]}}
+           "llama7b_decode_q4_0": {"per_N": [row, dict(row, N=16)]},
+           "tinyllama_decode_q4_k": {"per_N": [row, dict(row, N=4)]}}
     pf = {"tinyllama_prefill_n512": {"tflops": 900.0, "frac": 0.46},
           "llama7b_prefill_n2048_q8_0": {"tflops": 1100.0, "frac": 0.56}}
     s = bench.summarize(dec, pf, {"decode_us": {"single_2048x2048_N1": 4.0}}, 6796.9)
     assert s["w1_single_q4_0_2048x2048_N1"] == [3.0, 800.0, 0.12]
     assert s["w1_launch_floor_us"] == 2.0
     assert set(s["w5_llama7b_q4_0"]) == {"N1", "N16"}
+    assert set(s["w2_tinyllama_q4_k"]) == {"N1", "N4"}
     assert s["prefill_llama7b_prefill_n2048_q8_0"] == [1100.0, 0.56]

@@ -146,3 +146,38 @@ def test_fused_entry_points_argument_checks(gq_lib):
     assert sw(A16, A4, 2, 4, 64, A16, 1, A16, None) == -4            # up misaligned
     assert sw(None, A16, 2, 4, 64, A16, 1, A16, None) == -1          # gate missing
     assert sw(A16, A16, 2, 4, 64, A16, 0, A16, None) == 0            # N == 0
+
+
+def test_q4_k_sizes_and_host_checks(gq_lib):
+    """Q4_K super-blocks: 144 bytes per 256 weights; K must hold whole super-blocks, and the
+    entry points that take only 32-weight blocks refuse the type before any CUDA call."""
+    lib = gq_lib.lib
+    assert gq_lib.Q4_K == 12 and gq_lib.TYPES["q4_k"] == 12
+    assert lib.gq_block_bytes(12) == 144
+    assert lib.gq_row_bytes(12, 2048) == 8 * 144 and lib.gq_row_bytes(12, 5632) == 22 * 144
+    assert lib.gq_row_bytes(12, 288) == 0 and lib.gq_row_bytes(12, 0) == 0
+    q = lib.gq_quantize_q4_k
+    assert q(A16, 4, 288, A16, None) == -2                          # K % 256
+    assert q(A16, 4, 32, A16, None) == -2
+    assert q(None, 4, 256, A16, None) == -1
+    assert q(A2, 4, 256, A16, None) == -4
+    assert q(A16, 4, 256, A4, None) == -4
+    assert q(None, 0, 256, None, None) == 0
+    assert lib.gq_dequantize(A16, 12, 4, 288, A16, None) == -2
+    mm = lib.gq_mul_mat
+    assert mm(A16, 12, 4, 288, A16, 1, A16, None) == -2             # K % 256
+    assert mm(A4, 12, 4, 256, A16, 1, A16, None) == -4
+    assert mm(None, 12, 0, 256, None, 1, None, None) == 0
+    assert lib.gq_mul_mat_noalloc(A16, 12, 4, 288, A16, 1, A16, None) == -2
+    # the CUDA-core decode path needs no workspace at any N
+    for N in (1, 4, 16, 64, 512):
+        assert lib.gq_mul_mat_workspace_size(12, 64, 2048, N) == 0
+    # quantized activations pair with 32-weight blocks only
+    assert lib.gq_mul_mat_q8x(A16, 12, 4, 256, A16, 1, A16, None) == -3
+    P = gq_lib.Problem
+    arr = (P * 1)(P(A16, A16, A16, 4, 256))
+    assert lib.gq_mul_mat_q8x_batched(arr, 1, 12, 1, None) == -3
+    arr_bad = (P * 1)(P(A16, A16, A16, 4, 288))
+    assert lib.gq_mul_mat_batched(arr_bad, 1, 12, 1, None) == -2
+    assert lib.gq_mul_mat_rmsnorm(A16, 12, 4, 288, A16, A16, 1e-5, 1, A16, None) == -2
+    assert lib.gq_mul_mat_swiglu(A16, A16, 12, 4, 288, A16, 1, A16, None) == -2
