@@ -263,8 +263,8 @@ def run_reference(args, shapes):
 PREFILL_SETS = [("tinyllama_prefill_n512", 4, 512), ("llama7b_prefill_n2048", 5, 2048)]
 
 
-def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None, types=("q4_0", "q8_0"),
-                    rotate: bool = True):
+def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None,
+                    types=("q4_0", "q8_0", "q4_k"), rotate: bool = True):
     """Each prefill matrix as gq_mul_mat_ws calls replayed from a CUDA graph. Weight copies
     (distinct seeds) are rotated so that every call reads its weights from HBM, not from L2
     (TinyLLaMA gate / down are 6-7 MB, under the 129 MB L2); X and Y stay the same."""
@@ -318,7 +318,7 @@ def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None, types=("q4_0
                 del qs, X, Y, ws, g
             if rows:
                 tf = tot_flop / tot_s / 1e12
-                key = set_name if btype == "q4_0" else f"{set_name}_q8_0"
+                key = set_name if btype == "q4_0" else f"{set_name}_{btype}"
                 out[key] = {"type": btype, "tflops": round(tf, 1), "frac": round(tf / peak_tf, 4),
                             "matrices": rows}
         if binding.get_last_error() != 0:
@@ -334,7 +334,7 @@ DECODE_SETS = [
     ("tinyllama_decode_q8_0", 3, "q8_0", "tinyllama", (1, 2, 4, 8, 16)),
     ("llama7b_decode_q4_0", 5, "q4_0", "llama7b", (1, 16)),
     # the same TinyLLaMA weights (workload 2's seeds) in Q4_K super-blocks
-    ("tinyllama_decode_q4_k", 2, "q4_k", "tinyllama", (1, 2, 4)),
+    ("tinyllama_decode_q4_k", 2, "q4_k", "tinyllama", (1, 2, 4, 8, 16)),
 ]
 L2_BYTES = 129 * 2 ** 20
 STEPS_PER_GRAPH = 10
@@ -387,8 +387,7 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
             gbs = nb["total"] / sec / 1e9
             rows.append({"N": N, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
                          "frac": round(gbs / peak, 4),
-                         "path": "CUDA-core decode" if N <= 2 or btype == "q4_k"
-                         else "tensor-core decode"})
+                         "path": "CUDA-core decode" if N <= 2 else "tensor-core decode"})
             del runs, g
         if binding.get_last_error() != 0:
             raise RuntimeError("device status word set during the decode sets")
@@ -978,7 +977,7 @@ def main(argv=None):
                          "no clock sampling, no oracle); prints the device-timed line")
     ap.add_argument("--profile-prefill", metavar="MATRIX", default=None,
                     help="for ncu: time one prefill GEMM only, e.g. llama7b_prefill_n2048/lm_head "
-                         "(llama7b_prefill_n2048_q8_0/lm_head for Q8_0)")
+                         "(llama7b_prefill_n2048_q8_0/lm_head for Q8_0, _q4_k for Q4_K)")
     ap.add_argument("--profile-decode", metavar="TYPE/N", default=None,
                     help="for ncu: the TinyLLaMA decode step at N tokens, e.g. q8_0/16")
     args = ap.parse_args(argv)
@@ -989,8 +988,10 @@ def main(argv=None):
     if args.profile_prefill:
         import torch
         set_name, matrix = args.profile_prefill.split("/")
-        btype = "q8_0" if set_name.endswith("_q8_0") else "q4_0"
-        set_name = set_name.replace("_q8_0", "")
+        btype = "q4_0"
+        for suffix in ("_q8_0", "_q4_k"):
+            if set_name.endswith(suffix):
+                btype, set_name = suffix[1:], set_name[: -len(suffix)]
         emit(prefill_measure(torch.device("cuda", 0), reps=2, iters=1, only=(set_name, matrix),
                              types=(btype,), rotate=False))
         return

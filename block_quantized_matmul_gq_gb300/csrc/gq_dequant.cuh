@@ -2,7 +2,9 @@
 // kernels (prefill GEMM and tensor-core decode): raw Q4_0 / Q8_0 bytes in registers ->
 // (c - 8) * d or c * d, exact in fp32, rounded once to bf16, stored as 16-byte chunks of a
 // 128-byte-swizzled K-major row ("Development Guide for Small AI Models (TinyLLaMA, etc.)
-// Using C++", section 6.2: unpack with masks and shifts, then scale).
+// Using C++", section 6.2: unpack with masks and shifts, then scale). Q4_K sub-blocks
+// (published GGUF Q4_K layout) become d sc q - dmin m, rounded once in fp32 exactly as
+// gq_dequantize writes it, then once more to bf16.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,6 +30,12 @@ struct RawFmt<GQ_TYPE_Q8_0> {
     static constexpr int kBB = kQ8Bytes;
     static constexpr int kRow = 8 * kQ8Bytes;   // 272 bytes
     static constexpr int kElem = 2;             // uint16 elements keep the box <= 256
+};
+template <>
+struct RawFmt<GQ_TYPE_Q4_K> {
+    static constexpr int kBB = kQ4KBytes;       // the super-step is one super-block
+    static constexpr int kRow = kQ4KBytes;      // 144 bytes, as Q4_0
+    static constexpr int kElem = 1;
 };
 
 __device__ __forceinline__ uint32_t word_at(const uint32_t* r, int byte_off) {
@@ -129,6 +137,55 @@ __device__ __forceinline__ void dequant_block_at(const uint32_t* r, uint32_t (&o
     }
 }
 
+// (a - b) * c + e on two fp32 lanes at once (Blackwell packed fp32): the subtraction is
+// exact where it is used (2^23 + q - 2^23), the fma rounds once.
+__device__ __forceinline__ float2 sub_fma2(float2 a, float2 b, float2 c, float2 e) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, c, e, t;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "mov.b64 e, {%8, %9};\n\t"
+        "sub.rn.f32x2 t, a, b;\n\tfma.rn.f32x2 t, t, c, e;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(e.x), "f"(e.y));
+    return r;
+}
+
+// Q4_K sub-block 2 quarter + h of a super-block: hd = its 16 header bytes (fp16 d and
+// dmin, the packed 6-bit scales and mins), cw[0..7] = the quarter's 32 code bytes (word i:
+// elements 4i .. 4i + 3 of the sub-block, in nibble h of each byte). Each value is
+// fma(q, D, -M) with D = d sc and M = dmin m (both exact), i.e. d sc q - dmin m rounded
+// once in fp32, then rounded to bf16; out[i] = elements 2i, 2i + 1.
+template <int h>
+__device__ __forceinline__ void dequant_q4k_sub(const uint4& hd, int quarter, const uint32_t* cw,
+                                                uint32_t (&out)[16]) {
+    uint32_t sc2, m2;
+    q4k_scales(hd, quarter, sc2, m2);
+    const float D = __fmul_rn(half_bits_to_float(hd.x & 0xFFFFu),
+                              static_cast<float>((sc2 >> (8 * h)) & 0xFFu));
+    const float Mn = -__fmul_rn(half_bits_to_float(hd.x >> 16),
+                                static_cast<float>((m2 >> (8 * h)) & 0xFFu));
+    const float2 dd = make_float2(D, D), mm = make_float2(Mn, Mn);
+    const float2 off = make_float2(8388608.0f, 8388608.0f);   // 2^23
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = (cw[i] >> (4 * h)) & 0x0F0F0F0Fu;
+        const float2 p0 = sub_fma2(make_float2(byte_as_float<0>(w), byte_as_float<1>(w)), off, dd, mm);
+        const float2 p1 = sub_fma2(make_float2(byte_as_float<2>(w), byte_as_float<3>(w)), off, dd, mm);
+        const __nv_bfloat162 b0 = __floats2bfloat162_rn(p0.x, p0.y);
+        const __nv_bfloat162 b1 = __floats2bfloat162_rn(p1.x, p1.y);
+        out[2 * i] = *reinterpret_cast<const uint32_t*>(&b0);
+        out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+    }
+}
+
+// Q4_K sub-block j (0..7) of the super-block whose 144 bytes are in r (header words
+// r[0..3], quarter q's code words r[4 + 8q .. 4 + 8q + 7]).
+template <int j>
+__device__ __forceinline__ void dequant_subblock_q4k(const uint32_t* r, uint32_t (&out)[16]) {
+    dequant_q4k_sub<j & 1>(make_uint4(r[0], r[1], r[2], r[3]), j >> 1, r + 4 + 8 * (j >> 1), out);
+}
+
 // Codes only: the 32 exact integers c - 8 of the Q4_0 block that starts at byte kOff of r,
 // as bf16 pairs in the order of dequant_block_at (out[i] = elements 2i, 2i + 1). The
 // block's scale is applied to the product afterwards, in fp32.
@@ -153,10 +210,14 @@ __device__ __forceinline__ void q4_codes_at(const uint32_t* r, uint32_t (&out)[1
     }
 }
 
-// Block `blk` (0..7) of a row's super-step, raw bytes in r from the super-step's start.
+// Block `blk` (0..7) of a row's super-step (Q4_K: sub-block blk of its super-block), raw
+// bytes in r from the super-step's start.
 template <int kType, int blk>
 __device__ __forceinline__ void dequant_block(const uint32_t* r, uint32_t (&out)[16]) {
-    dequant_block_at<kType, blk * RawFmt<kType>::kBB>(r, out);
+    if constexpr (kType == GQ_TYPE_Q4_K)
+        dequant_subblock_q4k<blk>(r, out);
+    else
+        dequant_block_at<kType, blk * RawFmt<kType>::kBB>(r, out);
 }
 
 // Block 2q + h of the super-step, as four 16-byte chunks of the A row (elements

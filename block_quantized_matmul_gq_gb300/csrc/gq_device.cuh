@@ -142,4 +142,24 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
 
+// Q4_K. The 6-bit scales sc and mins m of sub-blocks 2g and 2g + 1 of a super-block
+// whose 16 header bytes are hd (fp16 d | fp16 dmin << 16, then scale bytes s[0..11]), as
+// two 8-bit lanes of a word: bits 0..7 for sub-block 2g, 8..15 for 2g + 1. The published
+// packing: j < 4: sc_j = s[j] & 63, m_j = s[j + 4] & 63; j >= 4: sc_j = (s[j + 4] & 15) |
+// (s[j - 4] >> 6) << 4, m_j = (s[j + 4] >> 4) | (s[j] >> 6) << 4. Sub-blocks 2g, 2g + 1
+// take bytes 2 (g & 1) and 2 (g & 1) + 1 of each group of four scale bytes.
+__device__ __forceinline__ void q4k_scales(const uint4& hd, int g, uint32_t& sc, uint32_t& m) {
+    const int sh = 16 * (g & 1);
+    const uint32_t a = (hd.y >> sh) & 0xFFFFu;   // s[j'] pair
+    const uint32_t b = (hd.z >> sh) & 0xFFFFu;   // s[4 + j'] pair
+    const uint32_t c = (hd.w >> sh) & 0xFFFFu;   // s[8 + j'] pair
+    if (g < 2) {
+        sc = a & 0x3F3Fu;
+        m = b & 0x3F3Fu;
+    } else {
+        sc = (c & 0x0F0Fu) | ((a >> 2) & 0x3030u);
+        m = ((c >> 4) & 0x0F0Fu) | ((b >> 2) & 0x3030u);
+    }
+}
+
 }  // namespace gq

@@ -18,7 +18,8 @@
 //               stage; it turns the block into 32 bf16 values, each (c - 8) * d (or c * d)
 //               computed exactly in fp32 (packed f32x2 arithmetic) and rounded once to
 //               bf16, and stores them in the 128-byte-swizzled K-major layout the MMA
-//               reads. After the K loop the same warps read the accumulator out of TMEM
+//               reads. A Q4_K super-step is one super-block (144 bytes, as 8 Q4_0 blocks);
+//               its "blocks" are the eight sub-blocks, each d sc q - dmin m. After the K loop the same warps read the accumulator out of TMEM
 //               (tcgen05.ld; warp w owns lanes 32*(w%4).., half the token columns) and
 //               write Y.
 // Shapes whose 256-token tiles fill two or more waves use 512-token tiles instead
@@ -60,11 +61,11 @@ constexpr unsigned long long kDrainNs = 100000000ull;   // 100 ms
 template <int kType, int kBN>
 struct Layout {
     // The dequant warps copy a raw super-step into registers as soon as it lands, so one
-    // raw stage already gives the next copy four MMA stages of lead; Q4_0 then fits four
-    // 48 KB operand stages. Q8_0 (272-byte raw rows) keeps two raw stages and three
-    // operand stages.
-    static constexpr int kRawStages = kType == GQ_TYPE_Q4_0 ? 1 : 2;
-    static constexpr int kStages = kBN >= 128 ? (kType == GQ_TYPE_Q4_0 ? 4 : 3) : 6;
+    // raw stage already gives the next copy four MMA stages of lead; Q4_0 and Q4_K (144-byte
+    // raw rows) then fit four 48 KB operand stages. Q8_0 (272-byte raw rows) keeps two raw
+    // stages and three operand stages.
+    static constexpr int kRawStages = kType != GQ_TYPE_Q8_0 ? 1 : 2;   // Q4_K rows are Q4_0's size
+    static constexpr int kStages = kBN >= 128 ? (kType != GQ_TYPE_Q8_0 ? 4 : 3) : 6;
     static constexpr int kA = kBM * kBK * 2;
     static constexpr int kB = kBN * kBK * 2;
     static constexpr int kRaw = kBM * RawFmt<kType>::kRow;
@@ -380,9 +381,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 template <int kType>
 struct WideLayout {
     static constexpr int kHalfN = 256;
-    static constexpr int kRawStages = kType == GQ_TYPE_Q4_0 ? 1 : 2;
+    static constexpr int kRawStages = kType != GQ_TYPE_Q8_0 ? 1 : 2;
     static constexpr int kAStages = 2;
-    static constexpr int kUnits = kType == GQ_TYPE_Q4_0 ? 5 : 3;
+    static constexpr int kUnits = kType != GQ_TYPE_Q8_0 ? 5 : 3;
     static constexpr int kA = kBM * kBK * 2;
     static constexpr int kU = kHalfN * kBK * 2;
     static constexpr int kRaw = kBM * RawFmt<kType>::kRow;
@@ -747,7 +748,7 @@ cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* x
     using L = Layout<kType, kBN>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const int64_t row_bytes = (p.K / 32) * RawFmt<kType>::kBB;
+    const int64_t row_bytes = (p.K / kSuperK) * RawFmt<kType>::kRow;
     CUtensorMap tw{}, tx{};
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / RawFmt<kType>::kElem),
@@ -756,7 +757,7 @@ cudaError_t launch_gemm_t(const MatProblem& p, int64_t N, const __nv_bfloat16* x
         const cuuint32_t box[2] = {static_cast<cuuint32_t>(RawFmt<kType>::kRow / RawFmt<kType>::kElem),
                                    static_cast<cuuint32_t>(kBM)};
         const cuuint32_t estr[2] = {1, 1};
-        CUresult r = enc(&tw, kType == GQ_TYPE_Q4_0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+        CUresult r = enc(&tw, kType != GQ_TYPE_Q8_0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT16,
                          2, const_cast<uint8_t*>(p.W), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -817,7 +818,7 @@ int64_t gemm_x_bytes(int64_t K, int64_t N) { return (N * K * 2 + 255) / 256 * 25
 int64_t gemm_workspace_bytes(int64_t K, int64_t N) { return gemm_x_bytes(K, N); }
 
 bool gemm_eligible(gq_type t, const MatProblem& p, int64_t N) {
-    if (t != GQ_TYPE_Q4_0 && t != GQ_TYPE_Q8_0) return false;   // 32-weight block types
+    if (block_bytes_of(t) == 0) return false;
     if (N < kGemmMinTokens || p.K % kSuperK != 0 || p.M <= 0) return false;
     if (p.M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 24) || p.K > (int64_t(1) << 24))
         return false;
@@ -838,6 +839,7 @@ cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspa
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (t == GQ_TYPE_Q4_0) return launch_gemm_t<GQ_TYPE_Q4_0, 256>(p, N, xb, info, s);
+    if (t == GQ_TYPE_Q4_K) return launch_gemm_t<GQ_TYPE_Q4_K, 256>(p, N, xb, info, s);
     return launch_gemm_t<GQ_TYPE_Q8_0, 256>(p, N, xb, info, s);
 }
 

@@ -30,7 +30,9 @@
 // block's MMAs write the block's own accumulator, and the dequantize warps add
 // d_blk * acc_blk to a per-row fp32 sum one super-step behind the MMAs; the two groups'
 // halves of a tile meet in shared memory and group 0 writes Y. The weights are never
-// rounded. Other forms dequantize to bf16 ((c - 8) * d or c * d, rounded once).
+// rounded. Other forms dequantize to bf16 ((c - 8) * d or c * d, rounded once; Q4_K
+// sub-blocks d sc q - dmin m, rounded once in fp32 and once to bf16: a 256-k super-step is
+// one 144-byte super-block, and group g takes its sub-blocks 4g .. 4g + 3).
 // All waits are bounded: a CTA that gives up records a timeout in the status word, lets
 // its copies and MMAs land, frees its TMEM and leaves.
 #include <cuda.h>   // CUtensorMap and its enums (header only; no libcuda link)
@@ -806,7 +808,8 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCols;
             int raw_n = 0;
             bool ok = true;
-            uint32_t raw[kHalfWords];
+            // Q4_K: the 16 header bytes and 64 code bytes of the group's two quarters
+            uint32_t raw[kType == GQ_TYPE_Q4_K ? 20 : kHalfWords];
             for (; w.valid && ok; tc_walk_next(P, w), ++raw_n) {
                 const int r = raw_n % R;
                 if (!mbar_wait(raw_full(r), (raw_n / R) & 1)) {
@@ -815,7 +818,23 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                 }
                 // Every row of the box is loaded; rows past the matrix end arrive as zeros and
                 // dequantize to zero operands (their outputs are dropped).
-                {
+                if constexpr (kType == GQ_TYPE_Q4_K) {
+                    // the super-block's 16 header bytes and the code bytes of its quarters
+                    // 2g and 2g + 1 (sub-blocks 4g .. 4g + 3): raw[0..3], raw[4..19]
+                    const uint8_t* rowp = base + L::kOffRaw + r * L::kStage + row * L::kRawRow;
+                    uint32_t dep = 0;
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            rowp + (i == 0 ? 0 : 16 + 64 * g + 16 * (i - 1)));
+                        raw[4 * i] = v.x;
+                        raw[4 * i + 1] = v.y;
+                        raw[4 * i + 2] = v.z;
+                        raw[4 * i + 3] = v.w;
+                        dep ^= v.x;
+                    }
+                    release_to_async_proxy(dep);
+                } else {
                     const uint8_t* src = base + L::kOffRaw + r * L::kStage + row * L::kRawRow +
                                          g * (L::kRawRow / 2);
                     uint32_t dep;
@@ -836,25 +855,38 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
                 }
                 tc_fence_after();
                 const uint32_t a_slot = a_lane + (g * G + gi) * kSlotCols;
-                {
+                if constexpr (kType == GQ_TYPE_Q4_K) {
+                    const uint4 hd = make_uint4(raw[0], raw[1], raw[2], raw[3]);
                     uint32_t packed[16];
-                    dequant_block<kType, 0>(raw, packed);
+                    dequant_q4k_sub<0>(hd, 2 * g, raw + 4, packed);
                     tmem_st16(a_slot, packed);
-                }
-                {
-                    uint32_t packed[16];
-                    dequant_block<kType, 1>(raw, packed);
+                    dequant_q4k_sub<1>(hd, 2 * g, raw + 4, packed);
                     tmem_st16(a_slot + 16, packed);
-                }
-                {
-                    uint32_t packed[16];
-                    dequant_block<kType, 2>(raw, packed);
+                    dequant_q4k_sub<0>(hd, 2 * g + 1, raw + 12, packed);
                     tmem_st16(a_slot + 32, packed);
-                }
-                {
-                    uint32_t packed[16];
-                    dequant_block<kType, 3>(raw, packed);
+                    dequant_q4k_sub<1>(hd, 2 * g + 1, raw + 12, packed);
                     tmem_st16(a_slot + 48, packed);
+                } else {
+                    {
+                        uint32_t packed[16];
+                        dequant_block<kType, 0>(raw, packed);
+                        tmem_st16(a_slot, packed);
+                    }
+                    {
+                        uint32_t packed[16];
+                        dequant_block<kType, 1>(raw, packed);
+                        tmem_st16(a_slot + 16, packed);
+                    }
+                    {
+                        uint32_t packed[16];
+                        dequant_block<kType, 2>(raw, packed);
+                        tmem_st16(a_slot + 32, packed);
+                    }
+                    {
+                        uint32_t packed[16];
+                        dequant_block<kType, 3>(raw, packed);
+                        tmem_st16(a_slot + 48, packed);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -1014,7 +1046,7 @@ cudaError_t weight_map(const uint8_t* W, int64_t M, int64_t K, CUtensorMap* out)
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     constexpr int kElem = RawFmt<kType>::kElem;
-    const int64_t row_bytes = (K / 32) * RawFmt<kType>::kBB;
+    const int64_t row_bytes = (K / kSuperK) * RawFmt<kType>::kRow;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / kElem), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(RawFmt<kType>::kRow / kElem),
@@ -1084,7 +1116,7 @@ cudaError_t launch_tc_t(const MatProblem* probs, int count, int64_t N, uint8_t* 
         g.Y = probs[i].Y;
         g.M = probs[i].M;
         g.K = static_cast<int32_t>(probs[i].K);
-        g.row_bytes = (probs[i].K / 32) * RawFmt<kType>::kBB;
+        g.row_bytes = (probs[i].K / kSuperK) * RawFmt<kType>::kRow;
         g.nsuper = static_cast<int32_t>(probs[i].K / kSuperK);
         g.unit_begin = units;
         units += (g.M + kBM - 1) / kBM * g.nsuper;
@@ -1124,7 +1156,7 @@ cudaError_t launch_tc_type(const MatProblem* probs, int count, int64_t N, uint8_
 }  // namespace
 
 bool gemv_tc_eligible(gq_type t, const MatProblem& p, int64_t N) {
-    if (t != GQ_TYPE_Q4_0 && t != GQ_TYPE_Q8_0) return false;   // 32-weight block types
+    if (block_bytes_of(t) == 0) return false;
     if (N < kGemvTcMinTokens || N > kGemvTcMaxTokens) return false;
     if (p.K % kSuperK != 0 || p.K > (int64_t(1) << 24) || p.M <= 0) return false;
     return reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 4 == 0;
@@ -1153,9 +1185,9 @@ cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_
     if (e != cudaSuccess) return e;
     for (int i0 = 0; i0 < count; i0 += kMaxLaunchProbs) {
         const int n = std::min(kMaxLaunchProbs, count - i0);
-        e = t == GQ_TYPE_Q4_0
-                ? launch_tc_type<GQ_TYPE_Q4_0>(probs + i0, n, N, part, xt, info, s)
-                : launch_tc_type<GQ_TYPE_Q8_0>(probs + i0, n, N, part, xt, info, s);
+        e = t == GQ_TYPE_Q4_0   ? launch_tc_type<GQ_TYPE_Q4_0>(probs + i0, n, N, part, xt, info, s)
+            : t == GQ_TYPE_Q4_K ? launch_tc_type<GQ_TYPE_Q4_K>(probs + i0, n, N, part, xt, info, s)
+                                : launch_tc_type<GQ_TYPE_Q8_0>(probs + i0, n, N, part, xt, info, s);
         if (e != cudaSuccess) return e;
         for (int i = i0; i < i0 + n; ++i) xt += static_cast<int64_t>(npad_for(N)) * probs[i].K * 2;
     }

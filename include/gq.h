@@ -130,8 +130,10 @@ gq_status gq_quantize_q8_0(const float* W, int64_t M, int64_t K, void* W_blocks,
  * to [0, 63] (0 where d or dmin is 0); codes roundf((w + M_j) / D_j) clamped to [0, 15]
  * with D_j = fp16(d) sc_j and M_j = fp16(dmin) m_j (0 where D_j = 0). K must be a
  * multiple of 256 (else GQ_ERR_SHAPE). Bit-for-bit reproducible.
- * The mul_mat entry points take Q4_K on the CUDA-core decode kernels at every N (up to
- * 4 tokens per pass over the weights; no workspace); gq_mul_mat_rmsnorm and
+ * The mul_mat entry points take Q4_K on the same paths as Q4_0 (CUDA-core decode for
+ * N <= 2, tensor-core decode for 3..64 tokens, prefill GEMM from 65, with the same
+ * workspace sizes); the tensor-core paths use each weight d sc q - dmin m rounded once in
+ * fp32, as gq_dequantize writes it, then rounded to bf16. gq_mul_mat_rmsnorm and
  * gq_mul_mat_swiglu take it in their composite forms (norm kernel, then the product; two
  * products, then the elementwise kernel); gq_mul_mat_q8x and gq_mul_mat_q8x_batched
  * return GQ_ERR_TYPE for it (their activation blocks pair with 32-weight blocks).
@@ -159,8 +161,11 @@ gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * dequantized values (rounded once), except Q4_0 decode with N <= 16, which multiplies
  * the exact codes c - 8 and applies each block's scale in fp32.
  * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element (for the bf16
- * path, at the K >= 256 it runs on, by a wide margin for non-adversarial data). Results
- * are deterministic: the same inputs give the same bits on every call.
+ * path, at the K >= 256 it runs on, by a wide margin for non-adversarial data). Q4_K on
+ * the CUDA-core kernels forms d (sum sc S) - dmin (sum m X) per quarter super-block in
+ * fp32; where the two terms cancel (super-block bytes the quantizer does not write) add
+ * (K / 256 + 32) * 2^-23 * sum_k (|d sc_j q_k| + |dmin m_j|) |X[n][k]| to the bound.
+ * Results are deterministic: the same inputs give the same bits on every call.
  * Y must not overlap W_blocks or X.
  */
 gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,

@@ -169,9 +169,13 @@ def test_q4_k_sizes_and_host_checks(gq_lib):
     assert mm(A4, 12, 4, 256, A16, 1, A16, None) == -4
     assert mm(None, 12, 0, 256, None, 1, None, None) == 0
     assert lib.gq_mul_mat_noalloc(A16, 12, 4, 288, A16, 1, A16, None) == -2
-    # the CUDA-core decode path needs no workspace at any N
-    for N in (1, 4, 16, 64, 512):
-        assert lib.gq_mul_mat_workspace_size(12, 64, 2048, N) == 0
+    # the same workspace as Q4_0 on every path: none for N <= 2, X tiles and partial sums for
+    # the tensor-core decode, the bf16 copy of X for prefill
+    for N in (1, 2, 4, 16, 40, 64, 512):
+        assert lib.gq_mul_mat_workspace_size(12, 64, 2048, N) == \
+            lib.gq_mul_mat_workspace_size(2, 64, 2048, N)
+    assert lib.gq_mul_mat_workspace_size(12, 64, 2048, 2) == 0
+    assert lib.gq_mul_mat_workspace_size(12, 64, 2048, 512) == 512 * 2048 * 2
     # quantized activations pair with 32-weight blocks only
     assert lib.gq_mul_mat_q8x(A16, 12, 4, 256, A16, 1, A16, None) == -3
     P = gq_lib.Problem

@@ -344,7 +344,7 @@ GEMM = [(128, 256, 64), (7, 256, 64), (300, 512, 100), (129, 768, 300), (1000, 2
         (256, 5632, 64), (128, 256, 65), (520, 1792, 130), (1001, 1280, 70)]
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 @pytest.mark.parametrize("M,K,N", GEMM)
 def test_gemm_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
     assert gq_lib.workspace_size(t, M, K, N) >= N * K * 2
@@ -352,7 +352,7 @@ def test_gemm_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
     check_tolerance(Y, Y_ref, What, X, f"gemm {t} M={M} K={K} N={N}")
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 def test_gemm_one_hot_returns_bf16_weights(gq_lib, oracle_mod, cuda_dev, t):
     """X = e_k: Y[n][m] is bf16(What[m][k]) exactly (one nonzero product, fp32 sum). This
     pins the in-kernel dequantization, the swizzled operand layouts and the descriptors."""
@@ -418,7 +418,7 @@ def test_llama7b_prefill_full_size(gq_lib, oracle_mod, cuda_dev):
 GEMM_WIDE = [(10240, 512, 300), (9728, 768, 777)]
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 @pytest.mark.parametrize("M,K,N", GEMM_WIDE)
 def test_gemm_wide_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
     _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 7, t, N, [workloads.MatShape("wide", M, K)],
@@ -430,14 +430,14 @@ def test_gemm_wide_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
 GEMM_UNSPLIT = [(10236, 256, 200), (10239, 256, 200)]
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 @pytest.mark.parametrize("M,K,N", GEMM_UNSPLIT)
 def test_gemm_unsplit_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
     _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 8, t, N, [workloads.MatShape("tile", M, K)],
                         rows_per_mat=24)
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 def test_gemm_wide_tiles_deterministic(gq_lib, cuda_dev, t):
     M, K, N = GEMM_WIDE[1]
     q = gq_lib.quantize(workloads.weights(M, K, 8, device=cuda_dev), t)
@@ -455,20 +455,21 @@ DECODE_TC = [(1, 256, 5), (7, 2048, 8), (129, 2048, 16), (1000, 2048, 17), (300,
              (200, 11008, 33), (128, 512, 64), (2048, 4096, 16)]
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 @pytest.mark.parametrize("M,K,N", DECODE_TC)
 def test_decode_tc_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
     Y, Y_ref, What, X = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, N, seed=3 * M + K + N)
     check_tolerance(Y, Y_ref, What, X, f"decode-tc {t} M={M} K={K} N={N}")
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 @pytest.mark.parametrize("N", [4, 16, 40])
 def test_decode_tc_one_hot_returns_operand_weights(gq_lib, oracle_mod, cuda_dev, t, N):
     """X = e_k returns column k of the weights exactly as the MMA saw them. Q4_0 with up to
     16 tokens multiplies the exact codes c - 8 and applies the fp16 scale in fp32, so it
-    returns What itself; the other forms dequantize to bf16 and return bf16(What). This
-    pins the operand layout, the per-block accumulators and the scale of each block."""
+    returns What itself; the other forms (Q4_K: What as gq_dequantize writes it) dequantize
+    to bf16 and return bf16(What). This pins the operand layout, the per-block accumulators
+    and the scale of each block."""
     M, K = 300, 1024
     ks = [(37 * n) % K for n in range(N)]
     X = np.zeros((N, K), np.float32)
@@ -483,12 +484,14 @@ def test_decode_tc_one_hot_returns_operand_weights(gq_lib, oracle_mod, cuda_dev,
         assert np.array_equal(Y[n], expect[:, k]), (n, k)
 
 
-@pytest.mark.parametrize("t", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 def test_decode_tc_batched_mixed_shapes(gq_lib, oracle_mod, cuda_dev, t):
     """One grouped tensor-core launch over problems of different M and K, with a
     CUDA-core-only shape (K % 256 != 0) mixed in."""
     shapes = [(256, 2048), (2048, 2048), (7, 256), (300, 5632), (1, 1024), (64, 11008),
               (33, 96)]
+    if t == "q4_k":   # whole super-blocks only
+        shapes = [s for s in shapes if s[1] % 256 == 0]
     N = 16
     items, refs = [], []
     for i, (M, K) in enumerate(shapes):

@@ -11,7 +11,11 @@ Bars:
   - mul_mat on arbitrary super-block bytes: the same plus the fp32 rounding of the
     format's two partial sums, (K / 256 + 32) 2^-23 sum_k (|D_j q_k| + |M_j|) |x_k|
     (where d sc q and dmin m cancel, What can be far smaller than either term);
-  - one-hot X returns What exactly.
+  - one-hot X returns What exactly on the CUDA-core decode kernels (and bf16(What) on the
+    tensor-core decode and the prefill GEMM, which tests/test_gpu_parity.py covers for all
+    three types).
+Token counts route as for the other types: N <= 2 (and shapes the tensor-core paths do
+not take) on the CUDA-core kernels, 3..64 on the tensor-core decode, >= 65 on the GEMM.
 """
 import numpy as np
 import pytest
@@ -108,10 +112,9 @@ def test_dequantize_bit_exact_on_arbitrary_bytes(gq_lib, oracle_mod, cuda_dev):
 # ------------------------------------------------------------------------------------
 # mul_mat
 # ------------------------------------------------------------------------------------
-# Streaming kernel at every token count (passes of up to 4 tokens: N = 5 is 4 + 1, N = 70
-# is 17 passes of 4 and one of 2); M leaves ragged 4-row tiles; K = 11008 is 43 super-
-# blocks (a partial last column group); K = 256 one super-block. Small M splits columns
-# between warps.
+# N <= 2: the streaming kernel (M leaves ragged 4-row tiles; K = 11008 is 43 super-blocks,
+# a partial last column group; K = 256 one super-block; small M splits columns between
+# warps). N = 3..64: the tensor-core decode; N = 70: the prefill GEMM.
 STREAM = [(1, 256, 1), (7, 2048, 1), (300, 2048, 1), (1000, 2048, 2), (129, 5632, 3),
           (64, 11008, 4), (33, 4096, 5), (257, 1024, 9), (2048, 2048, 1), (200, 11008, 1),
           (65, 4096, 2), (96, 2048, 16), (50, 2048, 70)]
@@ -143,7 +146,7 @@ def test_mul_mat_matches_oracle(gq_lib, oracle_mod, cuda_dev, M, K, N):
            f"M={M} K={K} N={N}")
 
 
-@pytest.mark.parametrize("N", [1, 3])
+@pytest.mark.parametrize("N", [1, 2])
 def test_mul_mat_misaligned_x_takes_the_generic_kernel(gq_lib, oracle_mod, cuda_dev, N):
     M, K = 70, 2048
     q, X, Y = _run(gq_lib, oracle_mod, cuda_dev, M, K, N, seed=5, offset=1)
@@ -151,11 +154,10 @@ def test_mul_mat_misaligned_x_takes_the_generic_kernel(gq_lib, oracle_mod, cuda_
            f"misaligned N={N}")
 
 
-@pytest.mark.parametrize("N,offset", [(2, 0), (4, 0), (2, 1)])
+@pytest.mark.parametrize("N,offset", [(2, 0), (2, 1)])
 def test_mul_mat_one_hot_is_exact(gq_lib, oracle_mod, cuda_dev, N, offset):
-    """X = e_k returns column k of What bit for bit: the streaming kernel at 2 and 4 tokens
-    per pass (its one-token and several-token forms are both reached: 4 tokens run as one
-    pass, the 2-token groups of the one-hot list too), the generic kernel (offset X)."""
+    """X = e_k returns column k of What bit for bit on the CUDA-core kernels: the streaming
+    kernel with two tokens and with one, the generic kernel (offset X)."""
     M, K = 77, 2048
     q = oracle_mod.quantize(T, workloads.weights(M, K, seed=6).numpy())
     What = oracle_mod.dequantize(T, q, M, K)
@@ -244,6 +246,27 @@ def test_tinyllama_decode_step_q4_k_full_size(gq_lib, oracle_mod, cuda_dev):
     from test_gpu_parity import _sampled_step_check
     _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 2, T, 1, workloads.tinyllama_decode_set(),
                         rows_per_mat=4)
+
+
+def test_tinyllama_prefill_q4_k_full_size(gq_lib, oracle_mod, cuda_dev):
+    """gate / down / lm_head at N = 512 tokens in Q4_K on the tensor-core GEMM."""
+    from test_gpu_parity import _sampled_step_check
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 4, T, 512, workloads.tinyllama_prefill_set(),
+                        rows_per_mat=3)
+
+
+@pytest.mark.parametrize("M,K,N", [(200, 2048, 70), (64, 1024, 300), (1000, 2304, 512)])
+def test_gemm_arbitrary_superblocks(gq_lib, oracle_mod, cuda_dev, M, K, N):
+    """Hand-made super-blocks through the prefill GEMM (in its split-K and plain forms).
+    The GEMM forms What exactly as gq_dequantize does and rounds it to bf16, so the
+    plain tolerance applies."""
+    q = workloads.q4k_superblocks(M, K, seed=M + K + N)
+    X = workloads.activations(N, K, seed=N + 3).numpy()
+    _, _, Y = _run(gq_lib, oracle_mod, cuda_dev, M, K, N, 0, q=q, X=X)
+    _check(Y, oracle_mod.mul_mat(T, q, M, K, X), _tol(X, oracle_mod.dequantize(T, q, M, K)),
+           f"gemm arbitrary M={M} K={K} N={N}")
+    zero_rows = [m for m in range(M) if m % 8 == 3]
+    assert not Y[:, zero_rows].any()
 
 
 @pytest.mark.parametrize("M,K,N", [(300, 2048, 1), (64, 5632, 3), (40, 2048, 70)])

@@ -30,12 +30,12 @@ def _check_close(Y, Y_ref, What, X, where):
 
 # N = 300 / 512: prefill GEMM (workspace in the fixed array); N = 3 and 16: tensor-core
 # decode (X tiles, partial sums and counters in the fixed array); N = 2: CUDA-core decode.
-# Q4_K runs on the CUDA-core decode kernels at every N (no workspace at all).
+# Q4_K takes the same paths: N = 1 CUDA-core, 5 and 40 tensor-core decode, 300 prefill.
 @pytest.mark.parametrize("t,M,K,N", [(t, *s) for t in ("q4_0", "q8_0") for s in
                                      [(1000, 2048, 300), (256, 5632, 512), (300, 2048, 3),
                                       (129, 5632, 16), (77, 2048, 2)]] +
                          [("q4_k", 300, 2048, 1), ("q4_k", 129, 5632, 5),
-                          ("q4_k", 77, 2048, 70)])
+                          ("q4_k", 77, 2048, 40), ("q4_k", 300, 2048, 300)])
 def test_noalloc_matches_oracle_on_two_calls(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
     q = oracle_mod.quantize(t, workloads.weights(M, K, seed=71).numpy())
     What = oracle_mod.dequantize(t, q, M, K)
