@@ -29,7 +29,8 @@ TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "q4_k": Q4_K, Q4_0: Q4_0, Q8_0: Q8_0, Q4_K:
 MAX_BATCH = 256
 
 STATUS = {0: "GQ_OK", -1: "GQ_ERR_NULL", -2: "GQ_ERR_SHAPE", -3: "GQ_ERR_TYPE",
-          -4: "GQ_ERR_ALIGN", -5: "GQ_ERR_CUDA", -6: "GQ_ERR_TIMEOUT"}
+          -4: "GQ_ERR_ALIGN", -5: "GQ_ERR_CUDA", -6: "GQ_ERR_TIMEOUT", -7: "GQ_ERR_FORMAT",
+          -8: "GQ_ERR_IO"}
 
 # Every symbol declared in include/gq.h.
 EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0",
@@ -38,13 +39,26 @@ EXPORTS = ("gq_abi_version", "gq_block_bytes", "gq_row_bytes", "gq_quantize_q4_0
            "gq_mul_mat_batched_workspace_size", "gq_mul_mat_batched_ws", "gq_mul_mat_q8x",
            "gq_mul_mat_q8x_batched", "gq_mul_mat_rmsnorm", "gq_mul_mat_swiglu",
            "gq_get_last_error",
-           "gq_selftest_wait_timeout", "gq_status_string")
+           "gq_selftest_wait_timeout", "gq_status_string",
+           # include/gq_gguf.h
+           "gq_gguf_open", "gq_gguf_close", "gq_gguf_version", "gq_gguf_tensor_count",
+           "gq_gguf_kv_count", "gq_gguf_alignment", "gq_gguf_tensor_info",
+           "gq_gguf_find_tensor", "gq_gguf_tensor_data", "gq_gguf_tensor_matrix",
+           "gq_gguf_upload", "gq_gguf_find_key", "gq_gguf_kv_key", "gq_gguf_kv_type",
+           "gq_gguf_kv_int", "gq_gguf_kv_float", "gq_gguf_kv_string", "gq_gguf_kv_array")
 
 
 class Problem(ctypes.Structure):
     """gq_mul_mat_problem."""
     _fields_ = [("W_blocks", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
                 ("M", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class GgufTensor(ctypes.Structure):
+    """gq_gguf_tensor."""
+    _fields_ = [("name", ctypes.c_char_p), ("n_dims", ctypes.c_uint32),
+                ("type", ctypes.c_uint32), ("ne", ctypes.c_int64 * 4),
+                ("offset", ctypes.c_uint64), ("nbytes", ctypes.c_uint64)]
 
 
 def load(path: str = LIB_PATH):
@@ -88,6 +102,31 @@ def load(path: str = LIB_PATH):
     L.gq_selftest_wait_timeout.argtypes = [i64, vp]
     L.gq_selftest_wait_timeout.restype = ctypes.c_int
     L.gq_status_string.argtypes, L.gq_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+    u32, u64, c = ctypes.c_uint32, ctypes.c_uint64, ctypes.c_char_p
+    L.gq_gguf_open.argtypes, L.gq_gguf_open.restype = [c, ctypes.POINTER(vp)], ctypes.c_int
+    L.gq_gguf_close.argtypes, L.gq_gguf_close.restype = [vp], None
+    L.gq_gguf_version.argtypes, L.gq_gguf_version.restype = [vp], u32
+    L.gq_gguf_tensor_count.argtypes, L.gq_gguf_tensor_count.restype = [vp], i64
+    L.gq_gguf_kv_count.argtypes, L.gq_gguf_kv_count.restype = [vp], i64
+    L.gq_gguf_alignment.argtypes, L.gq_gguf_alignment.restype = [vp], u64
+    L.gq_gguf_tensor_info.argtypes = [vp, i64, ctypes.POINTER(GgufTensor)]
+    L.gq_gguf_tensor_info.restype = ctypes.c_int
+    L.gq_gguf_find_tensor.argtypes, L.gq_gguf_find_tensor.restype = [vp, c], i64
+    L.gq_gguf_tensor_data.argtypes, L.gq_gguf_tensor_data.restype = [vp, i64], vp
+    L.gq_gguf_tensor_matrix.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_int),
+                                        ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.gq_gguf_tensor_matrix.restype = ctypes.c_int
+    L.gq_gguf_upload.argtypes, L.gq_gguf_upload.restype = [vp, i64, vp, ctypes.c_size_t, vp], ctypes.c_int
+    L.gq_gguf_find_key.argtypes, L.gq_gguf_find_key.restype = [vp, c], i64
+    L.gq_gguf_kv_key.argtypes, L.gq_gguf_kv_key.restype = [vp, i64], c
+    L.gq_gguf_kv_type.argtypes, L.gq_gguf_kv_type.restype = [vp, i64], i32
+    L.gq_gguf_kv_int.argtypes = [vp, i64, ctypes.POINTER(i64)]
+    L.gq_gguf_kv_float.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_double)]
+    L.gq_gguf_kv_string.argtypes = [vp, i64, ctypes.POINTER(vp), ctypes.POINTER(u64)]
+    L.gq_gguf_kv_array.argtypes = [vp, i64, ctypes.POINTER(u32), ctypes.POINTER(u64),
+                                   ctypes.POINTER(vp)]
+    for fn in (L.gq_gguf_kv_int, L.gq_gguf_kv_float, L.gq_gguf_kv_string, L.gq_gguf_kv_array):
+        fn.restype = ctypes.c_int
     lib = L
     return L
 

@@ -480,6 +480,8 @@ const char* gq_status_string(gq_status s) {
         case GQ_ERR_ALIGN: return "misaligned pointer (blocks need 16 bytes, fp32 arrays 4)";
         case GQ_ERR_CUDA: return "CUDA runtime error";
         case GQ_ERR_TIMEOUT: return "a device-side wait ran out of time";
+        case GQ_ERR_FORMAT: return "not a GGUF file, or a malformed or truncated one";
+        case GQ_ERR_IO: return "the file could not be opened or mapped";
     }
     return "unknown status";
 }

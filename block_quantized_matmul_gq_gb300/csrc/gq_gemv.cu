@@ -843,9 +843,9 @@ __device__ __forceinline__ int q4k_sub_dot(const uint4 (&x)[4], const uint32_t (
 // token's quarter record: out[r][t] += the quarter's partial (scaled by 2^e), with
 //     partial = d (sc_2g S_2g + sc_2g+1 S_2g+1) - dmin (m_2g X_2g + m_2g+1 X_2g+1),
 // S_j = sum q x16 and X_j = sum x16 over sub-block j (both sums exact in int32: at most
-// 63 * 2 * 15 * 32767 * 32 < 2^31 and 63 * 2 * 32767 * 32). At one token the record is
-// read once for all rows; at more tokens one sub-block at a time, and each row's codes
-// are read once per sub-block.
+// 63 * 2 * 15 * 32767 * 32 < 2^31 and 63 * 2 * 32767 * 32). Up to two tokens, the records
+// are read once for all rows and each row's bytes once; at more tokens one sub-block at a
+// time, and each row's codes once per sub-block.
 template <int kNT>
 __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs, int rows,
                                                 const uint8_t* xp, int rec_stride,
@@ -855,9 +855,10 @@ __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs
     for (int r = 0; r < kTileRows; ++r)
 #pragma unroll
         for (int t = 0; t < kNT; ++t) acc[r][t] = 0.0f;
-    if constexpr (kNT == 1) {
-        PairX X;
-        load_pair_x(xp, X);
+    if constexpr (kNT <= 2) {
+        PairX X[kNT];
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) load_pair_x(xp + t * rec_stride, X[t]);
 #pragma unroll
         for (int r = 0; r < kTileRows; ++r) {
             if (r >= rows) break;   // uniform across the warp
@@ -874,17 +875,24 @@ __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs
             }
             uint32_t sc, m;
             q4k_scales(hd, g, sc, m);
-            const int S0 = q4k_sub_dot(X.x[0], lo);
-            const int S1 = q4k_sub_dot(X.x[1], hi);
-            const int T = static_cast<int>(sc & 0xFFu) * S0 + static_cast<int>(sc >> 8) * S1;
-            const int U = static_cast<int>(m & 0xFFu) * X.bias[0] +
-                          static_cast<int>(m >> 8) * X.bias[1];
             const float d = half_bits_to_float(hd.x & 0xFFFFu);
             const float dmin = half_bits_to_float(hd.x >> 16);
-            acc[r][0] = fmaf(-dmin, static_cast<float>(U), fmaf(d, static_cast<float>(T), acc[r][0]));
+#pragma unroll
+            for (int t = 0; t < kNT; ++t) {
+                const int S0 = q4k_sub_dot(X[t].x[0], lo);
+                const int S1 = q4k_sub_dot(X[t].x[1], hi);
+                const int T = static_cast<int>(sc & 0xFFu) * S0 + static_cast<int>(sc >> 8) * S1;
+                const int U = static_cast<int>(m & 0xFFu) * X[t].bias[0] +
+                              static_cast<int>(m >> 8) * X[t].bias[1];
+                acc[r][t] = fmaf(-dmin, static_cast<float>(U),
+                                 fmaf(d, static_cast<float>(T), acc[r][t]));
+            }
         }
 #pragma unroll
-        for (int r = 0; r < kTileRows; ++r) out[r][0] = fmaf(acc[r][0] * X.sc.x, X.sc.y, out[r][0]);
+        for (int t = 0; t < kNT; ++t)
+#pragma unroll
+            for (int r = 0; r < kTileRows; ++r)
+                out[r][t] = fmaf(acc[r][t] * X[t].sc.x, X[t].sc.y, out[r][t]);
     } else {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

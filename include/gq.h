@@ -1,6 +1,7 @@
 /*
- * gq.h -- C ABI of libgq: block-quantized (Q4_0 / Q8_0) weights times fp32 activations on
- * one NVIDIA GB300 GPU (sm_103a).
+ * gq.h -- C ABI of libgq: block-quantized (Q4_0 / Q8_0 / Q4_K) weights times fp32
+ * activations on one NVIDIA GB300 GPU (sm_103a). Reading such weights out of GGUF files:
+ * gq_gguf.h.
  *
  * The operation is the `mul_mat` that "No Python! Building an AI Inference Engine
  * Exclusively in C++" (section 6) says takes over 90% of inference compute, with the
@@ -20,6 +21,8 @@
  *             element j in its low nibble and element j+16 in its high nibble; a code c
  *             means What = (c - 8) * d.
  *       Q8_0, 34 bytes: fp16 scale d, then 32 signed bytes c; What = c * d.
+ *       Q4_K, 144-byte super-blocks of 256 weights, K/256 per row (layout at
+ *             gq_quantize_q4_k).
  *   - Pointers. Every array pointer is a DEVICE pointer owned by the caller; the library
  *     keeps none of them after the call returns. W_blocks must be 16-byte aligned, fp32
  *     arrays 4-byte aligned (16-byte alignment of X is used when present). A pointer may
@@ -42,8 +45,8 @@
  *     GQ_ERR_CUDA. Kernels never trap: a device-side wait that runs past its limit sets a
  *     per-device status word that gq_get_last_error() returns.
  *   - Empty inputs. M == 0 or N == 0 is a valid no-op; K == 0 writes Y = 0 (empty sum).
- *   - Range. Values are finite; |w| / 7 and |w| / 127 must fit fp16 (|d| <= 65504).
- *     Non-finite inputs give unspecified results.
+ *   - Range. Values are finite; |w| / 7 and |w| / 127 (Q4_K: a sub-block's range / 945)
+ *     must fit fp16 (|d| <= 65504). Non-finite inputs give unspecified results.
  */
 #ifndef GQ_H_
 #define GQ_H_
@@ -73,7 +76,9 @@ typedef enum gq_status {
     GQ_ERR_TYPE = -3,     /* unknown gq_type, or one the entry point does not take */
     GQ_ERR_ALIGN = -4,    /* W_blocks not 16-byte aligned, or an fp32 array not 4-byte */
     GQ_ERR_CUDA = -5,     /* a CUDA runtime call failed (launch, attribute, no device) */
-    GQ_ERR_TIMEOUT = -6   /* a device-side wait ran out (reported by gq_get_last_error) */
+    GQ_ERR_TIMEOUT = -6,  /* a device-side wait ran out (reported by gq_get_last_error) */
+    GQ_ERR_FORMAT = -7,   /* gq_gguf.h: not a GGUF file, or a malformed or truncated one */
+    GQ_ERR_IO = -8        /* gq_gguf.h: the file could not be opened or mapped */
 } gq_status;
 
 /* Version of this ABI (GQ_ABI_VERSION of the header the library was built with). */

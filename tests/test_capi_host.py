@@ -7,13 +7,15 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "gq.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("gq.h", "gq_gguf.h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
@@ -42,7 +44,7 @@ def test_sizes(gq_lib):
 
 
 def test_status_strings(gq_lib):
-    for code in range(-6, 1):
+    for code in range(-8, 1):
         assert gq_lib.lib.gq_status_string(code)
     assert b"unknown" in gq_lib.lib.gq_status_string(-99)
 
