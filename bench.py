@@ -831,29 +831,48 @@ def run_gb300(args, shapes):
     value = bytes_all / t_max / 1e9
     per_gpu = nb["total"] * args.steps / elapsed / 1e9
 
-    # End to end through the public API, every step: pinned host X -> device, the batched
-    # call, device Y -> pinned host, and a host synchronize before the next step. The
-    # three operations of a step are recorded once into a CUDA graph (as a serving loop
-    # would), so a step costs one graph launch plus the synchronize.
+    # End to end through the public API with HOST buffers, every step: the step's X in
+    # pinned host memory, the batched call given the host X and a pinned host Y (the
+    # kernels read X and write Y across NVLink-C2C, include/gq.h), and a host synchronize
+    # before the host reads Y and the next step starts. The call is recorded once into a
+    # CUDA graph (as a serving loop would), so a step costs one graph launch plus the
+    # synchronize. Beside it, the same with explicit copies: pinned X -> device buffer,
+    # the call on device buffers, device Y -> pinned host, in one graph.
     X_host = X_flat.cpu().pin_memory()
-    Y_host = torch.empty(ys_total, dtype=torch.float32).pin_memory()
+    Y_host = torch.full((ys_total,), float("nan"), dtype=torch.float32).pin_memory()
+    xs_h, ys_h, xo, yo = [], [], 0, 0
+    for s in shapes:
+        xs_h.append(X_host[xo:xo + N * s.K].view(N, s.K))
+        ys_h.append(Y_host[yo:yo + N * s.M].view(N, s.M))
+        xo += N * s.K
+        yo += N * s.M
+    arrays_h = ws.problem_arrays(xs_h, ys_h)
     e2e_steps = max(10, min(args.steps, 2000))
-    e2e_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(e2e_graph):
+
+    def e2e_time(record):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            record()
+        for _ in range(5):
+            g.replay()
+            torch.cuda.synchronize(dev)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            g.replay()
+            torch.cuda.synchronize(dev)
+        t, b = aggregate(time.perf_counter() - t0, nb["total"] * e2e_steps, world, dev)
+        return t, b / t / 1e9
+
+    def explicit_copies():
         X_flat.copy_(X_host, non_blocking=True)
         ws.run(arrays, N)
         Y_host.copy_(Y_flat, non_blocking=True)
-    for _ in range(5):
-        e2e_graph.replay()
-        torch.cuda.synchronize(dev)
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_graph.replay()
-        torch.cuda.synchronize(dev)
-    e2e_t = time.perf_counter() - t0
-    e2e_t, e2e_bytes = aggregate(e2e_t, nb["total"] * e2e_steps, world, dev)
-    e2e_value = e2e_bytes / e2e_t / 1e9
+
+    e2e_t, e2e_value = e2e_time(lambda: ws.run(arrays_h, N))
+    if not torch.equal(Y_host.view(torch.int32), Y_flat.cpu().view(torch.int32)):
+        raise RuntimeError("host-buffer step differs from the device-buffer step")
+    e2e_copy_t, e2e_copy_value = e2e_time(explicit_copies)
 
     # Where an end-to-end step's time goes: each part alone, recorded and replayed the same
     # way with a host synchronize per step.
@@ -871,10 +890,14 @@ def run_gb300(args, shapes):
         return round((time.perf_counter() - t0) / 200 * 1e6, 2)
 
     e2e_parts = {
-        "h2d_copy_and_sync_us": per_step_us(lambda: X_flat.copy_(X_host, non_blocking=True)),
-        "kernel_and_sync_us": per_step_us(lambda: ws.run(arrays, N)),
-        "d2h_copy_and_sync_us": per_step_us(lambda: Y_host.copy_(Y_flat, non_blocking=True)),
         "e2e_step_us": round(e2e_t / e2e_steps * 1e6, 2),
+        "kernel_and_sync_us": per_step_us(lambda: ws.run(arrays, N)),
+        "explicit_copies": {
+            "value": round(e2e_copy_value, 2), "unit": UNIT,
+            "step_us": round(e2e_copy_t / e2e_steps * 1e6, 2),
+            "h2d_copy_and_sync_us": per_step_us(lambda: X_flat.copy_(X_host, non_blocking=True)),
+            "d2h_copy_and_sync_us": per_step_us(lambda: Y_host.copy_(Y_flat, non_blocking=True)),
+        },
     }
 
     peak, peak_src = measured_peaks()
@@ -903,6 +926,9 @@ def run_gb300(args, shapes):
                                    "launch / (CUDA-event step time)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                 "h2d_bytes_per_step": nb["x"], "d2h_bytes_per_step": nb["y"],
+                "how": "X and Y in pinned host memory passed to gq_mul_mat_batched (read "
+                       "and written by the kernels over NVLink-C2C), one graph launch and "
+                       "a host synchronize per step",
                 "parts": e2e_parts},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

@@ -3,7 +3,8 @@
 Every call passes device pointers and sizes straight to the C ABI on torch's current
 CUDA stream; all arithmetic runs in the library's sm_103a kernels. There is no CPU path:
 importing this module fails loudly if libgq.so has not been built, and the calls refuse
-CPU tensors.
+CPU tensors, except pinned (page-locked) host tensors for activations and outputs, which
+the kernels read and write in place (include/gq.h).
 """
 from __future__ import annotations
 
@@ -168,6 +169,26 @@ def _dev(t: torch.Tensor, dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _act(t: torch.Tensor, dtype, name: str) -> int:
+    """X, Y, gamma: a CUDA tensor, or a pinned (page-locked) host tensor, which the device
+    addresses directly (include/gq.h: the kernels read and write it over the host link)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory "
+                         "(libgq has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _out_like(X: torch.Tensor, shape) -> torch.Tensor:
+    """Y where X lives: on X's device, or pinned host memory for a pinned host X."""
+    if X.is_cuda:
+        return torch.empty(shape, dtype=torch.float32, device=X.device)
+    return torch.empty(shape, dtype=torch.float32, pin_memory=True)
+
+
 def block_bytes(t) -> int:
     return int(lib.gq_block_bytes(_type(t)))
 
@@ -207,9 +228,9 @@ def mul_mat(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
     if X.shape[1] != K:
         raise ValueError("X must be (N, K)")
     if out is None:
-        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+        out = _out_like(X, (N, M))
     _check(lib.gq_mul_mat(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
-                          _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
+                          _act(X, torch.float32, "X"), N, _act(out, torch.float32, "Y"),
                           _stream(stream)), "gq_mul_mat")
     return out
 
@@ -226,11 +247,11 @@ def mul_mat_ws(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
         X = X.view(1, -1)
     N = X.shape[0]
     if out is None:
-        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+        out = _out_like(X, (N, M))
     wp = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
     wn = workspace.numel() if workspace is not None else 0
     _check(lib.gq_mul_mat_ws(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
-                             _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
+                             _act(X, torch.float32, "X"), N, _act(out, torch.float32, "Y"),
                              wp, wn, _stream(stream)), "gq_mul_mat_ws")
     return out
 
@@ -243,22 +264,23 @@ def mul_mat_noalloc(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
         X = X.view(1, -1)
     N = X.shape[0]
     if out is None:
-        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+        out = _out_like(X, (N, M))
     _check(lib.gq_mul_mat_noalloc(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
-                                  _dev(X, torch.float32, "X"), N,
-                                  _dev(out, torch.float32, "Y"), _stream(stream)),
+                                  _act(X, torch.float32, "X"), N,
+                                  _act(out, torch.float32, "Y"), _stream(stream)),
            "gq_mul_mat_noalloc")
     return out
 
 
 def make_problems(items) -> ctypes.Array:
-    """items: iterable of (blocks, M, K, X, Y) CUDA tensors -> a gq_mul_mat_problem array
-    that can be handed to mul_mat_batched repeatedly (e.g. while capturing a graph)."""
+    """items: iterable of (blocks, M, K, X, Y) tensors (blocks on the device; X and Y on the
+    device or in pinned host memory) -> a gq_mul_mat_problem array that can be handed to
+    mul_mat_batched repeatedly (e.g. while capturing a graph)."""
     items = list(items)
     arr = (Problem * max(1, len(items)))()
     for i, (blocks, M, K, X, Y) in enumerate(items):
-        arr[i] = Problem(_dev(blocks, torch.uint8, "W_blocks"), _dev(X, torch.float32, "X"),
-                         _dev(Y, torch.float32, "Y"), M, K)
+        arr[i] = Problem(_dev(blocks, torch.uint8, "W_blocks"), _act(X, torch.float32, "X"),
+                         _act(Y, torch.float32, "Y"), M, K)
     arr._count = len(items)
     # The array holds raw device pointers: keep the tensors alive as long as it lives.
     arr._tensors = [(blocks, X, Y) for blocks, _, _, X, Y in items]
@@ -304,9 +326,9 @@ def mul_mat_q8x(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
     if X.shape[1] != K:
         raise ValueError("X must be (N, K)")
     if out is None:
-        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+        out = _out_like(X, (N, M))
     _check(lib.gq_mul_mat_q8x(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
-                              _dev(X, torch.float32, "X"), N, _dev(out, torch.float32, "Y"),
+                              _act(X, torch.float32, "X"), N, _act(out, torch.float32, "Y"),
                               _stream(stream)), "gq_mul_mat_q8x")
     return out
 
@@ -321,10 +343,10 @@ def mul_mat_rmsnorm(blocks: torch.Tensor, t, M: int, K: int, X: torch.Tensor,
     if X.shape[1] != K or gamma.numel() != K:
         raise ValueError("X must be (N, K) and gamma (K,)")
     if out is None:
-        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+        out = _out_like(X, (N, M))
     _check(lib.gq_mul_mat_rmsnorm(_dev(blocks, torch.uint8, "W_blocks"), _type(t), M, K,
-                                  _dev(X, torch.float32, "X"), _dev(gamma, torch.float32, "gamma"),
-                                  float(eps), N, _dev(out, torch.float32, "Y"), _stream(stream)),
+                                  _act(X, torch.float32, "X"), _act(gamma, torch.float32, "gamma"),
+                                  float(eps), N, _act(out, torch.float32, "Y"), _stream(stream)),
            "gq_mul_mat_rmsnorm")
     return out
 
@@ -338,10 +360,10 @@ def mul_mat_swiglu(gate: torch.Tensor, up: torch.Tensor, t, M: int, K: int, X: t
     if X.shape[1] != K:
         raise ValueError("X must be (N, K)")
     if out is None:
-        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+        out = _out_like(X, (N, M))
     _check(lib.gq_mul_mat_swiglu(_dev(gate, torch.uint8, "W_gate"), _dev(up, torch.uint8, "W_up"),
-                                 _type(t), M, K, _dev(X, torch.float32, "X"), N,
-                                 _dev(out, torch.float32, "H"), _stream(stream)),
+                                 _type(t), M, K, _act(X, torch.float32, "X"), N,
+                                 _act(out, torch.float32, "H"), _stream(stream)),
            "gq_mul_mat_swiglu")
     return out
 

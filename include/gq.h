@@ -23,11 +23,18 @@
  *       Q8_0, 34 bytes: fp16 scale d, then 32 signed bytes c; What = c * d.
  *       Q4_K, 144-byte super-blocks of 256 weights, K/256 per row (layout at
  *             gq_quantize_q4_k).
- *   - Pointers. Every array pointer is a DEVICE pointer owned by the caller; the library
- *     keeps none of them after the call returns. W_blocks must be 16-byte aligned, fp32
- *     arrays 4-byte aligned (16-byte alignment of X is used when present). A pointer may
- *     be NULL only when its array is empty. The CUDA-core decode path (N <= 2) allocates
- *     nothing; the tensor-core paths need a workspace (see gq_mul_mat_ws).
+ *   - Pointers. Every array pointer is owned by the caller; the library keeps none of them
+ *     after the call returns. W_blocks and workspaces are DEVICE pointers. X, Y (and the
+ *     fused forms' gamma and H) are device pointers or pointers to page-locked host memory
+ *     that the device can address (cudaHostAlloc, or cudaHostRegister with
+ *     cudaHostRegisterMapped; with unified addressing the host address is valid on the
+ *     device). Host buffers are read and written by the kernels themselves over the host
+ *     link (NVLink-C2C on GB300), with ordinary loads and stores and no separate copy; the
+ *     results are the same bits as with device buffers. W_blocks must be 16-byte
+ *     aligned, fp32 arrays 4-byte aligned (16-byte alignment of X is used when present).
+ *     A pointer may be NULL only when its array is empty. The CUDA-core decode path
+ *     (N <= 2) allocates nothing; the tensor-core paths need a workspace (see
+ *     gq_mul_mat_ws).
  *   - Streams. `stream` is a cudaStream_t (NULL = the legacy default stream) passed as
  *     void* so that this header needs no CUDA include. Calls only enqueue work: they do
  *     not synchronize, and results are ready when the stream reaches them.
