@@ -1,10 +1,9 @@
 // gq_noalloc.cu -- gq_mul_mat_noalloc: mul_mat that never allocates device memory.
 //
 // Some callers cannot call cudaMalloc (or anything that does) at the point where they
-// multiply: code being recorded into a CUDA graph (allocation is not a stream operation
-// and breaks or is refused during capture), engines that reserve all device memory up
-// front in their own arena and forbid later allocation, and real-time loops with a fixed
-// memory budget where an allocation could stall or fail mid-run. gq_mul_mat may allocate
+// multiply: engines that reserve all device memory up front in their own arena and forbid
+// later allocation, and real-time loops with a fixed memory budget where an allocation
+// could stall or fail mid-run. gq_mul_mat may allocate
 // (its tensor-core path grows a library-owned workspace); this entry point instead uses a
 // fixed array compiled into the library as that workspace.
 //

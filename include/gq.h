@@ -208,8 +208,8 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
                         size_t workspace_bytes, void* stream);
 
 /*
- * gq_mul_mat that never allocates device memory, for callers that cannot: code being
- * recorded into a CUDA graph, engines that reserve all device memory up front in their own
+ * gq_mul_mat that never allocates device memory, for callers that cannot allocate at the
+ * point where they multiply: engines that reserve all device memory up front in their own
  * arena, and real-time loops that must not stall or fail on an allocation mid-run. (The
  * pages have no counterpart: their engine allocates once from an arena; this entry point
  * exists for users of this library.)
@@ -222,10 +222,9 @@ gq_status gq_mul_mat_ws(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  *     exceeds 64 MiB (N * K > 32 Mi) return GQ_ERR_SHAPE;
  *   - the tensor-core decode (3 <= N <= 64) needs at most 64 * K * 2 bytes + 16 MiB + 4 KiB
  *     there; a larger K (beyond ~390k) runs on the CUDA-core decode kernels instead;
- *   - the first call on a device looks up that array's device address (set-up); make that
- *     first call before any stream capture on the device. The address is kept for the
- *     life of the process, so libgq must not be used again on a device the process has
- *     reset with cudaDeviceReset;
+ *   - the first call on a device looks up that array's device address (a one-time host-side
+ *     set-up). The address is kept for the life of the process, so libgq must not be used
+ *     again on a device the process has reset with cudaDeviceReset;
  *   - every call shares the array (each call rewrites what it reads there, and zeroes its
  *     counters, before use), so calls that overlap on the GPU -- on different streams, or
  *     from different threads -- race: serialize them.

@@ -1,6 +1,6 @@
 """gq_mul_mat_noalloc -- the entry point for callers that cannot allocate device memory
-(code recorded into a CUDA graph, engines whose arena owns all device memory, real-time
-loops that must not stall on an allocation) -- must give what gq_mul_mat gives. Collected
+(engines whose arena owns all device memory, real-time loops that must not stall on an
+allocation) -- must give what gq_mul_mat gives. Collected
 last on purpose: a failure here comes after every other test has run.
 
 Calls go through the C ABI (the ctypes binding). Each result is checked against the CPU
