@@ -13,7 +13,8 @@
 //               one 256-k "super-step" = 8 blocks per row per copy) and bf16 X tiles
 //               (64 k x kBN tokens, 128-byte swizzle) into rings of shared-memory stages.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=kBN, K=16),
-//               four per 64-k stage, and commits each stage back to the producers.
+//               four per 64-k stage, and commits each stage back to the producers. (The
+//               512-token kernel has a second issuing warp, warp 10: one per token half.)
 //   warps 2..9  dequantize: a thread owns one row and one of the two blocks of every 64-k
 //               stage; it turns the block into 32 bf16 values, each (c - 8) * d (or c * d)
 //               computed exactly in fp32 (packed f32x2 arithmetic) and rounded once to
@@ -396,12 +397,23 @@ struct WideLayout {
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr int kTmemCols = 512;
+    // Two MMA issuers, one per token half (warps 1 and kIssuer2Warp, on different SM
+    // sub-partitions), share every A stage and take alternate X units: the per-stage
+    // waits, issues and loop of one thread are split between two. Both have consumed
+    // stage ks - 2 when stage ks's A is ready, so an issuer waiting on unit 2 ks + h finds
+    // that unit slot's previous fill (2 ks + h - kUnits) consumed, and its parity test
+    // exact, when kUnits >= 4. With 3 units (Q8_0) an issuer could wait on a slot whose
+    // previous fill, the other issuer's, has not landed, and its parity test would see
+    // the phase two back: Q8_0 keeps one issuer.
+    static constexpr int kIssuers = kUnits >= 4 ? 2 : 1;
+    static constexpr int kIssuer2Warp = 2 + kDequantWarps;   // 10
+    static constexpr int kThreads = kIssuers == 2 ? 32 * (kIssuer2Warp + 1) : 64 + 32 * kDequantWarps;
     static_assert(kU % 1024 == 0 && kA % 1024 == 0 && kRaw % 1024 == 0, "1 KB aligned stages");
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
 };
 
 template <int kType>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(WideLayout<kType>::kThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, int M, int N, int K,
                  float* __restrict__ Y, unsigned* status) {
@@ -438,7 +450,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
             mbar_init(a_full(s), 32 * kDequantWarps);
-            mbar_init(a_empty(s), 1);
+            mbar_init(a_empty(s), L::kIssuers);   // every issuer's MMAs read the stage
         }
         for (int u = 0; u < SU; ++u) {
             mbar_init(u_full(u), 1);
@@ -448,7 +460,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(raw_full(r), 1);
             mbar_init(raw_empty(r), 32 * kDequantWarps);
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, L::kIssuers);   // one commit per MMA issuer
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -500,8 +512,12 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for (int j = max(0, raw_issued - R); j < raw_issued; ++j)
                 mbar_wait(raw_full(j % R), (j / R) & 1, kDrainNs);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 1 || (L::kIssuers == 2 && warp == L::kIssuer2Warp)) {
+        // ---------------- MMA issuers ----------------
+        // Issuer h0 issues the MMAs of token half h0 (accumulator columns [256 h0,
+        // 256 h0 + 256)) for every A stage; a single issuer takes both halves.
+        constexpr int I = L::kIssuers;
+        const int h0 = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kBM, L::kHalfN);
             bool ok = true;
@@ -511,7 +527,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     ok = false;
                     break;
                 }
-                for (int h = 0; h < 2; ++h) {
+                for (int h = h0; h < 2; h += I) {
                     const int ub = 2 * ks + h, u = ub % SU;
                     if (!mbar_wait(u_full(u), (ub / SU) & 1)) {
                         ok = false;
@@ -527,7 +543,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     }
                     umma_commit(u_empty(u));   // X unit u is free once these MMAs have read it
                 }
-                umma_commit(a_empty(sa));      // and A stage sa once both halves have
+                umma_commit(a_empty(sa));      // and A stage sa once every issuer's have
             }
             umma_commit(acc_full);             // accumulators complete (also after a timeout)
             if (!ok) report_status(status, kStatusTimeout);
@@ -727,7 +743,7 @@ cudaError_t launch_wide(CUtensorMap tw, CUtensorMap tx, const MatProblem& p, int
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(mt), static_cast<unsigned>((N + 511) / 512));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(WL::kThreads);
     cfg.dynamicSmemBytes = WL::kAlloc;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
