@@ -70,6 +70,23 @@ def step_bytes(shapes, N: int, block_bytes: int, block_weights: int = 32) -> dic
     return {"weights": w, "x": x, "y": y, "total": w + x + y}
 
 
+def replay_median_s(g, dev, replays: int) -> float:
+    """Median time of one replay of CUDA graph g over `replays` replays after warm-up
+    (seconds). The replays are queued back to back, each bracketed by its own pair of
+    CUDA events on the current stream, with one synchronize after the last, so that no
+    replay starts on an idle GPU."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(max(1, replays))]
+    for e0, e1 in evs:
+        e0.record()
+        g.replay()
+        e1.record()
+    torch.cuda.synchronize(dev)
+    times = sorted(e0.elapsed_time(e1) / 1e3 for e0, e1 in evs)
+    return times[len(times) // 2]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -263,7 +280,7 @@ def run_reference(args, shapes):
 PREFILL_SETS = [("tinyllama_prefill_n512", 4, 512), ("llama7b_prefill_n2048", 5, 2048)]
 
 
-def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None,
+def prefill_measure(dev, reps: int = 10, iters: int = 20, only=None,
                     types=("q4_0", "q8_0", "q4_k"), rotate: bool = True):
     """Each prefill matrix as gq_mul_mat_ws calls replayed from a CUDA graph. Weight copies
     (distinct seeds) are rotated so that every call reads its weights from HBM, not from L2
@@ -300,14 +317,8 @@ def prefill_measure(dev, reps: int = 10, iters: int = 5, only=None,
                         binding.mul_mat_ws(qs[r % copies], btype, sh.M, sh.K, X, ws, out=Y)
                 g.replay()
                 torch.cuda.synchronize(dev)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-                for _ in range(iters):
-                    g.replay()
-                e1.record()
-                torch.cuda.synchronize(dev)
-                sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+                rep_s = replay_median_s(g, dev, iters)
+                sec = rep_s / reps
                 flop = 2.0 * sh.M * N * sh.K
                 tf = flop / sec / 1e12
                 rows.append({"matrix": sh.name, "M": sh.M, "K": sh.K, "N": N,
@@ -340,7 +351,7 @@ L2_BYTES = 129 * 2 ** 20
 STEPS_PER_GRAPH = 10
 
 
-def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
+def decode_measure(dev, reps: int = 20, iters: int = 20) -> dict:
     """Each decode set as batched calls (one per step) replayed from a CUDA graph; weight
     sets smaller than 4x L2 are copied (distinct seeds) and rotated so every step reads
     its weights from HBM. GB/s counts weights + X + Y once per step."""
@@ -377,13 +388,8 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
                     ws.run(arrays, N, workspace=work)
             g.replay()
             torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(iters):
-                g.replay()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+            rep_s = replay_median_s(g, dev, iters)
+            sec = rep_s / reps
             gbs = nb["total"] / sec / 1e9
             rows.append({"N": N, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
                          "frac": round(gbs / peak, 4),
@@ -399,7 +405,73 @@ def decode_measure(dev, reps: int = 20, iters: int = 5) -> dict:
     return out
 
 
-def launch_floor(dev, reps: int = 20, iters: int = 5) -> dict:
+def per_matmul_measure(dev, iters: int = 20) -> dict:
+    """Each distinct TinyLLaMA matrix shape alone at N = 1 (gq_mul_mat, one call per
+    matrix), in Q4_0 and Q8_0: a graph of R calls, each on its own copy of the blocks so
+    that the R copies (>= 4 x L2 together) are read from HBM; the median of `iters`
+    replays, per call."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding, workloads
+    peak, _ = measured_peaks()
+    shapes = {"q_o_proj": (2048, 2048), "k_v_proj": (256, 2048), "gate_up_proj": (5632, 2048),
+              "down_proj": (2048, 5632), "lm_head": (32000, 2048)}
+    out = {"unit": "GB/s", "peak": peak, "N": 1}
+    for btype in ("q4_0", "q8_0"):
+        rows = {}
+        for name, (M, K) in shapes.items():
+            q = binding.quantize(workloads.weights(M, K, 9000 + M, device=dev), btype)
+            R = int(min(2048, max(4, -(-4 * L2_BYTES // q.numel()))))
+            copies = q.unsqueeze(0).expand(R, *q.shape).contiguous()   # R addresses
+            X = workloads.activations(1, K, 9100 + K, device=dev)
+            Y = torch.empty((1, M), device=dev)
+            for r in range(3):
+                binding.mul_mat(copies[r], btype, M, K, X, out=Y)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for r in range(R):
+                    binding.mul_mat(copies[r], btype, M, K, X, out=Y)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            sec = replay_median_s(g, dev, iters) / R
+            nbytes = q.numel() + 4 * (K + M)
+            gbs = nbytes / sec / 1e9
+            rows[name] = {"M": M, "K": K, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
+                          "frac": round(gbs / peak, 4), "copies_rotated": R}
+            del g, copies, q
+        out[btype] = rows
+    if binding.get_last_error() != 0:
+        raise RuntimeError("device status word set during the per-matmul sets")
+    return out
+
+
+def step_as_calls_measure(dev, ws, xs, ys, N: int, step_bytes_total: int, iters: int = 20,
+                          steps: int = 5) -> dict:
+    """The decode step as one gq_mul_mat call per matrix (155 launches) instead of one
+    batched launch, in a graph of `steps` steps; median of `iters` replays, per step."""
+    import torch
+    from block_quantized_matmul_gq_gb300 import binding
+    peak, _ = measured_peaks()
+
+    def step():
+        for m, x, y in zip(ws.mats, xs, ys):
+            binding.mul_mat(m.blocks, ws.btype, m.shape.M, m.shape.K, x, out=y)
+
+    step()
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(steps):
+            step()
+    g.replay()
+    torch.cuda.synchronize(dev)
+    sec = replay_median_s(g, dev, iters) / steps
+    gbs = step_bytes_total / sec / 1e9
+    return {"calls_per_step": len(ws.mats), "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
+            "frac": round(gbs / peak, 4)}
+
+
+def launch_floor(dev, reps: int = 20, iters: int = 20) -> dict:
     """The same call on a 1 x 256 matrix (144 bytes of blocks), timed exactly like the
     single 2048 x 2048 product: batched calls on one stream, each a programmatic dependent
     of the one before, replayed from a CUDA graph. What one call costs when it moves
@@ -419,16 +491,11 @@ def launch_floor(dev, reps: int = 20, iters: int = 5) -> dict:
             ws.run(arrays, 1)
     g.replay()
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(iters):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    return {"M": 1, "K": 256, "us": round(e0.elapsed_time(e1) / (reps * iters) * 1e3, 2)}
+    rep_s = replay_median_s(g, dev, iters)
+    return {"M": 1, "K": 256, "us": round(rep_s / reps * 1e6, 2)}
 
 
-def dense_context_measure(dev, reps: int = 20, iters: int = 5) -> dict:
+def dense_context_measure(dev, reps: int = 20, iters: int = 20) -> dict:
     """Same-box context, not a target: torch.matmul on dense bf16 weights and bf16 X at the
     workload shapes (the dense path that quantized decode avoids, and the library GEMM
     that prefill competes with). Weight sets under 4x L2 are copied and rotated."""
@@ -450,13 +517,8 @@ def dense_context_measure(dev, reps: int = 20, iters: int = 5) -> dict:
                 fn(r)
         g.replay()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(iters):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / (reps * iters) * 1e3   # us
+        rep_s = replay_median_s(g, dev, iters)
+        return rep_s / reps * 1e6   # us
 
     out = {"what": "torch.matmul, bf16 weights and activations, fp32 accumulate (cuBLAS)",
            "decode_us": {}, "prefill": {}}
@@ -578,7 +640,7 @@ def oracle_per_config(dev, target_s: float = 0.4) -> dict:
     return out
 
 
-def q8x_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2, 4, 8, 16)) -> dict:
+def q8x_measure(dev, reps: int = 20, iters: int = 20, Ns=(1, 2, 4, 8, 16)) -> dict:
     """The TinyLLaMA Q4_0 decode step through gq_mul_mat_q8x (X quantized per 32-block
     like Q8_0, integer block sums): batched calls replayed from a CUDA graph. GB/s counts
     weights + X + Y once per step, as for the exact path."""
@@ -601,13 +663,8 @@ def q8x_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2, 4, 8, 16)) -> dic
                 ws.run_q8x(arrays, N)
         g.replay()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(iters):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        sec = e0.elapsed_time(e1) / (reps * iters) / 1e3
+        rep_s = replay_median_s(g, dev, iters)
+        sec = rep_s / reps
         gbs = nb["total"] / sec / 1e9
         rows.append({"N": N, "us": round(sec * 1e6, 2), "GBps": round(gbs, 1),
                      "frac": round(gbs / peak, 4)})
@@ -618,7 +675,7 @@ def q8x_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2, 4, 8, 16)) -> dic
             "unit": "GB/s", "per_N": rows}
 
 
-def fused_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2)) -> dict:
+def fused_measure(dev, reps: int = 20, iters: int = 20, Ns=(1, 2)) -> dict:
     """The fused adjacent steps at decode, each timed from a CUDA graph against the plain
     products it replaces: TinyLLaMA's FFN gate/up pair (2 x 5632 x 2048) through
     gq_mul_mat_swiglu vs two gq_mul_mat calls, and the final RMSNorm into the LM head
@@ -643,13 +700,8 @@ def fused_measure(dev, reps: int = 20, iters: int = 5, Ns=(1, 2)) -> dict:
                 calls[r % len(calls)]()
         g.replay()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(iters):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / (reps * iters) / 1e3
+        rep_s = replay_median_s(g, dev, iters)
+        return rep_s / reps
 
     out = {"unit": "GB/s", "peak": peak}
     nf = copies(2 * Mf * rb)
@@ -938,14 +990,18 @@ def run_gb300(args, shapes):
         # the details after it
         line["summary"] = None
         line["cpu_baseline"] = None
+        step_calls = step_as_calls_measure(dev, ws, xs, ys, N, nb["total"])
         dec = decode_measure(dev)
+        per_mm = per_matmul_measure(dev)
         q8x = q8x_measure(dev)
         fused = fused_measure(dev)
         pf = prefill_measure(dev)
         dense = dense_context_measure(dev)
+        dec["tinyllama_step_as_155_calls_q4_0"] = step_calls
         line["summary"] = summarize(dec, pf, dense, peak)
         line["decode"] = {"unit": "GB/s", "peak": peak,
                           "peak_source": line["roofline"]["peak_source"], **dec}
+        line["decode_per_matmul"] = per_mm
         line["decode_q8x"] = q8x
         line["fused"] = fused
         line["prefill"] = {"unit": "TFLOP/s", "dtype": "bf16 operands, fp32 accumulate",
@@ -970,6 +1026,7 @@ def summarize(dec: dict, pf: dict, dense: dict, peak: float) -> dict:
     def per_n(key):
         return {f"N{r['N']}": [r["us"], r["GBps"], r["frac"]] for r in dec[key]["per_N"]}
 
+
     single = dec["single_q4_0_2048x2048"]
     r1 = single["per_N"][0]
     out = {
@@ -982,6 +1039,9 @@ def summarize(dec: dict, pf: dict, dense: dict, peak: float) -> dict:
         "w5_llama7b_q4_0": per_n("llama7b_decode_q4_0"),
         "w2_tinyllama_q4_k": per_n("tinyllama_decode_q4_k"),
     }
+    calls = dec.get("tinyllama_step_as_155_calls_q4_0")
+    if calls:
+        out["w2_tinyllama_q4_0_N1_as_155_calls"] = [calls["us"], calls["GBps"], calls["frac"]]
     for key, v in pf.items():
         out["prefill_" + key] = [v["tflops"], v["frac"]]
     ctx = dense.get("decode_us", {})

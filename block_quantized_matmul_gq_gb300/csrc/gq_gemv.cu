@@ -815,8 +815,10 @@ __device__ __forceinline__ void pair_dot_q4(const uint8_t* raw, int rs, int rows
 }
 
 // sum over one 32-element sub-block of q x16: x holds the sub-block's 32 int16 (word w =
-// elements 2w, 2w + 1), q[i] the codes of elements 4i .. 4i + 3 as bytes. Exact (|sum| <=
-// 15 * 32767 * 32 < 2^24); four independent dp2a chains.
+// elements 2w, 2w + 1), q[i] the codes of elements 4i .. 4i + 3 as bytes. The high-nibble
+// sub-block passes its codes as 16 q (the bytes masked, not shifted) and gets 16 S back,
+// exact in int32 (|16 S| <= 240 * 32767 * 32 < 2^31), so an arithmetic shift by 4 returns
+// S exactly. Four independent dp2a chains.
 __device__ __forceinline__ int q4k_sub_dot(const uint4 (&x)[4], const uint32_t (&q)[8]) {
     int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
     s0 = dp2a_lo_su(static_cast<int>(x[0].x), q[0], s0);
@@ -871,7 +873,7 @@ __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 lo[i] = cw[i] & 0x0F0F0F0Fu;
-                hi[i] = (cw[i] >> 4) & 0x0F0F0F0Fu;
+                hi[i] = cw[i] & 0xF0F0F0F0u;   // 16 q: one instruction, no shift
             }
             uint32_t sc, m;
             q4k_scales(hd, g, sc, m);
@@ -880,7 +882,7 @@ __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs
 #pragma unroll
             for (int t = 0; t < kNT; ++t) {
                 const int S0 = q4k_sub_dot(X[t].x[0], lo);
-                const int S1 = q4k_sub_dot(X[t].x[1], hi);
+                const int S1 = q4k_sub_dot(X[t].x[1], hi) >> 4;   // 16 S1 exactly
                 const int T = static_cast<int>(sc & 0xFFu) * S0 + static_cast<int>(sc >> 8) * S1;
                 const int U = static_cast<int>(m & 0xFFu) * X[t].bias[0] +
                               static_cast<int>(m >> 8) * X[t].bias[1];
@@ -915,7 +917,7 @@ __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs
                 const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                 uint32_t q[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) q[i] = (cw[i] >> (4 * h)) & 0x0F0F0F0Fu;
+                for (int i = 0; i < 8; ++i) q[i] = cw[i] & (h ? 0xF0F0F0F0u : 0x0F0F0F0Fu);
                 uint32_t sc, m;
                 q4k_scales(hd, g, sc, m);
                 const int scj = static_cast<int>((sc >> (8 * h)) & 0xFFu);
@@ -924,7 +926,7 @@ __device__ __forceinline__ void quarter_dot_q4k(const uint8_t* sb, int g, int rs
                 const float dmin = half_bits_to_float(hd.x >> 16);
 #pragma unroll
                 for (int t = 0; t < kNT; ++t) {
-                    const int S = q4k_sub_dot(xv[t], q);
+                    const int S = q4k_sub_dot(xv[t], q) >> (4 * h);   // h = 1: 16 S exactly
                     acc[r][t] = fmaf(-dmin, static_cast<float>(mj * xs[t]),
                                      fmaf(d, static_cast<float>(scj * S), acc[r][t]));
                 }
