@@ -739,3 +739,31 @@ def test_fused_misaligned_inputs_take_the_composite_path(gq_lib, oracle_mod, cud
     H = gq_lib.mul_mat_swiglu(qd, torch.from_numpy(qu).to(cuda_dev), t, M, K, Xm)
     _check_swiglu(oracle_mod, t, q, qu, M, K, X, H.cpu().numpy(), "swiglu, X misaligned")
     assert gq_lib.get_last_error() == 0
+
+
+# GEMM forms under back-to-back replay: 256-token tiles (80 tiles, unsplit), cluster split-K
+# (4 and 2 ways), 512-token tiles (two MMA issuers for Q4_0 / Q4_K). Each call's stage rings run many phases and the next
+# call starts right after the last; every replayed result must equal a single call's bits.
+GEMM_REPLAY = [(10236, 256, 200), (1000, 2048, 257), (300, 512, 100), (10240, 512, 300)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
+@pytest.mark.parametrize("M,K,N", GEMM_REPLAY)
+def test_gemm_graph_replays_match_a_single_call(gq_lib, cuda_dev, t, M, K, N):
+    q = gq_lib.quantize(workloads.weights(M, K, 61, device=cuda_dev), t)
+    X = workloads.activations(N, K, 62, device=cuda_dev)
+    ref = gq_lib.mul_mat(q, t, M, K, X)
+    ws = torch.empty(gq_lib.workspace_size(t, M, K, N), dtype=torch.uint8, device=cuda_dev)
+    outs = [torch.empty((N, M), device=cuda_dev) for _ in range(4)]
+    gq_lib.mul_mat_ws(q, t, M, K, X, ws, out=outs[0])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(12):
+            gq_lib.mul_mat_ws(q, t, M, K, X, ws, out=outs[i % 4])
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    assert gq_lib.get_last_error() == 0
+    for o in outs:
+        assert torch.equal(o.view(torch.int32), ref.view(torch.int32))
