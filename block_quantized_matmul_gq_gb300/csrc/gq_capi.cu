@@ -127,7 +127,7 @@ cudaError_t internal_workspace(cudaStream_t s, size_t bytes, void** out) {
 gq_status run_one(gq_type t, const gq::MatProblem& p, int64_t N, void* ws, size_t ws_bytes,
                   cudaStream_t s) {
     if (gq::gemv_tc_eligible(t, p, N)) {
-        const size_t need = static_cast<size_t>(gq::gemv_tc_workspace_bytes(&p, 1, N));
+        const size_t need = static_cast<size_t>(gq::gemv_tc_workspace_bytes(t, &p, 1, N));
         void* w = ws;
         if (w == nullptr) {
             if (internal_workspace(s, need, &w) != cudaSuccess) return GQ_ERR_CUDA;
@@ -208,7 +208,7 @@ size_t gq_mul_mat_workspace_size(gq_type t, int64_t M, int64_t K, int64_t N) {
     gq::MatProblem p{reinterpret_cast<const uint8_t*>(uintptr_t(256)),
                      reinterpret_cast<const float*>(uintptr_t(256)), nullptr, M, K};
     if (gq::gemv_tc_eligible(t, p, N))
-        return static_cast<size_t>(gq::gemv_tc_workspace_bytes(&p, 1, N));
+        return static_cast<size_t>(gq::gemv_tc_workspace_bytes(t, &p, 1, N));
     return gq::gemm_eligible(t, p, N) ? static_cast<size_t>(gq::gemm_workspace_bytes(K, N)) : 0;
 }
 
@@ -270,7 +270,7 @@ gq_status plan_batch(const gq_mul_mat_problem* problems, int32_t count, gq_type 
         }
     }
     const size_t tc_sum =
-        plan->n_tc ? static_cast<size_t>(gq::gemv_tc_workspace_bytes(plan->tc, plan->n_tc, N)) : 0;
+        plan->n_tc ? static_cast<size_t>(gq::gemv_tc_workspace_bytes(t, plan->tc, plan->n_tc, N)) : 0;
     plan->ws_bytes = std::max(gemm_max, tc_sum);
     return GQ_OK;
 }

@@ -210,6 +210,25 @@ __device__ __forceinline__ void q4_codes_at(const uint32_t* r, uint32_t (&out)[1
     }
 }
 
+// Codes only, Q4_K: the 32 exact codes q (0..15) of one sub-block as bf16 pairs in the
+// order of dequant_q4k_sub (out[i] = elements 2i, 2i + 1); cw[0..7] are the quarter's code
+// words, nibble h. The scales and mins are applied to the product afterwards, in fp32.
+template <int h>
+__device__ __forceinline__ void q4k_codes(const uint32_t* cw, uint32_t (&out)[16]) {
+    const __nv_bfloat162 off = __float2bfloat162_rn(128.0f);
+    auto pair = [&](uint32_t bytes4, uint32_t sel) {
+        const uint32_t v = __byte_perm(bytes4, 0x43434343u, sel);   // (128 + q, 128 + q')
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+        return *reinterpret_cast<const uint32_t*>(&q);
+    };
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = (cw[i] >> (4 * h)) & 0x0F0F0F0Fu;   // elements 4i .. 4i + 3
+        out[2 * i] = pair(w, 0x4140u);
+        out[2 * i + 1] = pair(w, 0x4342u);
+    }
+}
+
 // Block `blk` (0..7) of a row's super-step (Q4_K: sub-block blk of its super-block), raw
 // bytes in r from the super-step's start.
 template <int kType, int blk>

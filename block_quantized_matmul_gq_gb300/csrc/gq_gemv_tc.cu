@@ -73,10 +73,13 @@ struct TcLayout {
     // TMEM: kAccBufs sets of four accumulators (one per quarter) of kNPad columns, then
     // two groups x kGroupSlots A slots of 64 columns. Two sets let a tile's epilogue
     // overlap the next tile's MMAs; at 64 tokens only one set fits next to the A slots.
-    // Scaled form (Q4_0, up to 16 tokens): A holds the exact codes c - 8 and every 32-k
-    // block has its own accumulator, two buffers of a super-step's eight (256 columns);
-    // the issuer warps apply the block scales in fp32.
-    static constexpr bool kScaled = kType == GQ_TYPE_Q4_0 && kNPad == 16;
+    // Scaled form (Q4_0 and Q4_K, up to 16 tokens): A holds the exact codes (c - 8, or the
+    // Q4_K q) and every 32-k block has its own accumulator, two buffers of a super-step's
+    // eight (256 columns); the dequantize warps apply the block scales in fp32 (Q4_K: and
+    // the mins, against the per-token block sums of X that follow each super-step's X
+    // tiles, kSums).
+    static constexpr bool kScaled = (kType == GQ_TYPE_Q4_0 || kType == GQ_TYPE_Q4_K) && kNPad == 16;
+    static constexpr bool kSums = kScaled && kType == GQ_TYPE_Q4_K;
     static constexpr int kAccBufs = kNPad <= 32 ? 2 : 1;
     static constexpr int kUnitCols = (kSuperK / 32) * kNPad;   // scaled: a super-step's blocks
     static constexpr int kAccCols =
@@ -86,7 +89,12 @@ struct TcLayout {
     static constexpr int kB = kNPad * kBK * 2;              // one 64-k X tile: 2 / 4 / 8 KB
     static constexpr int kRawRow = RawFmt<kType>::kRow;     // 144 / 272
     static constexpr int kRaw = kBM * kRawRow;              // 18 / 34 KB of raw blocks
-    static constexpr int kStage = kRaw + 4 * kB;            // raw blocks + the super-step's X
+    // X of a super-step: four tiles, then with kSums the 8 x kNPad fp32 block sums (512 B,
+    // in a 1 KB slot that keeps the stages 1 KB aligned). kXCopy bytes are copied.
+    static constexpr int kXCopy = 4 * kB + (kSums ? 8 * kNPad * 4 : 0);
+    static constexpr int kXSlot = 4 * kB + (kSums ? 1024 : 0);
+    static constexpr int kStage = kRaw + kXSlot;            // raw blocks + the super-step's X
+    static constexpr int kStageTx = kRaw + kXCopy;          // bytes a stage's copies deliver
     static constexpr int kOffRaw = 0;
     // Scaled: the two dequantize groups' halves of a tile's y meet in shared memory, one
     // buffer (tiles are at least 8 super-steps apart), 128 rows x kNPad (+1 against bank
@@ -358,6 +366,10 @@ __device__ void tc_issue_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint32_
 // every super-step for all 128 rows, one row per thread). Per super-step it stores the
 // codes c - 8 of its half row in the group's A slot, then, one super-step behind the MMAs,
 // adds d_blk * acc_blk of its four blocks to its fp32 y (blocks and super-steps in order).
+// Q4_K: the blocks are sub-blocks 4g .. 4g + 3, the codes q, and each adds
+// D acc - M xsum with D = d sc and M = dmin m (exact) and xsum the block's sum of the bf16
+// X, per token, which the super-step's stage holds after its X tiles; the stage is
+// released only after that scaling.
 // At a tile's end group 1 hands its y to group 0 through shared memory; group 0 writes
 // y0 + y1 to Y, or to this CTA's partial slot of a split tile.
 template <int kType, int kNPad, int kMaxProbs>
@@ -368,7 +380,9 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
     constexpr int R = L::kRawStages;
     constexpr int G = L::kGroupSlots;
     constexpr int B = L::kAccBufs;
-    constexpr int kHalfWords = L::kRawRow / 8;   // 18
+    constexpr bool kQ4K = kType == GQ_TYPE_Q4_K;
+    // Q4_0: a half row of 72 bytes; Q4_K: the 16 header bytes and the group's two quarters
+    constexpr int kHalfWords = kQ4K ? 20 : L::kRawRow / 8;
     constexpr int kHalfBlocks = 4;
     auto raw_full = [&](int r) { return bar0 + 8u * r; };
     auto raw_empty = [&](int r) { return bar0 + 8u * (R + r); };
@@ -391,6 +405,7 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
 #pragma unroll
     for (int t = 0; t < kNPad; ++t) y[t] = 0.0f;
     float dprev[kHalfBlocks];
+    float mprev[kHalfBlocks];         // Q4_K: the blocks' M = dmin m
     int prev_n = -1;                  // super-step whose scaling is due
     bool prev_last = false;           // ... and it ends its tile
     int prev_p = 0, prev_rows = 0, prev_slot = -1;
@@ -399,7 +414,7 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
     int64_t head_row0 = 0;
     int tile_n = 0;                   // tiles finished by this CTA
 
-    auto scale = [&](int n, const float (&d)[kHalfBlocks]) -> bool {
+    auto scale = [&](int n, const float (&d)[kHalfBlocks], const float (&m)[kHalfBlocks]) -> bool {
         const int b = n & 1;
         if (!warp_wait(acc_full(b), (n >> 1) & 1)) return false;
         tc_fence_after();
@@ -409,12 +424,39 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
 #pragma unroll
         for (int blk = 0; blk < kHalfBlocks; ++blk) tmem_ld16_async(acc + blk * kNPad, v[blk]);
         tmem_ld_wait();
+        if constexpr (kQ4K) {
+            // the block sums of super-step n, in its stage after the X tiles (the stage is
+            // released below, once they have been read)
+            const int rn = n % R;
+            const float4* xs = reinterpret_cast<const float4*>(
+                base + L::kOffRaw + rn * L::kStage + L::kRaw + 4 * L::kB +
+                (g * kHalfBlocks) * kNPad * 4);
+            uint32_t dep = 0;
 #pragma unroll
-        for (int blk = 0; blk < kHalfBlocks; ++blk) {
+            for (int blk = 0; blk < kHalfBlocks; ++blk) {
 #pragma unroll
-            for (int t = 0; t < kNPad; t += 2)   // y = fma(d, acc, y) on two tokens at once
-                fma2_bcast(y[t], y[t + 1], d[blk], __uint_as_float(v[blk][t]),
-                           __uint_as_float(v[blk][t + 1]));
+                for (int t4 = 0; t4 < kNPad / 4; ++t4) {
+                    const float4 s4 = xs[blk * (kNPad / 4) + t4];
+                    const int t = 4 * t4;
+                    fma2_bcast(y[t], y[t + 1], d[blk], __uint_as_float(v[blk][t]),
+                               __uint_as_float(v[blk][t + 1]));
+                    fma2_bcast(y[t + 2], y[t + 3], d[blk], __uint_as_float(v[blk][t + 2]),
+                               __uint_as_float(v[blk][t + 3]));
+                    fma2_bcast(y[t], y[t + 1], -m[blk], s4.x, s4.y);
+                    fma2_bcast(y[t + 2], y[t + 3], -m[blk], s4.z, s4.w);
+                    dep ^= __float_as_uint(s4.x);
+                }
+            }
+            release_to_async_proxy(dep);
+            mbar_arrive(raw_empty(rn));
+        } else {
+#pragma unroll
+            for (int blk = 0; blk < kHalfBlocks; ++blk) {
+#pragma unroll
+                for (int t = 0; t < kNPad; t += 2)   // y = fma(d, acc, y) on two tokens at once
+                    fma2_bcast(y[t], y[t + 1], d[blk], __uint_as_float(v[blk][t]),
+                               __uint_as_float(v[blk][t + 1]));
+            }
         }
         return true;
     };
@@ -469,7 +511,35 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
             ok = false;
             break;
         }
-        {
+        float dcur[kHalfBlocks];
+        float mcur[kHalfBlocks];
+        if constexpr (kQ4K) {
+            // header and quarters 2g, 2g + 1 (sub-blocks 4g .. 4g + 3); the stage is released
+            // after the scaling of this super-step, which reads its block sums
+            const uint8_t* rowp = base + L::kOffRaw + r * L::kStage + row * L::kRawRow;
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    rowp + (i == 0 ? 0 : 16 + 64 * g + 16 * (i - 1)));
+                raw[4 * i] = v.x;
+                raw[4 * i + 1] = v.y;
+                raw[4 * i + 2] = v.z;
+                raw[4 * i + 3] = v.w;
+            }
+            const uint4 hd = make_uint4(raw[0], raw[1], raw[2], raw[3]);
+            uint32_t sc01, m01, sc23, m23;
+            q4k_scales(hd, 2 * g, sc01, m01);
+            q4k_scales(hd, 2 * g + 1, sc23, m23);
+            const float dd = half_bits_to_float(raw[0] & 0xFFFFu);
+            const float dm = half_bits_to_float(raw[0] >> 16);
+            const uint32_t scs[4] = {sc01 & 0xFFu, sc01 >> 8, sc23 & 0xFFu, sc23 >> 8};
+            const uint32_t ms[4] = {m01 & 0xFFu, m01 >> 8, m23 & 0xFFu, m23 >> 8};
+#pragma unroll
+            for (int blk = 0; blk < kHalfBlocks; ++blk) {
+                dcur[blk] = __fmul_rn(dd, static_cast<float>(scs[blk]));
+                mcur[blk] = __fmul_rn(dm, static_cast<float>(ms[blk]));
+            }
+        } else {
             const uint8_t* src =
                 base + L::kOffRaw + r * L::kStage + row * L::kRawRow + g * (L::kRawRow / 2);
             uint32_t dep;
@@ -481,43 +551,56 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
                 dep = half_row_dep<1>(raw);
             }
             release_to_async_proxy(dep);
-        }
-        mbar_arrive(raw_empty(r));
-        float dcur[kHalfBlocks];
+            mbar_arrive(raw_empty(r));
 #pragma unroll
-        for (int blk = 0; blk < kHalfBlocks; ++blk)
-            dcur[blk] = half_bits_to_float(u16_at(raw, blk * kQ4Bytes));
+            for (int blk = 0; blk < kHalfBlocks; ++blk) {
+                dcur[blk] = half_bits_to_float(u16_at(raw, blk * kQ4Bytes));
+                mcur[blk] = 0.0f;
+            }
+        }
         // The A slot of super-step n was last read by the MMAs of n - G (G = 2), which this
         // thread saw complete when it waited for acc_full(n - 2) while scaling it.
         static_assert(G == 2, "slot reuse follows the accumulator buffers");
         const int gi = raw_n % G;
         tc_fence_after();
         const uint32_t a_slot = a_lane + (g * G + gi) * kSlotCols;
-        {
+        if constexpr (kQ4K) {
             uint32_t packed[16];
-            q4_codes_at<0 * kQ4Bytes>(raw, packed);
+            q4k_codes<0>(raw + 4, packed);
             tmem_st16(a_slot, packed);
-        }
-        {
-            uint32_t packed[16];
-            q4_codes_at<1 * kQ4Bytes>(raw, packed);
+            q4k_codes<1>(raw + 4, packed);
             tmem_st16(a_slot + 16, packed);
-        }
-        {
-            uint32_t packed[16];
-            q4_codes_at<2 * kQ4Bytes>(raw, packed);
+            q4k_codes<0>(raw + 12, packed);
             tmem_st16(a_slot + 32, packed);
-        }
-        {
-            uint32_t packed[16];
-            q4_codes_at<3 * kQ4Bytes>(raw, packed);
+            q4k_codes<1>(raw + 12, packed);
             tmem_st16(a_slot + 48, packed);
+        } else {
+            {
+                uint32_t packed[16];
+                q4_codes_at<0 * kQ4Bytes>(raw, packed);
+                tmem_st16(a_slot, packed);
+            }
+            {
+                uint32_t packed[16];
+                q4_codes_at<1 * kQ4Bytes>(raw, packed);
+                tmem_st16(a_slot + 16, packed);
+            }
+            {
+                uint32_t packed[16];
+                q4_codes_at<2 * kQ4Bytes>(raw, packed);
+                tmem_st16(a_slot + 32, packed);
+            }
+            {
+                uint32_t packed[16];
+                q4_codes_at<3 * kQ4Bytes>(raw, packed);
+                tmem_st16(a_slot + 48, packed);
+            }
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(a_full(g, gi));
         if (prev_n >= 0) {
-            if (!scale(prev_n, dprev) ||
+            if (!scale(prev_n, dprev, mprev) ||
                 (prev_last && !finish_tile(prev_p, prev_row0, prev_rows, prev_slot))) {
                 ok = false;
                 break;
@@ -525,7 +608,10 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
         }
         prev_n = raw_n;
 #pragma unroll
-        for (int blk = 0; blk < kHalfBlocks; ++blk) dprev[blk] = dcur[blk];
+        for (int blk = 0; blk < kHalfBlocks; ++blk) {
+            dprev[blk] = dcur[blk];
+            mprev[blk] = mcur[blk];
+        }
         prev_last = w.j == w.jend - 1;
         if (prev_last) {
             // a tile cut by this share's start (jbeg > 0) is partial slot 0, one cut by its
@@ -537,7 +623,7 @@ __device__ void tc_dequant_scaled(const TcParams<kMaxProbs>& P, TcWalk& w, uint3
         }
     }
     if (ok && prev_n >= 0) {
-        ok = scale(prev_n, dprev);
+        ok = scale(prev_n, dprev, mprev);
         if (ok && prev_last) ok = finish_tile(prev_p, prev_row0, prev_rows, prev_slot);
     }
     if (ok && head_p >= 0) tc_finish_split<kNPad>(P, head_p, head_row0, head_rows, 0, quad, lane);
@@ -620,7 +706,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             for (; pre.valid && n_pre < R; tc_walk_next(P, pre), ++n_pre) {
                 if (lane == 0) {
                     const uint32_t dst = sRaw + n_pre * L::kStage;
-                    mbar_arrive_expect_tx(raw_full(n_pre), L::kStage);   // raw + X bytes
+                    mbar_arrive_expect_tx(raw_full(n_pre), L::kStageTx);   // raw + X bytes
                     // Whole 128-row box; rows past the matrix end are filled with zeros.
                     tma_load_2d(dst, &P.maps[pre.p], pre.j * (L::kRawRow / RawFmt<kType>::kElem),
                                 static_cast<int>(pre.row0), raw_full(n_pre));
@@ -639,12 +725,12 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             if (lane == 0) {
                 const uint32_t dst = sRaw + r * L::kStage;
                 if (raw_n >= n_pre) {
-                    mbar_arrive_expect_tx(raw_full(r), L::kStage);
+                    mbar_arrive_expect_tx(raw_full(r), L::kStageTx);
                     tma_load_2d(dst, &P.maps[w.p], w.j * (L::kRawRow / RawFmt<kType>::kElem),
                                 static_cast<int>(w.row0), raw_full(r));
                 }
-                bulk_g2s(dst + L::kRaw, P.p[w.p].Xt + static_cast<int64_t>(w.j) * 4 * L::kB,
-                         4 * L::kB, raw_full(r));
+                bulk_g2s(dst + L::kRaw, P.p[w.p].Xt + static_cast<int64_t>(w.j) * L::kXSlot,
+                         L::kXCopy, raw_full(r));
             }
             __syncwarp();
         }
@@ -919,13 +1005,25 @@ struct XtParams {
     int32_t n_tok;
     int* counters;
     int32_t n_counters;
+    int32_t sums;        // append each super-step's 8 x kNPad block sums (Q4_K scaled form)
+    int32_t pad_;
     XtProb p[GQ_MAX_BATCH];
 };
 
+// Bytes of one super-step's X in the workspace (and in a stage): four kNPad x 64 bf16
+// tiles, and with block sums a 1 KB slot holding 8 x kNPad fp32 sums.
+__host__ __device__ constexpr int64_t xt_superstep_bytes(int npad, bool sums) {
+    return int64_t(4) * npad * kBK * 2 + (sums ? 1024 : 0);
+}
+
 // X (n_tok x K fp32, rows of K) -> kNPad x 64 bf16 tiles per 64-k stage, each row 128 bytes
-// with 16-byte chunk c stored at c ^ (row % 8); tokens >= n_tok are zero. One launch for
-// all problems: each problem gets a run of blocks, each block 1024 of its 16-byte output
-// chunks. Block 0 also clears the split-tile counters of the decode kernels that follow.
+// with 16-byte chunk c stored at c ^ (row % 8); tokens >= n_tok are zero. Four tiles form a
+// super-step's slot (xt_superstep_bytes); with P.sums the slot also holds, for each of its
+// eight 32-k blocks b and token n, the fp32 sum of the block's bf16 values at float
+// index b * kNPad + n after the tiles (four threads' chunks, added by a fixed shuffle
+// tree). One launch for all problems: each problem gets a run of blocks, each block 1024
+// of its 16-byte output chunks. Block 0 also clears the split-tile counters of the decode
+// kernels that follow.
 template <int kNPad>
 __global__ void __launch_bounds__(256)
 x_tiles_kernel(const __grid_constant__ XtParams P) {
@@ -968,13 +1066,26 @@ x_tiles_kernel(const __grid_constant__ XtParams P) {
             for (int e = 0; e < 8; ++e) v[e] = 0.0f;
         }
         uint32_t packed[4];
+        float part = 0.0f;   // this chunk's share of its block sum (the bf16 values)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
             packed[e] = *reinterpret_cast<const uint32_t*>(&b);
+            part += __low2float(b) + __high2float(b);
         }
-        *reinterpret_cast<uint4*>(pr.Xt + ks * (kNPad * 128) + n * 128 + ((c ^ (n & 7)) << 4)) =
+        uint8_t* slot = pr.Xt + (ks >> 2) * xt_superstep_bytes(kNPad, P.sums != 0);
+        *reinterpret_cast<uint4*>(slot + (ks & 3) * (kNPad * 128) + n * 128 + ((c ^ (n & 7)) << 4)) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        if (P.sums) {   // uniform across the block: the same for every problem of a launch
+            // chunks c = 4h .. 4h + 3 of one token row are threads li .. li + 3 (li % 4 ==
+            // 0 at c = 4h): block 2 (ks % 4) + h of the super-step
+            part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+            part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
+            if ((c & 3) == 0) {
+                const int blk = 2 * static_cast<int>(ks & 3) + (c >> 2);
+                reinterpret_cast<float*>(slot + 4 * kNPad * 128)[blk * kNPad + n] = part;
+            }
+        }
     }
 }
 
@@ -1074,12 +1185,13 @@ constexpr int64_t kCounterBytes = kCounters * 4;   // 4 KB, keeps the X tiles 25
 
 template <int kNPad>
 cudaError_t launch_x_tiles(const MatProblem* probs, int count, int64_t N, uint8_t* part,
-                           uint8_t* xt, const DeviceInfo* info, cudaStream_t s) {
+                           uint8_t* xt, bool sums, const DeviceInfo* info, cudaStream_t s) {
     XtParams P{};
     P.count = count;
     P.n_tok = static_cast<int32_t>(N);
     P.counters = reinterpret_cast<int*>(part + tc_part_bytes(kNPad));
     P.n_counters = kCounters;
+    P.sums = sums ? 1 : 0;
     (void)info;
     int64_t blocks = 0, off = 0;
     for (int i = 0; i < count; ++i) {
@@ -1089,7 +1201,7 @@ cudaError_t launch_x_tiles(const MatProblem* probs, int count, int64_t N, uint8_
         P.p[i].block_begin = static_cast<int32_t>(blocks);
         P.p[i].x_aligned = reinterpret_cast<uintptr_t>(probs[i].X) % 16 == 0 && probs[i].K % 4 == 0;
         blocks += (probs[i].K / kBK * kNPad * 8 + kXtChunksPerBlock - 1) / kXtChunksPerBlock;
-        off += static_cast<int64_t>(kNPad) * probs[i].K * 2;
+        off += probs[i].K / kSuperK * xt_superstep_bytes(kNPad, sums);
     }
     void* args[] = {&P};
     return launch_pdl(reinterpret_cast<const void*>(x_tiles_kernel<kNPad>),
@@ -1120,7 +1232,7 @@ cudaError_t launch_tc_t(const MatProblem* probs, int count, int64_t N, uint8_t* 
         g.nsuper = static_cast<int32_t>(probs[i].K / kSuperK);
         g.unit_begin = units;
         units += (g.M + kBM - 1) / kBM * g.nsuper;
-        xt_off += static_cast<int64_t>(kNPad) * probs[i].K * 2;
+        xt_off += probs[i].K / kSuperK * xt_superstep_bytes(kNPad, L::kSums);
         cudaError_t e = weight_map<kType>(probs[i].W, probs[i].M, probs[i].K, &P.maps[i]);
         if (e != cudaSuccess) return e;
     }
@@ -1162,9 +1274,14 @@ bool gemv_tc_eligible(gq_type t, const MatProblem& p, int64_t N) {
     return reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 4 == 0;
 }
 
-int64_t gemv_tc_workspace_bytes(const MatProblem* probs, int count, int64_t N) {
-    int64_t b = tc_part_bytes(npad_for(N)) + kCounterBytes;
-    for (int i = 0; i < count; ++i) b += static_cast<int64_t>(npad_for(N)) * probs[i].K * 2;
+// Whether the X slots of this call carry the block sums: the scaled form of Q4_K.
+bool tc_sums(gq_type t, int64_t N) { return t == GQ_TYPE_Q4_K && npad_for(N) == 16; }
+
+int64_t gemv_tc_workspace_bytes(gq_type t, const MatProblem* probs, int count, int64_t N) {
+    const int npad = npad_for(N);
+    int64_t b = tc_part_bytes(npad) + kCounterBytes;
+    for (int i = 0; i < count; ++i)
+        b += probs[i].K / kSuperK * xt_superstep_bytes(npad, tc_sums(t, N));
     return b;
 }
 
@@ -1177,10 +1294,11 @@ cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_
     // tiles of all problems one after another. Launches take at most kMaxLaunchProbs.
     uint8_t* part = static_cast<uint8_t*>(workspace);
     uint8_t* xt = part + tc_part_bytes(npad_for(N)) + kCounterBytes;
+    const bool sums = tc_sums(t, N);
     switch (npad_for(N)) {
-        case 16: e = launch_x_tiles<16>(probs, count, N, part, xt, info, s); break;
-        case 32: e = launch_x_tiles<32>(probs, count, N, part, xt, info, s); break;
-        default: e = launch_x_tiles<64>(probs, count, N, part, xt, info, s); break;
+        case 16: e = launch_x_tiles<16>(probs, count, N, part, xt, sums, info, s); break;
+        case 32: e = launch_x_tiles<32>(probs, count, N, part, xt, false, info, s); break;
+        default: e = launch_x_tiles<64>(probs, count, N, part, xt, false, info, s); break;
     }
     if (e != cudaSuccess) return e;
     for (int i0 = 0; i0 < count; i0 += kMaxLaunchProbs) {
@@ -1189,7 +1307,8 @@ cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_
             : t == GQ_TYPE_Q4_K ? launch_tc_type<GQ_TYPE_Q4_K>(probs + i0, n, N, part, xt, info, s)
                                 : launch_tc_type<GQ_TYPE_Q8_0>(probs + i0, n, N, part, xt, info, s);
         if (e != cudaSuccess) return e;
-        for (int i = i0; i < i0 + n; ++i) xt += static_cast<int64_t>(npad_for(N)) * probs[i].K * 2;
+        for (int i = i0; i < i0 + n; ++i)
+            xt += probs[i].K / kSuperK * xt_superstep_bytes(npad_for(N), sums);
     }
     return cudaSuccess;
 }

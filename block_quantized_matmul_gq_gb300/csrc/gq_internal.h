@@ -92,11 +92,12 @@ cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspa
 
 // Decode on tensor cores for kGemvTcMinTokens..kGemvTcMaxTokens tokens (K % 256 == 0):
 // grouped like launch_mul_mat. Needs gemv_tc_workspace_bytes of workspace (pre-arranged
-// bf16 X tiles, 16 / 32 / 64 token rows per problem), 256-byte aligned.
+// bf16 X tiles, 16 / 32 / 64 token rows per problem; Q4_K up to 16 tokens also the X block
+// sums, 1 KB per 256 k), 256-byte aligned.
 constexpr int64_t kGemvTcMinTokens = 3;
 constexpr int64_t kGemvTcMaxTokens = 64;
 bool gemv_tc_eligible(gq_type t, const MatProblem& p, int64_t N);
-int64_t gemv_tc_workspace_bytes(const MatProblem* probs, int count, int64_t N);
+int64_t gemv_tc_workspace_bytes(gq_type t, const MatProblem* probs, int count, int64_t N);
 cudaError_t launch_gemv_tc(gq_type t, const MatProblem* probs, int count, int64_t N,
                            void* workspace, cudaStream_t s);
 

@@ -82,7 +82,7 @@ extern "C" gq_status gq_mul_mat_noalloc(const void* W_blocks, gq_type t, int64_t
     // zeroes the counters at the start of every call. Past that size, the CUDA-core decode
     // kernels, which need no workspace.
     if (gq::gemv_tc_eligible(t, p, N)) {
-        if (gq::gemv_tc_workspace_bytes(&p, 1, N) > cap)
+        if (gq::gemv_tc_workspace_bytes(t, &p, 1, N) > cap)
             return gq::launch_mul_mat(t, &p, 1, N, s) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
         void* scratch = nullptr;
         if (gq::noalloc_scratch(&scratch) != cudaSuccess) return GQ_ERR_CUDA;

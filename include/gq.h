@@ -144,8 +144,10 @@ gq_status gq_quantize_q8_0(const float* W, int64_t M, int64_t K, void* W_blocks,
  * multiple of 256 (else GQ_ERR_SHAPE). Bit-for-bit reproducible.
  * The mul_mat entry points take Q4_K on the same paths as Q4_0 (CUDA-core decode for
  * N <= 2, tensor-core decode for 3..64 tokens, prefill GEMM from 65, with the same
- * workspace sizes); the tensor-core paths use each weight d sc q - dmin m rounded once in
- * fp32, as gq_dequantize writes it, then rounded to bf16. gq_mul_mat_rmsnorm and
+ * workspace sizes, but for the X block sums below); the tensor-core decode with N <= 16
+ * multiplies the exact codes q and applies d sc and dmin m per sub-block in fp32, and the
+ * other tensor-core forms use each weight d sc q - dmin m rounded once in fp32, as
+ * gq_dequantize writes it, then rounded to bf16. gq_mul_mat_rmsnorm and
  * gq_mul_mat_swiglu take it in their composite forms (norm kernel, then the product; two
  * products, then the elementwise kernel); gq_mul_mat_q8x and gq_mul_mat_q8x_batched
  * return GQ_ERR_TYPE for it (their activation blocks pair with 32-weight blocks).
@@ -170,8 +172,9 @@ gq_status gq_dequantize(const void* W_blocks, gq_type t, int64_t M, int64_t K,
  * on a 16-bit fixed-point copy of X). 3 <= N <= 64 and K % 256 == 0: decode on tensor
  * cores; N >= 65 and K % 256 == 0: the prefill tensor-core GEMM. Both tensor-core paths
  * round X once to bf16 and accumulate in fp32. The weights enter the MMA as bf16
- * dequantized values (rounded once), except Q4_0 decode with N <= 16, which multiplies
- * the exact codes c - 8 and applies each block's scale in fp32.
+ * dequantized values (rounded once), except Q4_0 and Q4_K decode with N <= 16, which
+ * multiply the exact codes (c - 8, or q) and apply each block's scale (and Q4_K's min,
+ * against the block's sum of the bf16 X) in fp32.
  * Accuracy: |Y - Y_exact| <= 1e-3 * ||X[n]||_2 * ||What[m]||_2 per element (for the bf16
  * path, at the K >= 256 it runs on, by a wide margin for non-adversarial data). Q4_K on
  * the CUDA-core kernels forms d (sum sc S) - dmin (sum m X) per quarter super-block in
@@ -186,8 +189,9 @@ gq_status gq_mul_mat(const void* W_blocks, gq_type t, int64_t M, int64_t K,
 /*
  * Device workspace (bytes) that gq_mul_mat_ws needs for this shape: 0 on the CUDA-core
  * decode path (N <= 2); on the tensor-core decode path (3 <= N <= 64) P * K * 2 for
- * P = 16, 32 or 64 token rows of pre-arranged bf16 X, plus 2 * 256 * 128 * P * 4 + 4096
- * for the partial sums (and their counters) of tiles whose k range is split between CTAs;
+ * P = 16, 32 or 64 token rows of pre-arranged bf16 X (Q4_K with N <= 16: plus K / 256 * 1024
+ * for the X block sums), plus 2 * 256 * 128 * P * 4 + 4096 for the partial sums (and
+ * their counters) of tiles whose k range is split between CTAs;
  * N * K * 2 (a bf16 copy of X, rounded up to 256) on the prefill path (N >= 65).
  * Tensor-core paths need K a multiple of 256. 0 for invalid arguments.
  */

@@ -171,11 +171,15 @@ def test_q4_k_sizes_and_host_checks(gq_lib):
     assert mm(A4, 12, 4, 256, A16, 1, A16, None) == -4
     assert mm(None, 12, 0, 256, None, 1, None, None) == 0
     assert lib.gq_mul_mat_noalloc(A16, 12, 4, 288, A16, 1, A16, None) == -2
-    # the same workspace as Q4_0 on every path: none for N <= 2, X tiles and partial sums for
-    # the tensor-core decode, the bf16 copy of X for prefill
-    for N in (1, 2, 4, 16, 40, 64, 512):
+    # the workspace of Q4_0 on every path (none for N <= 2, X tiles and partial sums for the
+    # tensor-core decode, the bf16 copy of X for prefill), plus at 3..16 tokens the X block
+    # sums of the scaled form: 1 KB per 256 k
+    for N in (1, 2, 40, 64, 512):
         assert lib.gq_mul_mat_workspace_size(12, 64, 2048, N) == \
             lib.gq_mul_mat_workspace_size(2, 64, 2048, N)
+    for N in (3, 4, 16):
+        assert lib.gq_mul_mat_workspace_size(12, 64, 2048, N) == \
+            lib.gq_mul_mat_workspace_size(2, 64, 2048, N) + 2048 // 256 * 1024
     assert lib.gq_mul_mat_workspace_size(12, 64, 2048, 2) == 0
     assert lib.gq_mul_mat_workspace_size(12, 64, 2048, 512) == 512 * 2048 * 2
     # quantized activations pair with 32-weight blocks only

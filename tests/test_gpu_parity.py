@@ -465,18 +465,18 @@ def test_decode_tc_matches_oracle(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
 @pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 @pytest.mark.parametrize("N", [4, 16, 40])
 def test_decode_tc_one_hot_returns_operand_weights(gq_lib, oracle_mod, cuda_dev, t, N):
-    """X = e_k returns column k of the weights exactly as the MMA saw them. Q4_0 with up to
-    16 tokens multiplies the exact codes c - 8 and applies the fp16 scale in fp32, so it
-    returns What itself; the other forms (Q4_K: What as gq_dequantize writes it) dequantize
-    to bf16 and return bf16(What). This pins the operand layout, the per-block accumulators
-    and the scale of each block."""
+    """X = e_k returns column k of the weights exactly as the MMA saw them. Q4_0 and Q4_K
+    with up to 16 tokens multiply the exact codes (c - 8, q) and apply the scales (Q4_K: and
+    the mins, against the block sums of X) in fp32, so they return What itself; the other
+    forms (Q4_K: What as gq_dequantize writes it) dequantize to bf16 and return bf16(What).
+    This pins the operand layout, the per-block accumulators and the scale of each block."""
     M, K = 300, 1024
     ks = [(37 * n) % K for n in range(N)]
     X = np.zeros((N, K), np.float32)
     for n, k in enumerate(ks):
         X[n, k] = 1.0
     Y, _, What, _ = run_mul_mat(gq_lib, oracle_mod, cuda_dev, t, M, K, N, X=X)
-    if t == "q4_0" and N <= 16:
+    if t in ("q4_0", "q4_k") and N <= 16:
         expect = What
     else:
         expect = torch.from_numpy(What).to(torch.bfloat16).float().numpy()
