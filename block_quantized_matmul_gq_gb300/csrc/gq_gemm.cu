@@ -84,6 +84,16 @@ struct Layout {
     static_assert(kBM * kBN * 4 <= kOffRaw, "partial tile fits the operand stages");
 };
 
+// Up to 64 accumulator columns [taddr, taddr + 64) of the warp's 32 lanes into v, as x16
+// loads issued together and waited for once (a load's latency is paid per batch, not per
+// 16 columns). Loads only the 16-column groups that start below `avail` (warp-uniform).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64], int avail) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (16 * q < avail) tmem_ld16_async(taddr + 16 * q, v + 16 * q);
+    tmem_ld_wait();
+}
+
 // Stage q (0..3) of a super-step for dequantize half h: block 2q + h of the thread's row,
 // from the raw super-step in registers, into the row's 128-byte swizzled A line.
 template <int kType>
@@ -157,6 +167,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
         tmem_relinquish();
     }
+    __syncwarp();   // lane 0 of warp 0 initialized the barriers alone: the warp arrives whole
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -296,11 +307,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             if (done) {
                 const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
                 const int c_begin = half * (kBN / 2);
-                for (int c = c_begin; c < c_begin + kBN / 2; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tbase + c, v);
+                for (int c = c_begin; c < c_begin + kBN / 2; c += 64) {
+                    uint32_t v[64];
+                    tmem_ld64(tbase + c, v, c_begin + kBN / 2 - c);
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) part[(c + jj) * kBM + row] = __uint_as_float(v[jj]);
+                    for (int jj = 0; jj < 64; ++jj)
+                        if (c + jj < c_begin + kBN / 2) part[(c + jj) * kBM + row] = __uint_as_float(v[jj]);
                 }
             }
         } else if (done && ok) {
@@ -308,14 +320,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             const int c_begin = half * (kBN / 2);
             const int c_end = min(c_begin + kBN / 2, N - n0);
-            for (int c = c_begin; c < c_end; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tbase + c, v);
+            for (int c = c_begin; c < c_end; c += 64) {
+                uint32_t v[64];
+                tmem_ld64(tbase + c, v, c_end - c);
                 if (m < M) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
+                    for (int jj = 0; jj < 64; ++jj) {
                         const int n = n0 + c + jj;
-                        if (n < N) Y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[jj]);
+                        if (c + jj < c_end && n < N)
+                            Y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[jj]);
                     }
                 }
             }
@@ -364,6 +377,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         }
         cluster_sync();
     }
+    // Warps 0 and 1 ran their loops on lane 0 alone: each warp reconverges before the
+    // barrier, so that it counts whole warps and the TMEM is freed only after every
+    // epilogue read.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -467,6 +484,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
         tmem_relinquish();
     }
+    __syncwarp();   // lane 0 of warp 0 initialized the barriers alone: the warp arrives whole
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -598,14 +616,15 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
             const int c_begin = half * L::kHalfN;
             const int c_end = min(c_begin + L::kHalfN, N - n0);
-            for (int c = c_begin; c < c_end; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tbase + c, v);
+            for (int c = c_begin; c < c_end; c += 64) {
+                uint32_t v[64];
+                tmem_ld64(tbase + c, v, c_end - c);
                 if (m < M) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
+                    for (int jj = 0; jj < 64; ++jj) {
                         const int n = n0 + c + jj;
-                        if (n < N) Y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[jj]);
+                        if (c + jj < c_end && n < N)
+                            Y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[jj]);
                     }
                 }
             }
@@ -613,6 +632,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             report_status(status, kStatusTimeout);
         }
     }
+    __syncwarp();   // whole warps at the barrier (warps 0, 1 and 10 ran lane 0 alone)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -684,6 +684,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    __syncwarp();   // whole warps at the barrier (roles run on single lanes)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -981,6 +982,7 @@ gemv_tc_kernel(const __grid_constant__ TcParams<kMaxProbs> P) {
             if (!ok) report_status(P.status, kStatusTimeout);
         }
     }
+    __syncwarp();   // whole warps at the barrier (roles run on single lanes)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {

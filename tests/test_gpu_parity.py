@@ -437,6 +437,29 @@ def test_gemm_unsplit_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
                         rows_per_mat=24)
 
 
+# Several waves of 256-token tiles with ragged edges: 471 tiles (3.1 waves) with a 31-row
+# last row block and an 8-token tail; 400 tiles (2.6 waves) with a 4-token tail.
+GEMM_MULTIWAVE = [(19999, 256, 520), (25600, 512, 260)]
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
+@pytest.mark.parametrize("M,K,N", GEMM_MULTIWAVE)
+def test_gemm_multiwave_tiles_sampled(gq_lib, oracle_mod, cuda_dev, t, M, K, N):
+    _sampled_step_check(gq_lib, oracle_mod, cuda_dev, 9, t, N, [workloads.MatShape("tiles", M, K)],
+                        rows_per_mat=24)
+
+
+@pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
+def test_gemm_multiwave_tiles_deterministic(gq_lib, cuda_dev, t):
+    M, K, N = GEMM_MULTIWAVE[0]
+    q = gq_lib.quantize(workloads.weights(M, K, 10, device=cuda_dev), t)
+    X = workloads.activations(N, K, 11, device=cuda_dev)
+    y1 = gq_lib.mul_mat(q, t, M, K, X)
+    y2 = gq_lib.mul_mat(q, t, M, K, X)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert gq_lib.get_last_error() == 0
+
+
 @pytest.mark.parametrize("t", ["q4_0", "q8_0", "q4_k"])
 def test_gemm_wide_tiles_deterministic(gq_lib, cuda_dev, t):
     M, K, N = GEMM_WIDE[1]
