@@ -1001,7 +1001,7 @@ struct XtProb {
     int32_t block_begin;   // first block of x_tiles_kernel that works on this problem
     int32_t x_aligned;     // X is 16-byte aligned: vector loads
 };
-constexpr int kXtChunksPerBlock = 1024;   // 4 per thread
+constexpr int kXtChunksPerBlock = 1024;   // 4 per thread (256 threads)
 struct XtParams {
     int32_t count;
     int32_t n_tok;
@@ -1047,31 +1047,45 @@ x_tiles_kernel(const __grid_constant__ XtParams P) {
     const int64_t chunks = pr.K / kBK * kNPad * 8;
     const int64_t first = static_cast<int64_t>(blockIdx.x - pr.block_begin) * kXtChunksPerBlock;
     const int64_t last = min(chunks, first + kXtChunksPerBlock);
-    for (int64_t li = first + threadIdx.x; li < last; li += blockDim.x) {
+    // Every chunk of the thread is loaded before any is converted, so that all of them are
+    // in flight at once: a launch for few problems (a handful of blocks) is then one load
+    // latency long, not kXtPerThread of them.
+    constexpr int kXtPerThread = kXtChunksPerBlock / 256;
+    float v[kXtPerThread][8];
+#pragma unroll
+    for (int i = 0; i < kXtPerThread; ++i) {
+        const int64_t li = first + threadIdx.x + 256 * i;
         const int c = static_cast<int>(li & 7);
         const int n = static_cast<int>((li >> 3) % kNPad);
         const int64_t ks = (li >> 3) / kNPad;
-        float v[8];
-        if (n < P.n_tok) {
+        if (li < last && n < P.n_tok) {
             const float* x = pr.X + n * pr.K + ks * kBK + 8 * c;
             if (pr.x_aligned) {
                 const float4 a = *reinterpret_cast<const float4*>(x);
                 const float4 b = *reinterpret_cast<const float4*>(x + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
+                v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = x[e];
+                for (int e = 0; e < 8; ++e) v[i][e] = x[e];
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+            for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
         }
+    }
+#pragma unroll
+    for (int i = 0; i < kXtPerThread; ++i) {
+        const int64_t li = first + threadIdx.x + 256 * i;
+        if (li >= last) break;   // warp-uniform: chunk counts are multiples of 512
+        const int c = static_cast<int>(li & 7);
+        const int n = static_cast<int>((li >> 3) % kNPad);
+        const int64_t ks = (li >> 3) / kNPad;
         uint32_t packed[4];
         float part = 0.0f;   // this chunk's share of its block sum (the bf16 values)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v[i][2 * e], v[i][2 * e + 1]);
             packed[e] = *reinterpret_cast<const uint32_t*>(&b);
             part += __low2float(b) + __high2float(b);
         }
