@@ -641,7 +641,15 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 }
 
-// X (fp32, n4 * 4 elements) -> bf16, round to nearest even.
+// X (fp32, n elements) -> bf16, round to nearest even. Each thread keeps kXUnroll
+// 16-byte loads in flight. The kSide instance runs on a few blocks per SM with the
+// max-shared carveout, so that the GEMM after it (a programmatic dependent) finds room on
+// every SM and runs its prologue, first weight copies and dequantization beside the
+// conversion; it is used for small X, where that start-up is a large part of the call.
+constexpr int kXUnroll = 4;
+constexpr int kXSideBlocksPerSm = 2;
+constexpr int64_t kXSideMaxElems = int64_t(1) << 22;   // 16 MB of fp32 X
+template <bool kSide>
 __global__ void __launch_bounds__(256)
 x_to_bf16_kernel(const float* __restrict__ X, int64_t n, __nv_bfloat16* __restrict__ out) {
     // The GEMM launched after this kernel may start its prologue and weight copies now; it
@@ -651,11 +659,18 @@ x_to_bf16_kernel(const float* __restrict__ X, int64_t n, __nv_bfloat16* __restri
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if ((reinterpret_cast<uintptr_t>(X) & 15) == 0) {
         const int64_t n4 = n / 4;
-        for (int64_t i = i0; i < n4; i += stride) {
-            const float4 v = reinterpret_cast<const float4*>(X)[i];
-            __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + 4 * i);
-            o[0] = __floats2bfloat162_rn(v.x, v.y);
-            o[1] = __floats2bfloat162_rn(v.z, v.w);
+        for (int64_t i = i0; i < n4; i += stride * kXUnroll) {
+            float4 v[kXUnroll];
+#pragma unroll
+            for (int u = 0; u < kXUnroll; ++u)
+                if (i + u * stride < n4) v[u] = reinterpret_cast<const float4*>(X)[i + u * stride];
+#pragma unroll
+            for (int u = 0; u < kXUnroll; ++u) {
+                if (i + u * stride >= n4) break;
+                __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + 4 * (i + u * stride));
+                o[0] = __floats2bfloat162_rn(v[u].x, v[u].y);
+                o[1] = __floats2bfloat162_rn(v[u].z, v[u].w);
+            }
         }
         for (int64_t i = 4 * n4 + i0; i < n; i += stride) out[i] = __float2bfloat16_rn(X[i]);
     } else {
@@ -696,6 +711,19 @@ cudaError_t ensure_smem(KernelT kernel, int device, int64_t bytes) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
     if (e == cudaSuccess) set_bytes[key] = bytes;
+    return e;
+}
+
+template <typename KernelT>
+cudaError_t ensure_max_shared_carveout(KernelT kernel, int device) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, bool> done;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), device);
+    if (done.count(key)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess) done[key] = true;
     return e;
 }
 
@@ -869,9 +897,18 @@ cudaError_t launch_gemm(gq_type t, const MatProblem& p, int64_t N, void* workspa
     if (e != cudaSuccess) return e;
     __nv_bfloat16* xb = static_cast<__nv_bfloat16*>(workspace);
     const int64_t n = N * p.K;
-    const int grid = static_cast<int>(std::min<int64_t>((n / 4 + 255) / 256 + 1,
-                                                        int64_t(info->sm_count) * 8));
-    x_to_bf16_kernel<<<grid, 256, 0, s>>>(p.X, n, xb);
+    const int64_t blocks = (n / 4 + 256 * kXUnroll - 1) / (256 * kXUnroll) + 1;
+    if (n <= kXSideMaxElems) {
+        // The instance's carveout: an SM set up for it alone would hold little shared
+        // memory, and a GEMM CTA could not join it there until the SM drained.
+        e = ensure_max_shared_carveout(x_to_bf16_kernel<true>, info->device);
+        if (e != cudaSuccess) return e;
+        const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(info->sm_count) * kXSideBlocksPerSm));
+        x_to_bf16_kernel<true><<<grid, 256, 0, s>>>(p.X, n, xb);
+    } else {
+        const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(info->sm_count) * 8));
+        x_to_bf16_kernel<false><<<grid, 256, 0, s>>>(p.X, n, xb);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (t == GQ_TYPE_Q4_0) return launch_gemm_t<GQ_TYPE_Q4_0, 256>(p, N, xb, info, s);
