@@ -207,6 +207,15 @@ struct GemvParams {
 // group costs the same as a full one). 576 was the best of 0 / 576 / 1152 / 2304 / 4608
 // measured on the TinyLLaMA and LLaMA-7B sets (Q4_0 and Q8_0, N = 1 and 2).
 constexpr int64_t kGroupCost = 576;
+// Balancing weight of a problem boundary inside a CTA's share: the CTA prepares that
+// problem's activations and synchronizes its warps before streaming it (~2 us per extra
+// problem in a clock-stamped trace of the TinyLLaMA and LLaMA-7B steps, where the CTAs
+// with four or five problems finished up to 12 us after those with one).
+constexpr int64_t kSegCost = 65536;
+// Extra weight per column group of rows longer than one group, whose stages take one copy
+// per row instead of one for the whole tile. Measured against 0 / 512 / 768 / 1536 with the
+// segment weight: 256 was best on the TinyLLaMA Q4_0 step (93.0 -> 91.2 us at N = 1).
+constexpr int64_t kRowCopyCost = 256;
 
 // First row (problem p, row r) whose weight begins at or after `cost`; (count, 0) = end.
 // Host side: the cuts of the CTA shares (GemvParams::cut_p / cut_r). Costs increase with
@@ -1411,7 +1420,9 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
         g.K = static_cast<int32_t>(probs[i].K);
         g.C = static_cast<int32_t>(probs[i].K / wpc);
         g.row_bytes = static_cast<int64_t>(g.C) * cb;
-        g.row_cost = g.row_bytes + kGroupCost * ((g.C + kLanesPerRow - 1) / kLanesPerRow);
+        const int64_t groups = (g.C + kLanesPerRow - 1) / kLanesPerRow;
+        g.row_cost = g.row_bytes + (kGroupCost + (g.C > kLanesPerRow ? kRowCopyCost : 0)) * groups;
+        if (i > 0) cost += kSegCost;
         g.cost_begin = cost;
         bytes += g.M * g.row_bytes;
         cost += g.M * g.row_cost;
