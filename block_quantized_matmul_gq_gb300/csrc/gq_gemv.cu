@@ -210,12 +210,18 @@ constexpr int64_t kGroupCost = 576;
 // Balancing weight of a problem boundary inside a CTA's share: the CTA prepares that
 // problem's activations and synchronizes its warps before streaming it (~2 us per extra
 // problem in a clock-stamped trace of the TinyLLaMA and LLaMA-7B steps, where the CTAs
-// with four or five problems finished up to 12 us after those with one).
+// with four or five problems finished up to 12 us after those with one). Long rows (more
+// than one column group, one copy per row per stage) were slower per byte than their
+// weight said, the longest the most (LLaMA-7B down_proj, K = 11008: +19 %).
+//   Q8_0: kSegCost per boundary, kRowCopyCost more per column group of a long row.
+//   Q4_0 / Q4_K: kSegCost4 per boundary, and per column group of a row with g groups
+//   kLongRowCost4 * (g - 2) more (fitted to the per-CTA end times: TinyLLaMA K = 5632 and
+//   LLaMA-7B K = 11008 rows). Q8_0 rows have twice the chunks at the same K, and this form
+//   overweighted its K = 5632 rows (N = 2: 182.6 -> 190.7 us), so Q8_0 keeps the flat one.
 constexpr int64_t kSegCost = 65536;
-// Extra weight per column group of rows longer than one group, whose stages take one copy
-// per row instead of one for the whole tile. Measured against 0 / 512 / 768 / 1536 with the
-// segment weight: 256 was best on the TinyLLaMA Q4_0 step (93.0 -> 91.2 us at N = 1).
 constexpr int64_t kRowCopyCost = 256;
+constexpr int64_t kSegCost4 = 131072;
+constexpr int64_t kLongRowCost4 = 143;
 
 // First row (problem p, row r) whose weight begins at or after `cost`; (count, 0) = end.
 // Host side: the cuts of the CTA shares (GemvParams::cut_p / cut_r). Costs increase with
@@ -1421,8 +1427,11 @@ cudaError_t launch_stream(gq_type t, const MatProblem* probs, int count, int64_t
         g.C = static_cast<int32_t>(probs[i].K / wpc);
         g.row_bytes = static_cast<int64_t>(g.C) * cb;
         const int64_t groups = (g.C + kLanesPerRow - 1) / kLanesPerRow;
-        g.row_cost = g.row_bytes + (kGroupCost + (g.C > kLanesPerRow ? kRowCopyCost : 0)) * groups;
-        if (i > 0) cost += kSegCost;
+        g.row_cost = g.row_bytes +
+                     (t == GQ_TYPE_Q8_0
+                          ? (kGroupCost + (g.C > kLanesPerRow ? kRowCopyCost : 0)) * groups
+                          : (kGroupCost + kLongRowCost4 * std::max<int64_t>(0, groups - 2)) * groups);
+        if (i > 0) cost += t == GQ_TYPE_Q8_0 ? kSegCost : kSegCost4;
         g.cost_begin = cost;
         bytes += g.M * g.row_bytes;
         cost += g.M * g.row_cost;
