@@ -1002,13 +1002,16 @@ struct XtProb {
     int32_t x_aligned;     // X is 16-byte aligned: vector loads
 };
 constexpr int kXtChunksPerBlock = 1024;   // 4 per thread (256 threads)
+// A launch that would have fewer blocks than SMs takes 256 chunks per block (one per
+// thread) instead: more blocks, each one load latency long.
+constexpr int kXtChunksPerBlockSmall = 256;
 struct XtParams {
     int32_t count;
     int32_t n_tok;
     int* counters;
     int32_t n_counters;
     int32_t sums;        // append each super-step's 8 x kNPad block sums (Q4_K scaled form)
-    int32_t pad_;
+    int32_t chunks_per_block;   // kXtChunksPerBlock or kXtChunksPerBlockSmall
     XtProb p[GQ_MAX_BATCH];
 };
 
@@ -1045,8 +1048,8 @@ x_tiles_kernel(const __grid_constant__ XtParams P) {
     }
     const XtProb& pr = P.p[lo];
     const int64_t chunks = pr.K / kBK * kNPad * 8;
-    const int64_t first = static_cast<int64_t>(blockIdx.x - pr.block_begin) * kXtChunksPerBlock;
-    const int64_t last = min(chunks, first + kXtChunksPerBlock);
+    const int64_t first = static_cast<int64_t>(blockIdx.x - pr.block_begin) * P.chunks_per_block;
+    const int64_t last = min(chunks, first + P.chunks_per_block);
     // Every chunk of the thread is loaded before any is converted, so that all of them are
     // in flight at once: a launch for few problems (a handful of blocks) is then one load
     // latency long, not kXtPerThread of them.
@@ -1077,7 +1080,7 @@ x_tiles_kernel(const __grid_constant__ XtParams P) {
 #pragma unroll
     for (int i = 0; i < kXtPerThread; ++i) {
         const int64_t li = first + threadIdx.x + 256 * i;
-        if (li >= last) break;   // warp-uniform: chunk counts are multiples of 512
+        if (li >= last) break;   // block-uniform: chunk counts are multiples of 512
         const int c = static_cast<int>(li & 7);
         const int n = static_cast<int>((li >> 3) % kNPad);
         const int64_t ks = (li >> 3) / kNPad;
@@ -1208,7 +1211,11 @@ cudaError_t launch_x_tiles(const MatProblem* probs, int count, int64_t N, uint8_
     P.counters = reinterpret_cast<int*>(part + tc_part_bytes(kNPad));
     P.n_counters = kCounters;
     P.sums = sums ? 1 : 0;
-    (void)info;
+    int64_t big = 0;
+    for (int i = 0; i < count; ++i)
+        big += (probs[i].K / kBK * kNPad * 8 + kXtChunksPerBlock - 1) / kXtChunksPerBlock;
+    const int cpb = big < info->sm_count ? kXtChunksPerBlockSmall : kXtChunksPerBlock;
+    P.chunks_per_block = cpb;
     int64_t blocks = 0, off = 0;
     for (int i = 0; i < count; ++i) {
         P.p[i].X = probs[i].X;
@@ -1216,7 +1223,7 @@ cudaError_t launch_x_tiles(const MatProblem* probs, int count, int64_t N, uint8_
         P.p[i].K = probs[i].K;
         P.p[i].block_begin = static_cast<int32_t>(blocks);
         P.p[i].x_aligned = reinterpret_cast<uintptr_t>(probs[i].X) % 16 == 0 && probs[i].K % 4 == 0;
-        blocks += (probs[i].K / kBK * kNPad * 8 + kXtChunksPerBlock - 1) / kXtChunksPerBlock;
+        blocks += (probs[i].K / kBK * kNPad * 8 + cpb - 1) / cpb;
         off += probs[i].K / kSuperK * xt_superstep_bytes(kNPad, sums);
     }
     void* args[] = {&P};
